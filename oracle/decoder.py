@@ -1,0 +1,183 @@
+"""Stateful reference of the decode loop: append, attention, canary, tiers (oracle).
+
+Step order per decode step t, per layer l (readings of "EchoKV: watching a
+language model decide its own precision", section "How EchoKV works", where
+the step's K is written into K_ref "before being quantized into the paged
+cache", and "What happens to old blocks when a layer changes tier?"):
+
+  1. the new K enters the ring, then K and V enter the cache;
+  2. attention reads all cached tokens, the new one included;
+  3. on a firing step (t % period == 0) the canary measures delta_l.
+After all layers of a firing step the controller updates every layer's EMA
+and tier; the new tier governs pages allocated from step t+1 on.
+
+Cache bookkeeping (readings; the pages are silent on the open block):
+  * a page is allocated when a block's first token arrives; its K bits are
+    the layer's tier at that moment (admit-time bits) and never change;
+  * V is quantized per token as it arrives;
+  * K rows stay raw fp16 while the block is open and are quantized per
+    channel when the 16th token arrives (the block is "sealed"); attention
+    reads open rows as fp16.
+
+The state keeps the raw fp16 K/V of every token and derives codes on demand
+from the definitions in `quant`; nothing is cached that could drift.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import attention, canary, controller, pages, quant
+
+BLOCK = 16
+RING = 64
+
+
+class SeqState:
+    """Cache of one (layer, sequence) restricted to a list of KV heads."""
+
+    def __init__(self, n_heads: int, d: int, vbits: int):
+        self.k = np.zeros((0, n_heads, d), dtype=np.float16)
+        self.v = np.zeros((0, n_heads, d), dtype=np.float16)
+        self.kbits: list = []      # admit-time K bits per block
+        self.vbits = vbits
+
+    @property
+    def T(self) -> int:
+        return self.k.shape[0]
+
+    def append(self, k16: np.ndarray, v16: np.ndarray, tier: int):
+        k16 = np.asarray(k16, dtype=np.float16)
+        v16 = np.asarray(v16, dtype=np.float16)
+        for p in range(self.T, self.T + k16.shape[0]):
+            if p % BLOCK == 0:
+                self.kbits.append(int(tier))
+        self.k = np.concatenate([self.k, k16], axis=0)
+        self.v = np.concatenate([self.v, v16], axis=0)
+
+    def khat(self) -> np.ndarray:
+        """Stored K values [T, H, d] fp32: sealed blocks dequantized, open rows raw."""
+        out = self.k.astype(np.float32)
+        T = self.T
+        for j, kb in enumerate(self.kbits):
+            lo, hi = j * BLOCK, (j + 1) * BLOCK
+            if hi > T or kb == 16:
+                continue
+            q, s = quant.quantize(self.k[lo:hi], kb, axis=0)
+            out[lo:hi] = quant.dequantize(q, s, axis=0)
+        return out
+
+    def vhat(self) -> np.ndarray:
+        if self.vbits == 16:
+            return self.v.astype(np.float32)
+        q, s = quant.quantize(self.v, self.vbits, axis=2)
+        return quant.dequantize(q, s, axis=2)
+
+    def window(self) -> np.ndarray:
+        """The K_ref ring contents [n, H, d], oldest first (n = min(T, 64))."""
+        return self.k[max(0, self.T - RING):self.T]
+
+    def page_expect(self, j: int, h: int) -> dict:
+        """Expected bytes of the defined regions of page j, head index h."""
+        kb = self.kbits[j]
+        lo = j * BLOCK
+        hi = min(lo + BLOCK, self.T)
+        exp = {}
+        if hi - lo == BLOCK:
+            exp.update(pages.sealed_k_bytes(kb, self.k[lo:hi, h]))
+        exp.update(pages.v_rows_bytes(self.vbits, self.v[lo:hi, h]))
+        return exp
+
+
+def layer_windows(w, layer: int, step: int, device="cpu") -> list:
+    """Ring windows of every sequence after step `step`'s append: [Hkv, n_s, d] each.
+
+    Regenerated from the seeded draws: the newest n_s = min(T_s, 64) K's,
+    oldest first.
+    """
+    wins = []
+    for s in range(w.batch):
+        T = w.prefill[s] + step + 1
+        n_s = min(RING, T)
+        k, _ = w.prefill_kv(layer, [s], device=device, tok0=[T - n_s], n_tok=n_s)
+        wins.append(k[0].permute(1, 0, 2).cpu().numpy())
+    return wins
+
+
+class Trace:
+    """Controller history: tiers in effect at each step's append, deltas, EMAs."""
+
+    def __init__(self):
+        self.tiers = []       # tiers[t] = tier vector used by step t's appends
+        self.delta = {}       # step -> fp64 [L, 3]
+        self.ema = {}         # step -> fp32 [L, 3] after the update
+        self.after = {}       # step -> tiers after the update
+
+
+def controller_trace(w, n_steps: int, device="cpu") -> Trace:
+    """Run the canary + controller over all layers for steps 0..n_steps-1."""
+    ctl = controller.Controller(w.k_bits_init, w.alpha, w.tau)
+    tr = Trace()
+    for t in range(n_steps):
+        tr.tiers.append(list(ctl.tiers))
+        if not w.fires(t):
+            continue
+        deltas = np.zeros((w.num_layers, 3), dtype=np.float64)
+        for l in range(w.num_layers):
+            Q = w.step_q(l, t, 1, device=device)[:, 0].cpu().numpy()
+            deltas[l] = canary.layer_delta(Q, layer_windows(w, l, t, device))
+        tr.delta[t] = deltas
+        ctl.update(deltas.astype(np.float32))
+        tr.ema[t] = np.array(ctl.ema, dtype=np.float32)
+        tr.after[t] = list(ctl.tiers)
+    tr.tiers.append(list(ctl.tiers))
+    return tr
+
+
+class ReferenceRun:
+    """Attention and page contents for chosen layers, sequences and KV heads.
+
+    Tiers come from a `Trace` (the controller over all layers); K/V/Q are the
+    workload's seeded draws for the chosen coordinates only.
+    """
+
+    def __init__(self, w, trace: Trace, layers=None, seqs=None, heads=None, device="cpu"):
+        self.w = w
+        self.trace = trace
+        self.layers = list(range(w.num_layers)) if layers is None else list(layers)
+        self.seqs = list(range(w.batch)) if seqs is None else list(seqs)
+        self.heads = list(range(w.num_kv_heads)) if heads is None else list(heads)
+        self.device = device
+        self.state = {(l, s): SeqState(len(self.heads), w.head_dim, w.v_bits[l])
+                      for l in self.layers for s in self.seqs}
+        self.steps_done = 0
+
+    def prefill(self):
+        w = self.w
+        for l in self.layers:
+            for s in self.seqs:
+                k, v = w.prefill_kv(l, [s], device=self.device, n_tok=w.prefill[s])
+                k = k[0][:, self.heads].cpu().numpy()
+                v = v[0][:, self.heads].cpu().numpy()
+                self.state[(l, s)].append(k, v, w.k_bits_init[l])
+
+    def q_heads(self) -> list:
+        G = self.w.group
+        return [g * G + i for g in self.heads for i in range(G)]
+
+    def step(self) -> dict:
+        """Append step t's K/V and return {(l, s): o [len(heads)*G, d] fp64}."""
+        w, t = self.w, self.steps_done
+        tiers = self.trace.tiers[t]
+        out = {}
+        qh = self.q_heads()
+        for l in self.layers:
+            k, v = w.step_kv(l, t, 1, seqs=self.seqs, device=self.device)
+            q = w.step_q(l, t, 1, seqs=self.seqs, device=self.device)
+            for i, s in enumerate(self.seqs):
+                st = self.state[(l, s)]
+                st.append(k[i][:, self.heads].cpu().numpy(), v[i][:, self.heads].cpu().numpy(),
+                          tiers[l])
+                qs = q[i, 0][qh].cpu().numpy()
+                out[(l, s)] = attention.decode_attention(qs, st.khat(), st.vhat())
+        self.steps_done += 1
+        return out

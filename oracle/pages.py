@@ -1,0 +1,82 @@
+"""Byte layout of one cache page (oracle).
+
+A page holds 16 token slots of one (layer, sequence, KV head).  Its format is
+the pair (K bits, V bits); K bits are the layer's tier when the page was
+allocated ("already-allocated blocks are never modified", EchoKV page, "What
+happens to old blocks when a layer changes tier?"), V bits are the layer's
+fixed V width.  K is quantized per channel over the page's 16 tokens and V per
+token over the head's channels (Behavior-Guided KV-Cache Quantization page,
+"K/V Role-Aware Low-Bit Quantization": Key per channel, Value per token).
+
+Layout (our storage reading; the pages only say "packed low-bit storage"):
+
+    K part  kb < 16 : codes [16][d*kb/8]  then scales [d]  fp16 (per channel)
+            kb = 16 : raw fp16 [16][d]
+    V part  vb < 16 : codes [16][d*vb/8]  then scales [16] fp16 (per token)
+            vb = 16 : raw fp16 [16][d]
+    page  = K part || V part            (little-endian fp16)
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import quant
+
+BLOCK = 16
+
+
+def k_part_bytes(kb: int, d: int) -> int:
+    return BLOCK * d * 2 if kb == 16 else BLOCK * d * kb // 8 + 2 * d
+
+
+def v_part_bytes(vb: int, d: int) -> int:
+    return BLOCK * d * 2 if vb == 16 else BLOCK * d * vb // 8 + 2 * BLOCK
+
+
+def page_bytes(kb: int, vb: int, d: int) -> int:
+    return k_part_bytes(kb, d) + v_part_bytes(vb, d)
+
+
+def regions(kb: int, vb: int, d: int) -> dict:
+    """name -> (offset, row_bytes, rows) of each region of the page."""
+    r = {}
+    if kb == 16:
+        r["k_raw"] = (0, 2 * d, BLOCK)
+    else:
+        r["k_codes"] = (0, d * kb // 8, BLOCK)
+        r["k_scales"] = (BLOCK * d * kb // 8, 2 * d, 1)
+    o = k_part_bytes(kb, d)
+    if vb == 16:
+        r["v_raw"] = (o, 2 * d, BLOCK)
+    else:
+        r["v_codes"] = (o, d * vb // 8, BLOCK)
+        r["v_scales"] = (o + BLOCK * d * vb // 8, 2, BLOCK)
+    return r
+
+
+def sealed_k_bytes(kb: int, k16: np.ndarray) -> dict:
+    """Expected bytes of a full page's K part from its 16 raw fp16 rows [16, d]."""
+    k16 = np.asarray(k16, dtype=np.float16)
+    assert k16.shape[0] == BLOCK
+    if kb == 16:
+        return {"k_raw": k16.view(np.uint8).reshape(BLOCK, -1)}
+    q, s = quant.quantize(k16, kb, axis=0)          # one group per channel
+    return {"k_codes": quant.pack(q, kb), "k_scales": s.astype(np.float16).view(np.uint8)[None, :]}
+
+
+def v_rows_bytes(vb: int, v16: np.ndarray) -> dict:
+    """Expected bytes of V rows [n, d] (rows 0..n-1 of the page)."""
+    v16 = np.asarray(v16, dtype=np.float16)
+    if vb == 16:
+        return {"v_raw": v16.view(np.uint8).reshape(v16.shape[0], -1)}
+    q, s = quant.quantize(v16, vb, axis=1)          # one group per token
+    return {"v_codes": quant.pack(q, vb),
+            "v_scales": s.astype(np.float16).view(np.uint8).reshape(-1, 2)}
+
+
+def extract(page: np.ndarray, kb: int, vb: int, d: int, name: str, rows: int | None = None):
+    """Slice region `name` out of raw page bytes as [rows, row_bytes] uint8."""
+    off, rb, n = regions(kb, vb, d)[name]
+    if rows is None:
+        rows = n
+    return np.asarray(page, dtype=np.uint8)[off:off + rb * n].reshape(n, rb)[:rows]

@@ -1,0 +1,85 @@
+"""Symmetric uniform b-bit quantization and the packed code layout (oracle).
+
+Definition followed (the workloads' quantizer, the reading of "symmetric
+uniform quantization" on the KV-Kaizen page, "Three Non-Eviction Compression
+Axes", item 3, and of "symmetric INT4" / INT4-RoleAlign on the
+Behavior-Guided KV-Cache Quantization page, "K/V Role-Aware Low-Bit
+Quantization"):
+
+    qmax = 2**(b-1) - 1
+    m    = max |x_i|                       over the group (exact on fp16 values)
+    s    = fp16_rne( fp32(m) / fp32(qmax) ) the stored scale
+    q_i  = clamp( rne( fp32(x_i) / fp32(s) ), -qmax, +qmax ),  q_i = 0 if s == 0
+    xhat = fp32(q_i) * fp32(s)             (exact in fp32 for b <= 8)
+
+All divisions are IEEE fp32 correctly rounded (numpy float32 arithmetic),
+rne is round-half-to-even (numpy.rint), and the fp32 -> fp16 conversion is
+numpy's round-to-nearest-even.
+
+Stored code (our storage reading; the pages only say "packed low-bit
+storage"): u = q + 2**(b-1) (offset binary), b bits per element, elements
+packed along the channel axis least-significant-bits first: element c lives
+in byte (c*b)//8 at bit (c*b) % 8.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+F32 = np.float32
+F16 = np.float16
+
+
+def qmax(b: int) -> int:
+    if b not in (2, 4, 8):
+        raise ValueError(f"no integer quantizer for {b} bits")
+    return (1 << (b - 1)) - 1
+
+
+def quantize(x16: np.ndarray, b: int, axis: int):
+    """Quantize fp16 `x16` in groups along `axis` -> (q int16, s fp16 with `axis` removed)."""
+    x16 = np.asarray(x16)
+    if x16.dtype != F16:
+        raise TypeError("quantizer input must be fp16")
+    x = x16.astype(F32)
+    qm = F32(qmax(b))
+    m = np.max(np.abs(x), axis=axis, keepdims=True)
+    s32 = (m / qm).astype(F32)
+    s16 = s32.astype(F16)
+    sf = s16.astype(F32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = (x / sf).astype(F32)
+    q = np.clip(np.rint(r), -qm, qm)
+    q = np.where(sf == 0, F32(0), q)
+    return q.astype(np.int16), np.squeeze(s16, axis=axis)
+
+
+def dequantize(q: np.ndarray, s16: np.ndarray, axis: int) -> np.ndarray:
+    """xhat = fp32(q) * fp32(s), `s16` broadcast along `axis`."""
+    s = np.expand_dims(np.asarray(s16, dtype=F16).astype(F32), axis)
+    return (q.astype(F32) * s).astype(F32)
+
+
+def pack(q: np.ndarray, b: int) -> np.ndarray:
+    """Pack int codes along the last axis, offset binary, LSB first -> uint8."""
+    q = np.asarray(q, dtype=np.int64)
+    n = q.shape[-1]
+    if (n * b) % 8:
+        raise ValueError("row does not fill whole bytes")
+    u = q + (1 << (b - 1))
+    if np.any(u < 0) or np.any(u >= (1 << b)):
+        raise ValueError("code out of range")
+    out = np.zeros(q.shape[:-1] + (n * b // 8,), dtype=np.int64)
+    for c in range(n):
+        byte, bit = divmod(c * b, 8)
+        out[..., byte] |= u[..., c] << bit
+    return out.astype(np.uint8)
+
+
+def unpack(packed: np.ndarray, b: int, n: int) -> np.ndarray:
+    """Inverse of `pack`: uint8 rows -> int16 codes q."""
+    p = np.asarray(packed, dtype=np.int64)
+    q = np.zeros(p.shape[:-1] + (n,), dtype=np.int64)
+    for c in range(n):
+        byte, bit = divmod(c * b, 8)
+        q[..., c] = ((p[..., byte] >> bit) & ((1 << b) - 1)) - (1 << (b - 1))
+    return q.astype(np.int16)
