@@ -1,0 +1,208 @@
+/*
+ * ekv.h — C ABI of the mixed-precision quantized KV-cache decode library (GB300, sm_103a).
+ *
+ * The library keeps, per layer, a paged KV cache whose pages carry their own
+ * K bit-width (2, 4, 8 or 16 bits), an FP16 ring of each layer's newest 64 K
+ * vectors, and a per-layer tier controller.  It implements:
+ *
+ *   ekv_append       quantize-and-append of new K/V tokens into the paged cache
+ *   ekv_decode_attn  single-token GQA decode attention over the mixed-format pages
+ *   ekv_canary_kl    the canary: KL between FP16 attention over the ring and its
+ *                    2/4/8-bit quantize-dequantize copies
+ *   ekv_tier_update  EMA of the canary readings and lowest-bit-under-tau tier pick
+ *
+ * Sources of the operations (page title, section):
+ *   - "EchoKV: watching a language model decide its own precision":
+ *     "How EchoKV works" (ring written before quantization, tier vector routes
+ *     future K blocks), "Do we store the whole cache in FP16? — No." (64-key
+ *     FP16 ring, K only), "What happens to old blocks when a layer changes
+ *     tier?" (admit-time bits, forward-only), "Show the math" (KL, EMA, pick).
+ *   - "Behavior-Guided KV-Cache Quantization": "K/V Role-Aware Low-Bit
+ *     Quantization" (K per channel, V per token, symmetric), "Storage savings,
+ *     with a conditional speed trade-off" (packed low-bit storage, GQA head
+ *     mapping, decode kernels).
+ *   - "KV-Kaizen": "Three Non-Eviction Compression Axes" (symmetric uniform
+ *     quantization, b in {2,4,8,16}).
+ *
+ * Conventions for every entry point:
+ *   - Return value is an ekv_status; nothing throws across the ABI.
+ *   - "dev" pointers are CUDA device pointers, "host" pointers are host memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Work is enqueued asynchronously on it unless the comment says "syncs".
+ *   - Caller-owned buffers (Q, K, V, O, seq_slots, delta) must stay valid
+ *     until the enqueued work completes.  The library owns everything else.
+ *   - Errors found on the host (bad arguments) return at once and enqueue
+ *     nothing.  Errors found on the device (a page pool running empty, a
+ *     sequence growing past max_seq_len, a corrupt page entry) are recorded in
+ *     a device error word; ekv_sync returns and clears it.
+ *   - A handle is not thread-safe; calls on one handle must be serialized,
+ *     and the work of one layer must not run concurrently on two streams.
+ *   - Inputs must be finite fp16 values.
+ */
+#ifndef EKV_H
+#define EKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define EKV_API __attribute__((visibility("default")))
+#else
+#define EKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum ekv_status {
+  EKV_OK = 0,
+  EKV_EINVAL = 1,         /* invalid argument; nothing was enqueued                     */
+  EKV_ENOMEM = 2,         /* allocation failed, or a page pool ran empty on the device  */
+  EKV_ECUDA = 3,          /* a CUDA call or kernel launch failed                        */
+  EKV_ETIMEOUT = 4,       /* a bounded device-side wait gave up                         */
+  EKV_EUNSUPPORTED = 5,   /* valid request outside what this build implements           */
+  EKV_ESTATE = 6          /* device detected an inconsistent state (capacity, entries)  */
+} ekv_status;
+
+#define EKV_BLOCK_TOKENS 16 /* tokens per page                                          */
+#define EKV_RING_LEN 64     /* K vectors kept in each FP16 ring                          */
+
+/* Page formats: index = kcode * 4 + vcode, code 0..3 <-> 2, 4, 8, 16 bits. */
+#define EKV_NUM_FORMATS 16
+#define EKV_FORMAT(kbits_code, vbits_code) ((kbits_code) * 4 + (vbits_code))
+
+typedef struct ekv_cache ekv_cache;
+
+typedef struct ekv_config {
+  int32_t num_layers;
+  int32_t max_seqs;        /* sequence slots 0 .. max_seqs-1                           */
+  int32_t num_q_heads;     /* Hq; must be a multiple of num_kv_heads                   */
+  int32_t num_kv_heads;    /* Hkv; query head h reads KV head h / (Hq / Hkv)           */
+  int32_t head_dim;        /* 64 or 128                                                */
+  int32_t max_seq_len;     /* tokens per sequence per layer (sets the block-table width) */
+  int64_t pool_pages[EKV_NUM_FORMATS]; /* page capacity per format (0 = no pool)     */
+  float softmax_scale;     /* 0 -> 1/sqrt(head_dim)                                    */
+  float ema_alpha;         /* EMA weight of a new canary reading                        */
+  float tau;               /* divergence budget of the tier pick                        */
+  /* Device allocator.  NULL -> cudaMalloc/cudaFree.  Called only inside
+   * ekv_create/ekv_destroy. */
+  void* (*dev_alloc)(size_t bytes, void* ctx);
+  void (*dev_free)(void* ptr, void* ctx);
+  void* alloc_ctx;
+} ekv_config;
+
+/* Human-readable name of a status code (static string, never NULL). */
+EKV_API const char* ekv_status_string(int status);
+
+/* Bytes of one page of format (k_bits, v_bits) at head_dim d; -1 if invalid.
+ * Layout (one layer, one sequence, one KV head, 16 token slots):
+ *   K part  k_bits < 16: codes [16][d*k_bits/8], then per-channel scales [d] fp16
+ *           k_bits = 16: raw fp16 [16][d]
+ *   V part  v_bits < 16: codes [16][d*v_bits/8], then per-token scales [16] fp16
+ *           v_bits = 16: raw fp16 [16][d]
+ * Codes are offset binary (q + 2^(b-1)), packed along channels, least
+ * significant bits first: channel c sits in byte c*b/8 at bit (c*b)%8. */
+EKV_API int32_t ekv_page_bytes(int32_t k_bits, int32_t v_bits, int32_t head_dim);
+
+/* Create a cache.  k_bits_init[num_layers] (host): each layer's starting K tier
+ * (2, 4, 8 or 16).  v_bits[num_layers] (host): each layer's fixed V width.
+ * Allocates every pool, table, ring and scratch buffer up front and zeroes
+ * them; syncs the device.  *out receives the handle. */
+EKV_API int ekv_create(const ekv_config* cfg, const uint8_t* k_bits_init, const uint8_t* v_bits,
+               ekv_cache** out);
+
+/* Free everything ekv_create allocated (syncs the device).  NULL is a no-op. */
+EKV_API int ekv_destroy(ekv_cache* cache);
+
+/* Return every page of sequence slot `seq_slot` (all layers) to its pool and
+ * set its length to 0. */
+EKV_API int ekv_seq_reset(ekv_cache* cache, int32_t seq_slot, void* stream);
+
+/* Append n_new tokens to each listed sequence of one layer.
+ *   seq_slots [n_seqs] int32 dev — distinct slot ids
+ *   k, v      [n_seqs][n_new][Hkv][d] fp16 dev — the new tokens, in order
+ * Per token: the K vector enters the layer's FP16 ring; a page is allocated
+ * at the layer's current tier when the token opens a block (its K bits never
+ * change afterwards); V is quantized per token (absmax over d channels) into
+ * the page; K is kept raw in the block's staging rows until the 16th token
+ * seals the block, which quantizes each channel over the 16 tokens.
+ * Quantizer: s = fp16_rne(absmax / qmax) with qmax = 2^(b-1)-1,
+ * q = clamp(rne(x / s), -qmax, qmax) (q = 0 if s = 0).  n_new >= 1 (prefill
+ * in one call is allowed).  A pool running empty sets EKV_ENOMEM on the
+ * device; that sequence must then be reset. */
+EKV_API int ekv_append(ekv_cache* cache, int32_t layer, int32_t n_seqs, const int32_t* seq_slots,
+               int32_t n_new, const void* k, const void* v, void* stream);
+
+/* Decode attention of one layer.
+ *   q [n_seqs][Hq][d] fp16 dev;  o [n_seqs][Hq][d] fp16 dev (written)
+ * o_h = sum_t softmax_t(scale * q_h . khat_t) vhat_t over every cached token
+ * of the sequence, with KV head h / (Hq/Hkv); khat/vhat are the dequantized
+ * page values (raw fp16 for rows of a still-open block).  fp32 accumulation,
+ * split over the context with a log-sum-exp merge; o rounded to fp16 (RNE).
+ * A sequence with no tokens gets o = 0.  Requires Hq/Hkv <= 8. */
+EKV_API int ekv_decode_attn(ekv_cache* cache, int32_t layer, int32_t n_seqs, const int32_t* seq_slots,
+                    const void* q, void* o, void* stream);
+
+/* Canary of one layer: for every listed sequence and query head, the KL
+ * divergence KL(softmax(scale q W^T) || softmax(scale q quant_b(W)^T)) over
+ * the ring window W (the newest min(len, 64) K vectors, oldest first), for
+ * b = 2, 4, 8, where quant_b quantizes each channel over consecutive 16-row
+ * groups of W starting at the oldest row.  The mean over all n_seqs*Hq
+ * queries is stored as the layer's reading delta[layer][0..2] (internal) and,
+ * if delta_out (dev float[3]) is not NULL, copied there. */
+EKV_API int ekv_canary_kl(ekv_cache* cache, int32_t layer, int32_t n_seqs, const int32_t* seq_slots,
+                  const void* q, float* delta_out, void* stream);
+
+/* Controller update for every layer whose layer_mask entry is nonzero
+ * (layer_mask dev uint8[num_layers], NULL = all layers):
+ *   ema = first reading ? delta : (1-alpha)*ema + alpha*delta   (fp32, unfused)
+ *   tier = min{ b in {2,4,8} : ema_b < tau }, else 8.
+ * delta (dev float[num_layers][3]) NULL = the readings stored by ekv_canary_kl.
+ * freeze != 0 leaves every EMA and tier unchanged.  A new tier governs pages
+ * allocated by later appends only. */
+EKV_API int ekv_tier_update(ekv_cache* cache, const float* delta, const uint8_t* layer_mask,
+                    int32_t freeze, void* stream);
+
+/* Overwrite the tiers (host uint8[num_layers], each 2, 4, 8 or 16). */
+EKV_API int ekv_set_tiers(ekv_cache* cache, const uint8_t* tiers, void* stream);
+
+/* Controller state (syncs stream).  Any output pointer may be NULL.
+ *   tiers uint8[L], ema float[L][3], delta float[L][3], ema_valid int32[L] (host). */
+EKV_API int ekv_get_state(ekv_cache* cache, uint8_t* tiers, float* ema, float* delta,
+                  int32_t* ema_valid, void* stream);
+
+/* Length (tokens) of one (layer, slot) (syncs stream). */
+EKV_API int ekv_seq_len(ekv_cache* cache, int32_t layer, int32_t seq_slot, int32_t* out, void* stream);
+
+/* Page-table entries of one (layer, slot, kv_head), in block order (syncs stream).
+ * entry = (format << 28) | page index, -1 = no page.  Writes min(cap, blocks
+ * in use) entries to out (host) and the number of blocks in use to *n_out. */
+EKV_API int ekv_block_table(ekv_cache* cache, int32_t layer, int32_t seq_slot, int32_t kv_head,
+                    int32_t* out, int32_t cap, int32_t* n_out, void* stream);
+
+/* Copy the raw bytes of pages first_block .. first_block+n_blocks-1 of one
+ * (layer, slot, kv_head) into dst (dev), page i at dst + i*dst_stride
+ * (dst_stride >= the largest page size of the layer).  Blocks without a page
+ * are left untouched. */
+EKV_API int ekv_read_pages(ekv_cache* cache, int32_t layer, int32_t seq_slot, int32_t kv_head,
+                   int32_t first_block, int32_t n_blocks, void* dst, size_t dst_stride,
+                   void* stream);
+
+/* Free pages left in the pool of one format (syncs stream). */
+EKV_API int ekv_pool_free(ekv_cache* cache, int32_t format, int64_t* out, void* stream);
+
+/* Wait for the stream, then return and clear the device error word. */
+EKV_API int ekv_sync(ekv_cache* cache, void* stream);
+
+/* Controller checkpoint: tiers, EMA, EMA-valid flags, last readings.
+ * ekv_state_size gives the blob size; save/load sync the stream. */
+EKV_API int64_t ekv_state_size(ekv_cache* cache);
+EKV_API int ekv_state_save(ekv_cache* cache, void* host_blob, int64_t bytes, void* stream);
+EKV_API int ekv_state_load(ekv_cache* cache, const void* host_blob, int64_t bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EKV_H */

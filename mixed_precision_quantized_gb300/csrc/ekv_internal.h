@@ -1,0 +1,88 @@
+// ekv_internal.h — device-side state and helpers shared by the library's kernels.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ekv.h"
+
+namespace ekv {
+
+constexpr int BLOCK = EKV_BLOCK_TOKENS;  // tokens per page
+constexpr int RING = EKV_RING_LEN;       // K vectors per ring
+constexpr int NFMT = EKV_NUM_FORMATS;
+constexpr int MAX_G = 8;                  // query heads per KV head handled by one CTA
+
+__host__ __device__ inline int bits_of_code(int code) { return 2 << code; }
+__host__ __device__ inline int code_of_bits(int b) {
+  return b == 2 ? 0 : b == 4 ? 1 : b == 8 ? 2 : b == 16 ? 3 : -1;
+}
+__host__ __device__ inline int k_part_bytes(int kb, int d) {
+  return kb == 16 ? BLOCK * d * 2 : BLOCK * d * kb / 8 + 2 * d;
+}
+__host__ __device__ inline int v_part_bytes(int vb, int d) {
+  return vb == 16 ? BLOCK * d * 2 : BLOCK * d * vb / 8 + 2 * BLOCK;
+}
+__host__ __device__ inline int page_bytes(int kb, int vb, int d) {
+  return k_part_bytes(kb, d) + v_part_bytes(vb, d);
+}
+
+// Page entry: (format << 28) | index, -1 = none.
+__host__ __device__ inline int entry_fmt(int32_t e) { return (int)((uint32_t)e >> 28); }
+__host__ __device__ inline int entry_idx(int32_t e) { return e & 0x0FFFFFFF; }
+
+// Everything a kernel needs, passed by value.
+struct DevState {
+  int L, S, Hq, Hkv, D, G, maxblk;
+  float scale;       // softmax scale sigma
+  float scale_log2;  // sigma * log2(e)
+  float alpha, tau;
+  uint8_t* pool_base[NFMT];
+  int32_t pool_page_bytes[NFMT];
+  int32_t pool_cap[NFMT];
+  int32_t* stack[NFMT];     // free page indices
+  int32_t* top;             // [NFMT] free-stack heights
+  int32_t* len;             // [L][S]
+  int32_t* bt;              // [L][S][Hkv][maxblk]
+  __half* staging;          // [L][S][Hkv][16][D]  open-block K rows
+  __half* ring;             // [L][S][Hkv][64][D]  FP16 K_ref ring
+  int32_t* tier;            // [L] current K tier (bits)
+  int32_t* vbits;           // [L]
+  float* ema;               // [L][3]
+  int32_t* ema_valid;       // [L]
+  float* delta;             // [L][3] last canary readings
+  int32_t* err;             // device error word
+  int32_t* append_ticket;   // [L][S]
+  float* attn_acc;          // [parts][G][D]   split partial numerators
+  float* attn_ml;           // [parts][G][2]   split partial (max, sum), log2 domain
+  int32_t* attn_ticket;     // [S][Hkv]
+  int32_t attn_parts_cap;
+  float* canary_part;       // [S*Hkv][3]
+  int32_t* canary_ticket;   // [L]
+};
+
+__device__ inline void set_error(const DevState& st, int code) { atomicCAS(st.err, 0, code); }
+
+__host__ __device__ inline size_t ls_index(const DevState& st, int l, int s) {
+  return (size_t)l * st.S + s;
+}
+__host__ __device__ inline size_t lsh_index(const DevState& st, int l, int s, int h) {
+  return ((size_t)l * st.S + s) * st.Hkv + h;
+}
+
+// ---- launchers (defined in the kernel translation units) ----------------------
+cudaError_t launch_append(const DevState& st, int layer, int n_seqs, const int32_t* slots,
+                          int n_new, const __half* k, const __half* v, cudaStream_t s);
+cudaError_t launch_decode_attn(const DevState& st, int layer, int n_seqs, const int32_t* slots,
+                               const __half* q, __half* o, int splits, int vb, cudaStream_t s);
+cudaError_t launch_canary(const DevState& st, int layer, int n_seqs, const int32_t* slots,
+                          const __half* q, float* delta_out, cudaStream_t s);
+cudaError_t launch_tier_update(const DevState& st, const float* delta, const uint8_t* mask,
+                               int freeze, cudaStream_t s);
+cudaError_t launch_seq_reset(const DevState& st, int slot, cudaStream_t s);
+cudaError_t launch_read_pages(const DevState& st, int layer, int slot, int h, int first, int n,
+                              uint8_t* dst, size_t stride, cudaStream_t s);
+cudaError_t launch_init_stack(int32_t* stack, int32_t n, cudaStream_t s);
+
+}  // namespace ekv

@@ -40,6 +40,7 @@ class SeqState:
         self.v = np.zeros((0, n_heads, d), dtype=np.float16)
         self.kbits: list = []      # admit-time K bits per block
         self.vbits = vbits
+        self._sealed = {}          # block -> dequantized K of a sealed block (never changes)
 
     @property
     def T(self) -> int:
@@ -62,8 +63,10 @@ class SeqState:
             lo, hi = j * BLOCK, (j + 1) * BLOCK
             if hi > T or kb == 16:
                 continue
-            q, s = quant.quantize(self.k[lo:hi], kb, axis=0)
-            out[lo:hi] = quant.dequantize(q, s, axis=0)
+            if j not in self._sealed:
+                q, s = quant.quantize(self.k[lo:hi], kb, axis=0)
+                self._sealed[j] = quant.dequantize(q, s, axis=0)
+            out[lo:hi] = self._sealed[j]
         return out
 
     def vhat(self) -> np.ndarray:
@@ -164,20 +167,25 @@ class ReferenceRun:
         G = self.w.group
         return [g * G + i for g in self.heads for i in range(G)]
 
-    def step(self) -> dict:
-        """Append step t's K/V and return {(l, s): o [len(heads)*G, d] fp64}."""
+    def advance(self):
+        """Append decode step t's K/V for the chosen coordinates (no attention)."""
         w, t = self.w, self.steps_done
         tiers = self.trace.tiers[t]
-        out = {}
-        qh = self.q_heads()
         for l in self.layers:
             k, v = w.step_kv(l, t, 1, seqs=self.seqs, device=self.device)
-            q = w.step_q(l, t, 1, seqs=self.seqs, device=self.device)
             for i, s in enumerate(self.seqs):
-                st = self.state[(l, s)]
-                st.append(k[i][:, self.heads].cpu().numpy(), v[i][:, self.heads].cpu().numpy(),
-                          tiers[l])
-                qs = q[i, 0][qh].cpu().numpy()
-                out[(l, s)] = attention.decode_attention(qs, st.khat(), st.vhat())
+                self.state[(l, s)].append(k[i][:, self.heads].cpu().numpy(),
+                                          v[i][:, self.heads].cpu().numpy(), tiers[l])
         self.steps_done += 1
-        return out
+
+    def attend(self, l: int, s: int) -> np.ndarray:
+        """Attention of the last appended step for (l, s): o [len(heads)*G, d] fp64."""
+        t = self.steps_done - 1
+        q = self.w.step_q(l, t, 1, seqs=[s], device=self.device)[0, 0][self.q_heads()]
+        st = self.state[(l, s)]
+        return attention.decode_attention(q.cpu().numpy(), st.khat(), st.vhat())
+
+    def step(self) -> dict:
+        """Append step t's K/V and return {(l, s): o [len(heads)*G, d] fp64}."""
+        self.advance()
+        return {(l, s): self.attend(l, s) for l in self.layers for s in self.seqs}

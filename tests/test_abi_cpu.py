@@ -1,0 +1,67 @@
+"""The C-ABI library builds for sm_103a, loads, and exports every symbol
+include/ekv.h declares; host-only entry points agree with the oracle's byte
+accounting.  No GPU needed (no compute call is made)."""
+import os
+import re
+import shutil
+
+import pytest
+
+from conftest import ROOT
+from oracle import pages
+
+HEADER = os.path.join(ROOT, "include", "ekv.h")
+
+
+def declared_symbols():
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"EKV_API\s+[\w\s\*]+?\b(ekv_\w+)\s*\(", txt)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("no CUDA toolkit on this host")
+    from mixed_precision_quantized_gb300 import build, ekv
+    build.build()
+    return ekv.lib()
+
+
+def test_header_declares_the_hot_path():
+    syms = declared_symbols()
+    for s in ("ekv_append", "ekv_decode_attn", "ekv_canary_kl", "ekv_tier_update",
+              "ekv_block_table", "ekv_create", "ekv_destroy", "ekv_sync"):
+        assert s in syms
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from mixed_precision_quantized_gb300 import ekv
+    for s in declared_symbols():
+        assert hasattr(lib, s), s
+    assert sorted(ekv.EXPORTS) == declared_symbols()
+
+
+def test_page_bytes_matches_oracle_layout(lib):
+    for kb in (2, 4, 8, 16):
+        for vb in (2, 4, 8, 16):
+            for d in (64, 128):
+                assert lib.ekv_page_bytes(kb, vb, d) == pages.page_bytes(kb, vb, d)
+    assert lib.ekv_page_bytes(3, 4, 128) == -1
+    assert lib.ekv_page_bytes(4, 4, 96) == -1
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.ekv_status_string(code)
+    assert lib.ekv_status_string(99) == b"unknown status"
+
+
+def test_create_rejects_bad_config_without_gpu(lib):
+    import ctypes
+    from mixed_precision_quantized_gb300 import ekv
+    cfg = ekv.EkvConfig()
+    cfg.num_layers = 0
+    h = ctypes.c_void_p()
+    kb = (ctypes.c_uint8 * 1)(4)
+    assert lib.ekv_create(ctypes.byref(cfg), kb, kb, ctypes.byref(h)) == 1   # EINVAL
+    assert lib.ekv_create(None, kb, kb, ctypes.byref(h)) == 1

@@ -1,0 +1,192 @@
+"""CUDA path vs the oracle through the C ABI, at sizes the oracle finishes in
+seconds: every page byte, every attention output, every canary reading and
+every tier of the run."""
+import numpy as np
+import pytest
+import torch
+
+from mixed_precision_quantized_gb300 import build, ekv, workloads
+from oracle import controller, decoder
+
+from gpu_harness import Run
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    ekv.lib()
+
+
+def _full_run(w, steps, attn_steps=None):
+    r = Run(w, steps)
+    try:
+        for t in range(steps):
+            r.step(check_attn_now=attn_steps is None or t in attn_steps)
+        r.check_all_pages()
+        return r.max_err, r.flips
+    finally:
+        r.close()
+
+
+def test_tiny_config_brute_force():
+    """2 layers, d=64, K bits [4,8], V8, canary + controller every step."""
+    err, flips = _full_run(workloads.tiny(), 8)
+    assert flips == []
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8, 16])
+def test_llama8b_layer_small(bits):
+    """Uniform K=V bits, G=4, ragged prefill tail (300 = 18 blocks + 12), crosses a block."""
+    w = workloads.llama8b_layer(bits).scaled(batch=2, prefill=[300, 300], steps=6)
+    _full_run(w, 6)
+
+
+def test_qwen14b_mixed_small():
+    """G=5 (padding heads), per-layer K bits 2/4/8 mixed across layers, V4."""
+    w = workloads.qwen14b_32k()
+    w = w.scaled(num_layers=3, prefill=[1000], steps=4,
+                 k_bits_init=[2, 4, 8], v_bits=[4, 4, 4])
+    _full_run(w, 4)
+
+
+def test_llama70b_controller_small():
+    """Canary every 64 steps changes tiers mid-run: pages of several formats in one layer."""
+    w = workloads.llama70b_128k().scaled(num_layers=2, prefill=[700], steps=130)
+    err, flips = _full_run(w, 130, attn_steps={0, 1, 15, 63, 64, 65, 100, 127, 128, 129})
+
+
+def test_llama8b_batch_ragged_small():
+    """Ragged batch incl. a sequence shorter than the ring (37 tokens), tau 0.03."""
+    w = workloads.llama8b_batch32().scaled(num_layers=2, batch=4, prefill=[37, 300, 129, 64],
+                                           steps=70)
+    _full_run(w, 70, attn_steps={0, 1, 2, 26, 27, 28, 63, 64, 65, 69})
+
+
+@pytest.mark.parametrize("T0,d,Hq,Hkv", [(1, 64, 2, 2), (15, 128, 8, 1), (16, 64, 8, 8),
+                                         (17, 128, 16, 2), (33, 128, 40, 8)])
+def test_edge_lengths_and_groups(T0, d, Hq, Hkv):
+    """Single-token, 15/16/17-token prefills, G = 1, 2, 5, 8."""
+    w = workloads.Workload("edge", 9, 1, 1, Hq, Hkv, d, [T0], 20, [4], [8],
+                           outlier_frac=0.02, outlier_gain=8.0)
+    _full_run(w, 20)
+
+
+def test_mixed_formats_in_one_layer_forced_tiers():
+    """Tiers forced 2 -> 16 -> 8 -> 4 mid-run: one layer holds four K formats (V16)."""
+    w = workloads.Workload("mixed", 10, 1, 2, 8, 2, 128, [40, 23], 70, [2], [16])
+    sched = {0: 2, 10: 16, 30: 8, 50: 4}
+    tr = decoder.Trace()
+    cur = 2
+    for t in range(71):
+        cur = sched.get(t, cur)
+        tr.tiers.append([cur])
+    pools = {(kb, 16): 64 for kb in (2, 4, 8, 16)}
+    r = Run(w, 70, trace=tr, pool_pages=pools)
+    try:
+        for t in range(70):
+            if t in sched:
+                r.cache.set_tiers([sched[t]])
+            r.step()
+        r.check_all_pages()
+        assert set(r.ref.state[(0, 0)].kbits) == {2, 16, 8, 4}
+    finally:
+        r.close()
+
+
+def test_tier_update_bit_exact_with_injected_readings():
+    w = workloads.Workload("ctl", 11, 6, 1, 4, 2, 64, [16], 1, [4] * 6, [4] * 6, alpha=0.25,
+                           tau=0.05)
+    cache = ekv.cache_for(w)
+    try:
+        ctl = controller.Controller(w.k_bits_init, w.alpha, w.tau)
+        rng = np.random.default_rng(0)
+        for it in range(12):
+            d = rng.exponential(0.04, size=(6, 3)).astype(np.float32)
+            d[:, 0] *= 4
+            mask = np.ones(6, dtype=np.uint8)
+            if it % 3 == 2:
+                mask[rng.integers(0, 6, 2)] = 0
+            freeze = it == 7
+            dt = torch.from_numpy(d).cuda()
+            mt = torch.from_numpy(mask).cuda()
+            cache.tier_update(dt, mt, freeze=freeze)
+            ctl.update(d, mask=mask, freeze=freeze)
+            st = cache.state()
+            assert st["tiers"] == ctl.tiers
+            ema_gpu = np.array(st["ema"], dtype=np.float32)
+            for l in range(6):
+                if ctl.ema[l] is not None:
+                    assert np.array_equal(ema_gpu[l], ctl.ema[l])
+    finally:
+        cache.close()
+
+
+def test_state_save_load_round_trip():
+    w = workloads.tiny()
+    cache = ekv.cache_for(w)
+    try:
+        cache.tier_update(torch.tensor([[0.3, 0.01, 0.001], [0.2, 0.2, 0.001]], device="cuda"))
+        blob = cache.save_state()
+        s1 = cache.state()
+        cache.tier_update(torch.tensor([[0.0, 0.0, 0.0], [0.0, 0.0, 0.0]], device="cuda"))
+        assert cache.state()["tiers"] == [2, 2]
+        cache.load_state(blob)
+        assert cache.state() == s1
+    finally:
+        cache.close()
+
+
+def test_pool_exhaustion_reports_enomem_and_reset_returns_pages():
+    w = workloads.Workload("oom", 12, 1, 1, 4, 2, 64, [64], 1, [4], [4])
+    cache = ekv.Cache(1, 1, 4, 2, 64, 256, {(4, 4): 8}, [4], [4])
+    try:
+        slots = torch.zeros(1, dtype=torch.int32, device="cuda")
+        k, v = w.prefill_kv(0, [0], device="cuda", n_tok=64)   # 4 blocks x 2 heads = 8 pages
+        cache.append(0, slots, k, v)
+        cache.sync()
+        assert cache.pool_free(4, 4) == 0
+        k2, v2 = w.prefill_kv(0, [0], device="cuda", tok0=[64], n_tok=1)
+        cache.append(0, slots, k2, v2)
+        with pytest.raises(ekv.EkvError) as ei:
+            cache.sync()
+        assert ei.value.code == 2
+        cache.reset(0)
+        cache.sync()
+        assert cache.pool_free(4, 4) == 8
+        assert cache.seq_len(0, 0) == 0
+    finally:
+        cache.close()
+
+
+def test_invalid_arguments_rejected_on_host():
+    cache = ekv.Cache(1, 2, 4, 2, 64, 64, {(4, 4): 16}, [4], [4])
+    try:
+        slots = torch.zeros(1, dtype=torch.int32, device="cuda")
+        q = torch.zeros(1, 4, 64, dtype=torch.float16, device="cuda")
+        with pytest.raises(ekv.EkvError) as ei:
+            cache.decode_attn(5, slots, q)       # layer out of range
+        assert ei.value.code == 1
+        with pytest.raises(ekv.EkvError):
+            cache.reset(7)
+        # zero sequences is a no-op
+        cache.decode_attn(0, slots[:0], q[:0])
+        cache.sync()
+    finally:
+        cache.close()
+    with pytest.raises(ekv.EkvError) as ei:
+        ekv.Cache(1, 1, 32, 2, 64, 64, {}, [4], [4])   # G = 16 > 8
+    assert ei.value.code == 5
+
+
+def test_empty_sequence_attends_to_zero():
+    cache = ekv.Cache(1, 2, 4, 2, 64, 64, {(4, 4): 16}, [4], [4])
+    try:
+        slots = torch.tensor([1], dtype=torch.int32, device="cuda")
+        q = torch.randn(1, 4, 64, device="cuda").half()
+        o = cache.decode_attn(0, slots, q)
+        cache.sync()
+        assert torch.all(o == 0)
+    finally:
+        cache.close()
