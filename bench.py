@@ -1,0 +1,444 @@
+"""Decode-step benchmark of the mixed-precision quantized KV-cache path on GB300.
+
+One step = one decode token for every sequence through every layer: per layer
+append (ring write, V quantization, K staging/seal, page admission at the
+layer's tier) and decode attention over the whole cache; on every 64th step the
+canary runs for every layer and the controller updates the tiers.
+
+Default workload: Llama-3.1-70B shape, 80 layers, batch 1, 64 q / 8 kv heads,
+head_dim 128, 131072 cached tokens, K starting at INT4 with the canary every 64
+steps (tau 0.05, alpha 0.25), V INT4; synthetic N(0,1) inputs with one K
+outlier channel (x10) per head and K gain 1 + 0.05 * layer.  A step reads
+~12.3 GB of pages, far above the 129 MB L2, so no L2 flush is needed.
+
+Timed regions (all on one stream, CUDA events, synchronize + barrier on both
+sides, max over ranks):
+  A  K steps replayed as one CUDA graph                  -> value, ms_per_step
+  B  the next K steps, each attention launch bracketed by
+     timing events inside the graph                      -> roofline (attention)
+  E  the next K steps with a pinned-host -> device copy of the step's inputs
+     and a device -> pinned-host copy of every layer's output per step -> e2e
+The canary cost is timed separately (all layers' canary + one controller
+update, replayed as a graph) -> canary_us_per_firing.
+
+`--impl reference` times the CPU oracle on the same workload on a bounded
+sample (a few layers of one decode step), on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "quantized-KV decode attn HBM GB/s (% of peak), tokens/s; canary µs/firing"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=64)
+    p.add_argument("--warmup", type=int, default=4)
+    p.add_argument("--impl", default="ekv", choices=["ekv", "reference"])
+    p.add_argument("--workload", default="llama70b_128k")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-sample-layers", type=int, default=2)
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling during a timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+        time.sleep(1.0)
+        return self
+
+    def __exit__(self, *a):
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+
+    def summary(self):
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+                for n, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def attn_bytes_per_layer(cache, w, layer: int) -> float:
+    """Algorithmic bytes one decode-attention launch reads and writes for a layer."""
+    from mixed_precision_quantized_gb300 import ekv
+    d, Hkv, Hq = w.head_dim, w.num_kv_heads, w.num_q_heads
+    vb = w.v_bits[layer]
+    total = 0.0
+    for s in range(w.batch):
+        T = cache.seq_len(layer, s)
+        nopen = T % 16
+        for h in range(Hkv):
+            bt = cache.block_table(layer, s, h)
+            for j, e in enumerate(bt):
+                fmt = (e >> 28) & 15
+                kb = 2 << (fmt >> 2)
+                if nopen and j == len(bt) - 1:
+                    vrow = d * 2 if vb == 16 else d * vb // 8 + 2
+                    total += nopen * (2 * d + vrow)       # open rows: fp16 K + V row
+                else:
+                    total += ekv.page_bytes(kb, vb, d)
+                total += 4                                  # page-table entry
+        total += 2 * Hq * d * 2                             # Q in, O out
+    return total
+
+
+def cpu_baseline(w, sample_layers: int, device):
+    """Time the oracle (as it stands) on a bounded sample of one decode step."""
+    import numpy as np  # noqa: F401
+    from oracle import decoder
+    layers = list(range(min(sample_layers, w.num_layers)))
+    tr = decoder.Trace()
+    tr.tiers = [list(w.k_bits_init)] * (w.steps + 1)
+    ref = decoder.ReferenceRun(w, tr, layers=layers, device=device)
+    ref.prefill()
+    ref.advance()                      # step 0 (untimed: fills sealed-block memo)
+    for l in layers:
+        for s in ref.seqs:
+            ref.attend(l, s)
+    c0, t0 = time.process_time(), time.perf_counter()
+    ref.advance()                      # step 1, timed: append + attention
+    for l in layers:
+        for s in ref.seqs:
+            ref.attend(l, s)
+    wall = time.perf_counter() - t0
+    cpu = time.process_time() - c0
+    per_step = wall * w.num_layers / len(layers)
+    return {"value": w.batch / per_step, "unit": "tokens/s",
+            "cores": round(max(1.0, cpu / wall), 1), "kind": "oracle",
+            "sample": f"{len(layers)} of {w.num_layers} layers of one decode step at the full "
+                      f"context, all {w.batch} sequence(s) and heads; per-step time scaled by "
+                      f"{w.num_layers / len(layers):g}; wall {wall:.2f} s",
+            "host": os.uname().machine, "nproc": os.cpu_count()}
+
+
+def main():
+    a = parse()
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if a.impl == "ekv" else "gloo")
+    from mixed_precision_quantized_gb300 import workloads
+
+    w = workloads.by_name(a.workload)
+
+    if a.impl == "reference":
+        if rank != 0:
+            return
+        dev = "cuda:0" if torch.cuda.is_available() else "cpu"
+        cb = cpu_baseline(w, a.cpu_sample_layers, dev)
+        line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "tokens/s",
+                "n_gpus": 0, "steps": 1, "warmup": 1, "ms_per_step": 1e3 * w.batch / cb["value"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64", "data": "synthetic",
+                "config": {"workload": w.name}, "cpu_baseline": cb,
+                "e2e": {"value": cb["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    from mixed_precision_quantized_gb300 import build, ekv, runner
+
+    build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    K, W = a.steps, a.warmup
+    if W < 3:
+        raise SystemExit("at least 3 warm-up steps")
+    n_steps_total = W + (3 if not a.no_e2e else 2) * K
+    if n_steps_total > w.steps:
+        raise SystemExit(f"workload holds {w.steps} decode steps; asked for {n_steps_total}")
+
+    cache = ekv.cache_for(w, device=dev)
+    slots = torch.arange(w.batch, dtype=torch.int32, device=dev)
+    t0 = time.perf_counter()
+    runner.prefill(cache, w, slots, device=dev)
+    cache.sync()
+    prefill_s = time.perf_counter() - t0
+    inp = runner.Inputs(w, 0, W + 2 * K, device=dev)
+    L, B = w.num_layers, w.batch
+    out = torch.empty(L, B, w.num_q_heads, w.head_dim, dtype=torch.float16, device=dev)
+    outs = [out[l] for l in range(L)]
+
+    # warm-up (eager)
+    for i in range(W):
+        runner.decode_step(cache, w, slots, inp, i, outs, w.fires(i))
+    cache.sync()
+
+    stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream())
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        return g
+
+    # ---- A: K steps as one graph -------------------------------------------------
+    gA = capture(lambda: [runner.decode_step(cache, w, slots, inp, i, outs, w.fires(i))
+                          for i in range(W, W + K)])
+    launches = sum(2 * L + ((L + 1) if w.fires(i) else 0) for i in range(W, W + K))
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    clk = Clocks(local).__enter__()
+    if world > 1:
+        dist.barrier()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        gA.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    tA = ev0.elapsed_time(ev1) / 1e3
+    cache.sync()
+    fired_A = sum(1 for i in range(W, W + K) if w.fires(i))
+
+    # ---- B: next K steps, attention launches bracketed by timing events --------
+    try:
+        pairs = [(torch.cuda.Event(enable_timing=True, external=True),
+                  torch.cuda.Event(enable_timing=True, external=True)) for _ in range(K * L)]
+        external_ok = True
+    except TypeError:
+        pairs, external_ok = [], False
+
+    def steps_with_events():
+        for n, i in enumerate(range(W + K, W + 2 * K)):
+            for l in range(L):
+                q, k, v = inp.layer(l, i)
+                cache.append(l, slots, k, v)
+                if external_ok:
+                    pairs[n * L + l][0].record(stream)
+                cache.decode_attn(l, slots, q, outs[l])
+                if external_ok:
+                    pairs[n * L + l][1].record(stream)
+                if w.fires(i):
+                    cache.canary_kl(l, slots, q)
+            if w.fires(i):
+                cache.tier_update()
+
+    gB = capture(steps_with_events)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        gB.replay()
+    torch.cuda.synchronize()
+    cache.sync()
+    attn_ms = [p[0].elapsed_time(p[1]) for p in pairs] if external_ok else []
+    # algorithmic bytes per attention launch, at the state of region B's middle
+    layer_bytes = [attn_bytes_per_layer(cache, w, l) for l in range(L)]
+    bytes_per_launch = sum(layer_bytes) / L
+    attn_avg_s = (sum(attn_ms) / len(attn_ms) / 1e3) if attn_ms else None
+
+    # ---- canary: all layers + one controller update ----------------------------
+    q_last = [inp.layer(l, W + 2 * K - 1)[0] for l in range(L)]
+
+    def firing():
+        for l in range(L):
+            cache.canary_kl(l, slots, q_last[l])
+        cache.tier_update(freeze=True)
+
+    gC = capture(firing)
+    reps = 20
+    with torch.cuda.stream(stream):
+        gC.replay()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(reps):
+            gC.replay()
+        c1.record(stream)
+    torch.cuda.synchronize()
+    canary_us = c0.elapsed_time(c1) * 1e3 / reps
+
+    # ---- attention alone, all layers back to back (read-only, replayable) ------
+    def attn_only():
+        for l in range(L):
+            cache.decode_attn(l, slots, q_last[l], outs[l])
+
+    gD = capture(attn_only)
+    with torch.cuda.stream(stream):
+        gD.replay()
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        d0.record(stream)
+        for _ in range(5):
+            gD.replay()
+        d1.record(stream)
+    torch.cuda.synchronize()
+    attn_only_us = d0.elapsed_time(d1) * 1e3 / (5 * L)
+    if attn_avg_s is None:
+        attn_avg_s = attn_only_us * 1e-6
+
+    # ---- E: end to end with host buffers ------------------------------------------
+    e2e = None
+    if not a.no_e2e:
+        s0 = W + 2 * K
+        inpE = runner.Inputs(w, s0, K, device=dev)
+        per_step = [torch.cat([inpE.q[l][i].reshape(-1) for l in range(L)] +
+                              [inpE.k[l][i].reshape(-1) for l in range(L)] +
+                              [inpE.v[l][i].reshape(-1) for l in range(L)]) for i in range(K)]
+        host_in = torch.stack(per_step).cpu().pin_memory()
+        del per_step, inpE
+        nq, nkv = B * w.num_q_heads * w.head_dim, B * w.num_kv_heads * w.head_dim
+        dbuf = torch.empty(host_in.shape[1], dtype=torch.float16, device=dev)
+        qd = [dbuf[l * nq:(l + 1) * nq].view(B, w.num_q_heads, w.head_dim) for l in range(L)]
+        kd = [dbuf[L * nq + l * nkv:L * nq + (l + 1) * nkv].view(B, 1, w.num_kv_heads, w.head_dim)
+              for l in range(L)]
+        vd = [dbuf[L * (nq + nkv) + l * nkv:L * (nq + nkv) + (l + 1) * nkv]
+              .view(B, 1, w.num_kv_heads, w.head_dim) for l in range(L)]
+        host_out = torch.empty(K, *out.shape, dtype=torch.float16).pin_memory()
+
+        def e2e_steps():
+            for n in range(K):
+                i = s0 + n
+                dbuf.copy_(host_in[n], non_blocking=True)
+                for l in range(L):
+                    cache.append(l, slots, kd[l], vd[l])
+                    cache.decode_attn(l, slots, qd[l], outs[l])
+                    if w.fires(i):
+                        cache.canary_kl(l, slots, qd[l])
+                if w.fires(i):
+                    cache.tier_update()
+                host_out[n].copy_(out, non_blocking=True)
+
+        gE = capture(e2e_steps)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        with torch.cuda.stream(stream):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            gE.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        tE = e0.elapsed_time(e1) / 1e3
+        cache.sync()
+        if world > 1:
+            tt = torch.tensor([tE], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            tE = float(tt)
+        e2e = {"value": world * B * K / tE, "unit": "tokens/s",
+               "h2d_bytes_per_step": int(host_in.shape[1] * 2),
+               "d2h_bytes_per_step": int(out.numel() * 2)}
+
+    clk.__exit__(None, None, None)
+    if world > 1:
+        tt = torch.tensor([tA], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        tA = float(tt)
+
+    peak, peak_kind = peaks()
+    achieved = bytes_per_launch / attn_avg_s / 1e9 if attn_avg_s else None
+    step_bytes = sum(layer_bytes)
+    line = {
+        "metric": METRIC,
+        "value": world * B * K / tA,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": 1e3 * tA / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.num_layers} layers, batch {B}, "
+                               f"{w.num_q_heads} q / {w.num_kv_heads} kv heads, d {w.head_dim}, "
+                               f"{w.prefill[0] if len(set(w.prefill)) == 1 else 'ragged'} cached "
+                               f"tokens, K tier by canary every {w.canary_period} steps "
+                               f"(tau {w.tau}), V INT{w.v_bits[0]}",
+                   "l2": f"inputs larger than L2: {step_bytes / 1e9:.2f} GB of pages read per step",
+                   "parallelism": f"replicas x{world} (one sequence set per GPU)",
+                   "graph": "CUDA graph of the timed steps", "canary_fires_in_timed": fired_A},
+        "attn_hbm_gbs": achieved,
+        "attn_frac_of_8tbs": achieved / NOMINAL_HBM_GBS if achieved else None,
+        "step_hbm_gbs": step_bytes / (tA / K) / 1e9,
+        "canary_us_per_firing": canary_us,
+        "canary_overhead_frac_at_1_in_64": canary_us * 1e-6 / 64 / (tA / K),
+        "prefill_s": prefill_s,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak if achieved else None, "traffic": None,
+                     "kernel": "decode_attn_kernel", "peak_kind": peak_kind,
+                     "bytes_per_launch": bytes_per_launch,
+                     "avg_launch_us": attn_avg_s * 1e6 if attn_avg_s else None,
+                     "launches_timed": len(attn_ms),
+                     "timing": "events around each launch inside timed region B" if attn_ms
+                               else "attention-only graph (all layers back to back)",
+                     "attn_only_avg_us": attn_only_us},
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1:
+        try:
+            line["cpu_baseline"] = cpu_baseline(w, a.cpu_sample_layers, dev)
+        except Exception as ex:  # noqa: BLE001
+            line["cpu_baseline"] = {"value": None, "error": repr(ex)}
+    cache.close()
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

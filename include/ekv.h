@@ -176,7 +176,8 @@ EKV_API int ekv_get_state(ekv_cache* cache, uint8_t* tiers, float* ema, float* d
 EKV_API int ekv_seq_len(ekv_cache* cache, int32_t layer, int32_t seq_slot, int32_t* out, void* stream);
 
 /* Page-table entries of one (layer, slot, kv_head), in block order (syncs stream).
- * entry = (format << 28) | page index, -1 = no page.  Writes min(cap, blocks
+ * entry = (format << 28) | page index (negative as int32 for formats >= 8),
+ * -1 = no page.  Writes min(cap, blocks
  * in use) entries to out (host) and the number of blocks in use to *n_out. */
 EKV_API int ekv_block_table(ekv_cache* cache, int32_t layer, int32_t seq_slot, int32_t kv_head,
                     int32_t* out, int32_t cap, int32_t* n_out, void* stream);

@@ -186,7 +186,7 @@ append_kernel(DevState st, int layer, const int32_t* __restrict__ slots, int n_n
     __syncthreads();
     const int32_t e = s_entry;
     __half* stg = st.staging + lsh_index(st, layer, slot, h) * (BLOCK * D);
-    if (e >= 0) {
+    if (e != -1) {
       const int fmt = entry_fmt(e);
       const int kb = bits_of_code(fmt >> 2), vb = bits_of_code(fmt & 3);
       uint8_t* page = st.pool_base[fmt] + (size_t)entry_idx(e) * st.pool_page_bytes[fmt];
@@ -202,7 +202,7 @@ append_kernel(DevState st, int layer, const int32_t* __restrict__ slots, int n_n
               *reinterpret_cast<const uint4*>(kin + (size_t)(p - told) * in_row + 8 * cc);
         }
       }
-    } else if (e != -1 || j * BLOCK < told) {
+    } else if (j * BLOCK < told) {  // an existing block must have a page
       if (tid == 0) set_error(st, EKV_ESTATE);
     }
     // ring: the newest 64 K vectors, slot p % 64
@@ -234,7 +234,7 @@ __global__ void seq_reset_kernel(DevState st, int slot) {
   int32_t* bt = st.bt + lsh_index(st, l, slot, 0) * st.maxblk;
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
     const int32_t e = bt[i];
-    if (e < 0) continue;
+    if (e == -1) continue;
     const int fmt = entry_fmt(e);
     const int pos = atomicAdd(st.top + fmt, 1);
     if (pos < st.pool_cap[fmt]) st.stack[fmt][pos] = entry_idx(e);
@@ -253,7 +253,7 @@ __global__ void read_pages_kernel(DevState st, int layer, int slot, int h, int f
   const int i = blockIdx.x, j = first + i;
   if (j >= st.maxblk) return;
   const int32_t e = st.bt[lsh_index(st, layer, slot, h) * st.maxblk + j];
-  if (e < 0) return;
+  if (e == -1) return;
   const int fmt = entry_fmt(e);
   const uint8_t* page = st.pool_base[fmt] + (size_t)entry_idx(e) * st.pool_page_bytes[fmt];
   const int n16 = st.pool_page_bytes[fmt] / 16;

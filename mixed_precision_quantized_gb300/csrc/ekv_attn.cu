@@ -15,7 +15,7 @@
 // block the warp
 //   1. loads its slice of the page (codes + scales) with 128/64/32-bit loads,
 //   2. unpacks K codes to exact fp16 integers in registers (PRMT/LOP3/HFMA2)
-//      and folds the per-channel K scales into Q,
+//      and folds the per-channel K scales into Q as an fp16 hi + lo pair,
 //   3. S^T[16 tokens x 8 heads] = K . Q^T with mma.sync m16n8k16 (fp32 acc):
 //      the block's tokens are M, the GQA group (padded to 8) is N,
 //   4. runs the online softmax in the log2 domain, folds each token's V scale
@@ -251,7 +251,7 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
 
   for (int blk = b0 + warp; blk < b1; blk += NW) {
     const int32_t e = bt[blk];
-    if (e < 0) {
+    if (e == -1) {
       if (lane == 0) set_error(st, EKV_ESTATE);
       continue;
     }
@@ -266,28 +266,41 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
     const int kb = open ? 16 : kbp;
     const uint8_t* kbase = open ? reinterpret_cast<const uint8_t*>(stg) : page;
     const int krow = kb == 16 ? 2 * D : D * kb / 8;
-    uint32_t kwa[KW], kwb[KW], qs[KW];
+    uint32_t kwa[KW], kwb[KW];
     k_row_words<D>(kbase + (size_t)g * krow, kb, c, kwa);
     k_row_words<D>(kbase + (size_t)(g + 8) * krow, kb, c, kwb);
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
     if (kb < 16) {
+      // Fold the per-channel K scale into Q: q*s = hi + lo with hi = fp16(q*s) and
+      // lo = fp16(q*s - hi) from one fused multiply-add (the residual of a rounded
+      // fp16 product is itself an fp16 value).  Two MMAs against the exact integer
+      // codes keep the logits accurate to fp32 accumulation.
+      uint32_t qh[KW], ql[KW];
       const uint4* sp = reinterpret_cast<const uint4*>(page + BLOCK * D * kb / 8 + c * KCH * 2);
 #pragma unroll
       for (int i = 0; i < KW / 4; ++i) {
         const uint4 u = __ldg(sp + i);
-        qs[4 * i] = hmul2u(qw[4 * i], u.x);
-        qs[4 * i + 1] = hmul2u(qw[4 * i + 1], u.y);
-        qs[4 * i + 2] = hmul2u(qw[4 * i + 2], u.z);
-        qs[4 * i + 3] = hmul2u(qw[4 * i + 3], u.w);
+        const uint32_t sv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          qh[4 * i + x] = hmul2u(qw[4 * i + x], sv[x]);
+          ql[4 * i + x] = hfma2u(qw[4 * i + x], sv[x], qh[4 * i + x] ^ 0x80008000u);
+        }
       }
+#pragma unroll
+      for (int kk = 0; kk < NKS; ++kk)
+        mma16816(s, kwa[2 * kk], kwb[2 * kk], kwa[2 * kk + 1], kwb[2 * kk + 1], qh[2 * kk],
+                 qh[2 * kk + 1]);
+#pragma unroll
+      for (int kk = 0; kk < NKS; ++kk)
+        mma16816(s, kwa[2 * kk], kwb[2 * kk], kwa[2 * kk + 1], kwb[2 * kk + 1], ql[2 * kk],
+                 ql[2 * kk + 1]);
     } else {
 #pragma unroll
-      for (int i = 0; i < KW; ++i) qs[i] = qw[i];
+      for (int kk = 0; kk < NKS; ++kk)
+        mma16816(s, kwa[2 * kk], kwb[2 * kk], kwa[2 * kk + 1], kwb[2 * kk + 1], qw[2 * kk],
+                 qw[2 * kk + 1]);
     }
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int kk = 0; kk < NKS; ++kk)
-      mma16816(s, kwa[2 * kk], kwb[2 * kk], kwa[2 * kk + 1], kwb[2 * kk + 1], qs[2 * kk],
-               qs[2 * kk + 1]);
 
     // ---- online softmax (log2 domain) -----------------------------------------
     float x0 = s[0] * sl, x1 = s[1] * sl, x2 = s[2] * sl, x3 = s[3] * sl;

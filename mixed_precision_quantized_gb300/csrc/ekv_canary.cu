@@ -196,18 +196,24 @@ __global__ void tier_update_kernel(DevState st, const float* __restrict__ delta,
 
 }  // namespace
 
+cudaError_t canary_init() {
+  cudaError_t e = cudaFuncSetAttribute(canary_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)canary_smem_bytes<64>());
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(canary_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)canary_smem_bytes<128>());
+  return e;
+}
+
 cudaError_t launch_canary(const DevState& st, int layer, int n_seqs, const int32_t* slots,
                           const __half* q, float* delta_out, cudaStream_t s) {
   dim3 grid(st.Hkv, n_seqs);
-  if (st.D == 64) {
-    constexpr size_t sm = canary_smem_bytes<64>();
-    cudaFuncSetAttribute(canary_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    canary_kernel<64><<<grid, CANARY_THREADS, sm, s>>>(st, layer, slots, q, delta_out, n_seqs);
-  } else {
-    constexpr size_t sm = canary_smem_bytes<128>();
-    cudaFuncSetAttribute(canary_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    canary_kernel<128><<<grid, CANARY_THREADS, sm, s>>>(st, layer, slots, q, delta_out, n_seqs);
-  }
+  if (st.D == 64)
+    canary_kernel<64><<<grid, CANARY_THREADS, canary_smem_bytes<64>(), s>>>(st, layer, slots, q,
+                                                                           delta_out, n_seqs);
+  else
+    canary_kernel<128><<<grid, CANARY_THREADS, canary_smem_bytes<128>(), s>>>(st, layer, slots, q,
+                                                                             delta_out, n_seqs);
   return cudaGetLastError();
 }
 

@@ -167,7 +167,7 @@ int ekv_create(const ekv_config* cfg, const uint8_t* k_bits_init, const uint8_t*
     return EKV_ENOMEM;
   }
 
-  cudaError_t e = cudaSuccess;
+  cudaError_t e = canary_init();
   auto Z = [&](void* p, size_t bytes) {
     if (e == cudaSuccess) e = cudaMemset(p, 0, bytes);
   };

@@ -28,7 +28,8 @@ __host__ __device__ inline int page_bytes(int kb, int vb, int d) {
   return k_part_bytes(kb, d) + v_part_bytes(vb, d);
 }
 
-// Page entry: (format << 28) | index, -1 = none.
+// Page entry: (format << 28) | index, -1 = none.  Formats >= 8 make the int32
+// negative, so "no page" is tested as e == -1 (index < 2^28 - 1 never forms -1).
 __host__ __device__ inline int entry_fmt(int32_t e) { return (int)((uint32_t)e >> 28); }
 __host__ __device__ inline int entry_idx(int32_t e) { return e & 0x0FFFFFFF; }
 
@@ -76,6 +77,7 @@ cudaError_t launch_append(const DevState& st, int layer, int n_seqs, const int32
                           int n_new, const __half* k, const __half* v, cudaStream_t s);
 cudaError_t launch_decode_attn(const DevState& st, int layer, int n_seqs, const int32_t* slots,
                                const __half* q, __half* o, int splits, int vb, cudaStream_t s);
+cudaError_t canary_init();  // once per process, before any launch
 cudaError_t launch_canary(const DevState& st, int layer, int n_seqs, const int32_t* slots,
                           const __half* q, float* delta_out, cudaStream_t s);
 cudaError_t launch_tier_update(const DevState& st, const float* delta, const uint8_t* mask,

@@ -54,7 +54,7 @@ def check_pages(cache: ekv.Cache, ref: decoder.ReferenceRun, l: int, s: int, hea
         raw = cache.read_pages(l, s, h, 0, nb).cpu().numpy()
         for j in range(nb):
             e = bt[j]
-            assert e >= 0, f"no page for block {j}"
+            assert e != -1, f"no page for block {j}"
             fmt = (e >> 28) & 15
             kb, vb = 2 << (fmt >> 2), 2 << (fmt & 3)
             assert kb == st.kbits[j], f"layer {l} seq {s} block {j}: page K bits {kb} != {st.kbits[j]}"

