@@ -144,6 +144,34 @@ EKV_API int ekv_append(ekv_cache* cache, int32_t layer, int32_t n_seqs, const in
 EKV_API int ekv_decode_attn(ekv_cache* cache, int32_t layer, int32_t n_seqs, const int32_t* seq_slots,
                     const void* q, void* o, void* stream);
 
+/* Allocation-free decode attention.  The pages have no counterpart of this
+ * entry point; it exists for callers that cannot allocate device memory where
+ * they run attention (a process that reserves all device memory at start-up
+ * and forbids later cudaMalloc, or code that cannot reach the allocator the
+ * handle was created with).
+ * Same arguments, kernel, split schedule and results as ekv_decode_attn, but
+ * the split-K scratch (partial numerators, (max, sum) pairs and merge
+ * tickets) comes from one static device array of EKV_NOALLOC_SCRATCH_BYTES
+ * built into the library instead of the handle's scratch.  It calls no
+ * allocator.
+ *   - Limit: n_seqs * Hkv * splits * G * (d + 2) * 4 bytes of partials plus
+ *     n_seqs * Hkv * 4 bytes of tickets (each part 256-byte aligned) must fit
+ *     in EKV_NOALLOC_SCRATCH_BYTES; larger requests return EKV_EINVAL and
+ *     enqueue nothing.  splits is the split count ekv_decode_attn uses for
+ *     n_seqs on this handle.
+ *   - Every GPU that loads the library holds the array until the process
+ *     exits.  The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the array and it keeps the last call's contents; each
+ *     call clears the tickets it uses (cudaMemsetAsync on `stream`) before
+ *     launching.  Calls that overlap on the GPU race on the array: serialize
+ *     them. */
+#define EKV_NOALLOC_SCRATCH_BYTES (4u << 20)
+EKV_API int ekv_decode_attn_noalloc(ekv_cache* cache, int32_t layer, int32_t n_seqs,
+                                    const int32_t* seq_slots, const void* q, void* o,
+                                    void* stream);
+
 /* Canary of one layer: for every listed sequence and query head, the KL
  * divergence KL(softmax(scale q W^T) || softmax(scale q quant_b(W)^T)) over
  * the ring window W (the newest min(len, 64) K vectors, oldest first), for

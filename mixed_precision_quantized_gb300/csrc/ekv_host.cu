@@ -57,6 +57,16 @@ bool valid_bits(int b) { return b == 2 || b == 4 || b == 8 || b == 16; }
 
 }  // namespace
 
+namespace ekv {
+int attn_plan(ekv_cache* c, int layer, int n_seqs, DevState* st, int* splits, int* vb) {
+  if (!c || layer < 0 || layer >= c->st.L || n_seqs < 0 || n_seqs > c->st.S) return EKV_EINVAL;
+  *st = c->st;
+  *splits = attn_splits(c, n_seqs > 0 ? n_seqs : 1);
+  *vb = c->vbits[layer];
+  return EKV_OK;
+}
+}  // namespace ekv
+
 extern "C" {
 
 const char* ekv_status_string(int status) {

@@ -87,4 +87,8 @@ cudaError_t launch_read_pages(const DevState& st, int layer, int slot, int h, in
                               uint8_t* dst, size_t stride, cudaStream_t s);
 cudaError_t launch_init_stack(int32_t* stack, int32_t n, cudaStream_t s);
 
+// Argument checks and launch plan of decode attention for a handle: a copy of
+// its device state, the split count and the layer's V bits.
+int attn_plan(ekv_cache* c, int layer, int n_seqs, DevState* st, int* splits, int* vb);
+
 }  // namespace ekv

@@ -54,6 +54,7 @@ _SIGS = {
     "ekv_seq_reset": (ctypes.c_int, [_P, _I32, _P]),
     "ekv_append": (ctypes.c_int, [_P, _I32, _I32, _P, _I32, _P, _P, _P]),
     "ekv_decode_attn": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P, _P]),
+    "ekv_decode_attn_noalloc": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P, _P]),
     "ekv_canary_kl": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P, _P]),
     "ekv_tier_update": (ctypes.c_int, [_P, _P, _P, _I32, _P]),
     "ekv_set_tiers": (ctypes.c_int, [_P, _P, _P]),
@@ -183,6 +184,14 @@ class Cache:
             out = torch.empty_like(q)
         _check(lib().ekv_decode_attn(self._h, layer, seq_slots.numel(), _ptr(seq_slots), _ptr(q),
                                      _ptr(out), _stream(stream)), "ekv_decode_attn")
+        return out
+
+    def decode_attn_noalloc(self, layer: int, seq_slots: torch.Tensor, q: torch.Tensor,
+                            out: torch.Tensor, stream=None) -> torch.Tensor:
+        """Decode attention with the library's static scratch (no allocation at all)."""
+        _check(lib().ekv_decode_attn_noalloc(self._h, layer, seq_slots.numel(), _ptr(seq_slots),
+                                             _ptr(q), _ptr(out), _stream(stream)),
+               "ekv_decode_attn_noalloc")
         return out
 
     def canary_kl(self, layer: int, seq_slots: torch.Tensor, q: torch.Tensor,

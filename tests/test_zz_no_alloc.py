@@ -1,0 +1,91 @@
+"""ekv_decode_attn_noalloc: decode attention for callers that cannot allocate
+device memory where they run attention (a process that reserves all device
+memory up front, or code that cannot reach the handle's allocator).  Its
+split-K scratch lives in a static device array inside the library, so it
+must give the same outputs as ekv_decode_attn, call after call, and refuse
+requests whose scratch would not fit in that array.
+
+Called through the C ABI directly (ctypes), after the regular entry point has
+produced the reference output on the same cache state.  This file is named to
+be collected last."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from mixed_precision_quantized_gb300 import build, ekv, runner, workloads
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 2e-3, 1e-2
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _cache_after_one_step(w):
+    cache = ekv.cache_for(w)
+    slots = torch.arange(w.batch, dtype=torch.int32, device="cuda")
+    runner.prefill(cache, w, slots)
+    inp = runner.Inputs(w, 0, 1)
+    for l in range(w.num_layers):
+        _, k, v = inp.layer(l, 0)
+        cache.append(l, slots, k, v)
+    cache.sync()
+    return cache, slots, inp
+
+
+@pytest.mark.parametrize("w", [
+    workloads.llama8b_layer(4).scaled(batch=2, prefill=[300, 300], steps=1),
+    workloads.llama70b_128k().scaled(num_layers=1, prefill=[20000], steps=1),
+    workloads.tiny(),
+], ids=["batch2_int4", "one_seq_many_splits", "tiny_d64"])
+def test_noalloc_matches_decode_attn_on_two_calls(w):
+    build.build()
+    lib = ekv.lib()
+    cache, slots, inp = _cache_after_one_step(w)
+    try:
+        for l in range(w.num_layers):
+            q = inp.layer(l, 0)[0]
+            ref = torch.empty_like(q)
+            assert lib.ekv_decode_attn(cache.handle, l, w.batch, _ptr(slots), _ptr(q), _ptr(ref),
+                                       _stream()) == 0
+            cache.sync()
+            r = ref.float().cpu().numpy().astype(np.float64)
+            for call in range(2):
+                o = torch.full_like(q, float("nan"))
+                rc = lib.ekv_decode_attn_noalloc(cache.handle, l, w.batch, _ptr(slots), _ptr(q),
+                                                 _ptr(o), _stream())
+                assert rc == 0, lib.ekv_status_string(rc)
+                cache.sync()
+                g = o.float().cpu().numpy().astype(np.float64)
+                assert np.all(np.isfinite(g)), f"layer {l} call {call}: unwritten outputs"
+                assert np.all(np.abs(g - r) <= ATOL + RTOL * np.abs(r)), (
+                    f"layer {l} call {call}: max diff {np.abs(g - r).max():.3e}")
+    finally:
+        cache.close()
+
+
+def test_noalloc_rejects_requests_beyond_its_scratch():
+    build.build()
+    lib = ekv.lib()
+    # 128 sequences x 8 KV heads x group 8 x d 128: the partials alone exceed 4 MiB.
+    cache = ekv.Cache(1, 128, 64, 8, 128, 16, {}, [4], [4])
+    try:
+        slots = torch.arange(128, dtype=torch.int32, device="cuda")
+        q = torch.zeros(128, 64, 128, dtype=torch.float16, device="cuda")
+        o = torch.zeros_like(q)
+        assert lib.ekv_decode_attn_noalloc(cache.handle, 0, 128, _ptr(slots), _ptr(q), _ptr(o),
+                                           _stream()) == 1          # EKV_EINVAL
+        cache.sync()                                                  # nothing was enqueued
+        assert lib.ekv_decode_attn_noalloc(cache.handle, 0, 2, _ptr(slots), _ptr(q), _ptr(o),
+                                           _stream()) == 0          # small request still fits
+        cache.sync()
+    finally:
+        cache.close()
