@@ -52,6 +52,9 @@ def parse():
     p.add_argument("--workload", default="llama70b_128k")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-sample-layers", type=int, default=2)
+    p.add_argument("--layers", type=int, default=0,
+                   help="run only the first N layers of the workload (profiling cases)")
+    p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     return p.parse_args()
 
 
@@ -179,6 +182,8 @@ def main():
     from mixed_precision_quantized_gb300 import workloads
 
     w = workloads.by_name(a.workload)
+    if a.layers:
+        w = w.scaled(num_layers=a.layers)
 
     if a.impl == "reference":
         if rank != 0:
@@ -428,7 +433,7 @@ def main():
         "gpu_launches": launches,
         "clocks": clk.summary(),
     }
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and not a.no_cpu:
         try:
             line["cpu_baseline"] = cpu_baseline(w, a.cpu_sample_layers, dev)
         except Exception as ex:  # noqa: BLE001

@@ -176,6 +176,7 @@ append_kernel(DevState st, int layer, const int32_t* __restrict__ slots, int n_n
           e = -1;
         } else {
           e = (int32_t)(((uint32_t)fmt << 28) | (uint32_t)st.stack[fmt][old - 1]);
+          atomicMax(st.kmax + layer, st.tier[layer]);
         }
         *btp = e;
       } else {

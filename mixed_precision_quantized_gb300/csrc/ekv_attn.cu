@@ -11,19 +11,22 @@
 // conditional speed trade-off").
 //
 // Work split: grid (split, kv_head, seq).  A split owns a contiguous range of
-// 16-token blocks; each warp of the CTA walks every NW-th block of it.  Per
-// block the warp
-//   1. loads its slice of the page (codes + scales) with 128/64/32-bit loads,
-//   2. unpacks K codes to exact fp16 integers in registers (PRMT/LOP3/HFMA2)
+// 16-token blocks; warp w of the CTA takes every NW-th block of it.  Each warp
+// runs its own pipeline of shared-memory stages: lane 0 issues one TMA bulk
+// copy (cp.async.bulk, completion counted on the stage's mbarrier) per page,
+// `ns` pages ahead of the page being computed, so the warp's HBM requests stay
+// in flight while it computes.  Per page the warp
+//   1. unpacks K codes to exact fp16 integers in registers (PRMT/LOP3/HFMA2)
 //      and folds the per-channel K scales into Q as an fp16 hi + lo pair,
-//   3. S^T[16 tokens x 8 heads] = K . Q^T with mma.sync m16n8k16 (fp32 acc):
-//      the block's tokens are M, the GQA group (padded to 8) is N,
-//   4. runs the online softmax in the log2 domain, folds each token's V scale
+//   2. S^T[16 tokens x 8 heads] = K . Q^T with mma.sync m16n8k16 (fp32 acc):
+//      the page's tokens are M, the GQA group (padded to 8) is N,
+//   3. runs the online softmax in the log2 domain, folds each token's V scale
 //      into its probability and transposes P with movmatrix,
-//   5. O^T[d x 8] += V^T . P^T with mma.sync (channels are M, tokens K).
-// Warps merge in shared memory; splits write (max, sum, numerator) partials and
-// the last CTA of a (sequence, KV head) — found with an atomic ticket, no
-// waiting — merges them by log-sum-exp and writes fp16 O.
+//   4. O^T[d x 8] += V^T . P^T with mma.sync (channels are M, tokens K).
+// The still-open last block (raw fp16 K rows in the staging buffer) is read
+// straight from global memory.  Warps merge in shared memory; splits write
+// (max, sum, numerator) partials and the last CTA of a (sequence, KV head) —
+// found with an atomic ticket, no waiting — merges them by log-sum-exp.
 #include <math_constants.h>
 
 #include "ekv_internal.h"
@@ -33,6 +36,17 @@ namespace {
 
 constexpr int NW = 4;  // warps per CTA
 constexpr int NT = NW * 32;
+constexpr int NSMAX = 8;                 // stages per warp at most
+// Resident CTAs per SM and dynamic shared memory per CTA.  Quantized V: 4 CTAs
+// (16 warps, registers capped at 128) with 54 KB each.  FP16 V pages are 3.5x
+// larger and need more registers: 3 CTAs with 72 KB each.
+template <int VB>
+struct AttnCfg {
+  static constexpr int CTAS = VB == 16 ? 3 : 4;
+  static constexpr int SMEM = VB == 16 ? 72 * 1024 : 54 * 1024;
+  static constexpr int WARP_BYTES = SMEM / NW;
+};
+constexpr int WAIT_LIMIT = 1 << 22;      // bounded mbarrier polls before giving up
 
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
@@ -41,15 +55,11 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t
 }
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
-
 __device__ __forceinline__ uint32_t hsub2u(uint32_t a, uint32_t b) {
   return h2u(__hsub2(u2h(a), u2h(b)));
 }
 __device__ __forceinline__ uint32_t hfma2u(uint32_t a, uint32_t b, uint32_t c) {
   return h2u(__hfma2(u2h(a), u2h(b), u2h(c)));
-}
-__device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
-  return h2u(__hmul2(u2h(a), u2h(b)));
 }
 
 // fp16 bit patterns of constants (exact)
@@ -60,33 +70,105 @@ constexpr uint32_t H_MAGIC = 0x64006400u;  // 1024, 1024 exponent pattern
 
 __device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 __device__ __forceinline__ uint32_t movtrans(uint32_t x) {
   uint32_t y;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
   return y;
 }
 
-// ---- K: one row's chunk of KCH = D/4 channels -> KW = KCH/2 half2 words ------
-// Word w holds channels (2w, 2w+1) of the chunk as exact fp16 integers q
-// (or raw fp16 for 16-bit pages and open-block staging rows).
-template <int D>
-__device__ __forceinline__ void k_row_words(const uint8_t* row, int kb, int c, uint32_t* kw) {
+// 2^x with one MUFU op (flushes results below 2^-126 to zero; inputs are
+// max-subtracted logits, so the largest term is exactly 1).
+__device__ __forceinline__ float fexp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ---- mbarrier + TMA bulk copy -----------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+// Poll the stage barrier for the given phase; false if the bound ran out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (int i = 0; i < WAIT_LIMIT; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; "
+        "selp.u32 %0, 1, 0, p; }"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+// ---- loads from global (open block) or shared memory (pipelined pages) ------------
+struct GLd {
+  const uint8_t* p;
+  __device__ __forceinline__ uint4 v4(int o) const {
+    return __ldg(reinterpret_cast<const uint4*>(p + o));
+  }
+  __device__ __forceinline__ uint2 v2(int o) const {
+    return __ldg(reinterpret_cast<const uint2*>(p + o));
+  }
+  __device__ __forceinline__ uint32_t v1(int o) const {
+    return __ldg(reinterpret_cast<const uint32_t*>(p + o));
+  }
+  __device__ __forceinline__ uint32_t h1(int o) const {
+    return __ldg(reinterpret_cast<const uint16_t*>(p + o));
+  }
+};
+// Shared-memory loads through a pointer into the dynamic shared array: ordinary
+// loads the compiler may schedule freely after the stage's mbarrier wait (whose
+// asm carries a memory clobber, so no load is hoisted above it).
+struct SLd {
+  const uint8_t* p;
+  __device__ __forceinline__ uint4 v4(int o) const {
+    return *reinterpret_cast<const uint4*>(p + o);
+  }
+  __device__ __forceinline__ uint2 v2(int o) const {
+    return *reinterpret_cast<const uint2*>(p + o);
+  }
+  __device__ __forceinline__ uint32_t v1(int o) const {
+    return *reinterpret_cast<const uint32_t*>(p + o);
+  }
+  __device__ __forceinline__ uint32_t h1(int o) const {
+    return *reinterpret_cast<const uint16_t*>(p + o);
+  }
+};
+
+// ---- K: one row's chunk of KCH = D/4 channels -> KW = KCH/2 half2 words -----------
+// Word w holds channels (2w, 2w+1) of the chunk as exact fp16 integers q (or raw
+// fp16 for 16-bit pages and open-block staging rows).  `row` is the row's offset.
+template <int D, int KB, class LD>
+__device__ __forceinline__ void k_row_words(const LD& ld, int row, int c, uint32_t* kw) {
   constexpr int KCH = D / 4;
   constexpr int KW = KCH / 2;
-  if (kb == 4) {
+  if constexpr (KB == 4) {
     constexpr int NB = KCH / 2;  // bytes
     uint32_t r[NB / 4];
     if constexpr (NB == 16) {
-      const uint4 u = __ldg(reinterpret_cast<const uint4*>(row + c * NB));
+      const uint4 u = ld.v4(row + c * NB);
       r[0] = u.x; r[1] = u.y; r[2] = u.z; r[3] = u.w;
     } else {
-      const uint2 u = __ldg(reinterpret_cast<const uint2*>(row + c * NB));
+      const uint2 u = ld.v2(row + c * NB);
       r[0] = u.x; r[1] = u.y;
     }
     const uint32_t mul = 0x2C003C00u;  // (1, 1/16)
@@ -98,14 +180,14 @@ __device__ __forceinline__ void k_row_words(const uint8_t* row, int kb, int c, u
         const uint32_t t = __byte_perm(r[i], 0, b * 0x1111);
         kw[4 * i + b] = hfma2u(lop3_and_or(t, 0x00F0000Fu, H_MAGIC), mul, add);
       }
-  } else if (kb == 2) {
+  } else if constexpr (KB == 2) {
     constexpr int NB = KCH / 4;
     uint32_t r[NB / 4];
     if constexpr (NB == 8) {
-      const uint2 u = __ldg(reinterpret_cast<const uint2*>(row + c * NB));
+      const uint2 u = ld.v2(row + c * NB);
       r[0] = u.x; r[1] = u.y;
     } else {
-      r[0] = __ldg(reinterpret_cast<const uint32_t*>(row + c * NB));
+      r[0] = ld.v1(row + c * NB);
     }
     const uint32_t mul_lo = 0x34003C00u;  // (1, 1/4)
     const uint32_t add_lo = 0xDC08E402u;  // (-1026, -258)
@@ -119,11 +201,11 @@ __device__ __forceinline__ void k_row_words(const uint8_t* row, int kb, int c, u
         kw[8 * i + 2 * b] = hfma2u(lop3_and_or(t, 0x000C0003u, H_MAGIC), mul_lo, add_lo);
         kw[8 * i + 2 * b + 1] = hfma2u(lop3_and_or(t, 0x00C00030u, H_MAGIC), mul_hi, add_hi);
       }
-  } else if (kb == 8) {
+  } else if constexpr (KB == 8) {
     constexpr int NB = KCH;
 #pragma unroll
     for (int i = 0; i < NB / 16; ++i) {
-      const uint4 u = __ldg(reinterpret_cast<const uint4*>(row + c * NB) + i);
+      const uint4 u = ld.v4(row + c * NB + 16 * i);
       const uint32_t r[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int x = 0; x < 4; ++x) {
@@ -134,35 +216,33 @@ __device__ __forceinline__ void k_row_words(const uint8_t* row, int kb, int c, u
   } else {  // raw fp16
 #pragma unroll
     for (int i = 0; i < KW / 4; ++i) {
-      const uint4 u = __ldg(reinterpret_cast<const uint4*>(row + c * KCH * 2) + i);
+      const uint4 u = ld.v4(row + c * KCH * 2 + 16 * i);
       kw[4 * i] = u.x; kw[4 * i + 1] = u.y; kw[4 * i + 2] = u.z; kw[4 * i + 3] = u.w;
     }
   }
 }
 
-// ---- V: token pair (t, t+1), chunk of VCH = D/8 channels -> VCH words -------
+// ---- V: token pair (t, t+1), chunk of VCH = D/8 channels -> VCH words -------------
 // Word i = (v[t][ch i], v[t+1][ch i]) as exact fp16 integers (raw for 16 bits).
-template <int D, int VB>
-__device__ __forceinline__ void v_pair_words(const uint8_t* r0, const uint8_t* r1, uint32_t* vw) {
+template <int D, int VB, class LD>
+__device__ __forceinline__ void v_pair_words(const LD& ld, int r0, int r1, uint32_t* vw) {
   constexpr int VCH = D / 8;
   constexpr int NB = VCH * VB / 8;  // bytes per row chunk
   constexpr int NWD = NB >= 4 ? NB / 4 : 1;
   uint32_t a[NWD], b[NWD];
   if constexpr (NB == 2) {
-    a[0] = __ldg(reinterpret_cast<const uint16_t*>(r0));
-    b[0] = __ldg(reinterpret_cast<const uint16_t*>(r1));
+    a[0] = ld.h1(r0);
+    b[0] = ld.h1(r1);
   } else if constexpr (NB == 4) {
-    a[0] = __ldg(reinterpret_cast<const uint32_t*>(r0));
-    b[0] = __ldg(reinterpret_cast<const uint32_t*>(r1));
+    a[0] = ld.v1(r0);
+    b[0] = ld.v1(r1);
   } else if constexpr (NB == 8) {
-    const uint2 x = __ldg(reinterpret_cast<const uint2*>(r0));
-    const uint2 y = __ldg(reinterpret_cast<const uint2*>(r1));
+    const uint2 x = ld.v2(r0), y = ld.v2(r1);
     a[0] = x.x; a[1] = x.y; b[0] = y.x; b[1] = y.y;
   } else {
 #pragma unroll
     for (int i = 0; i < NB / 16; ++i) {
-      const uint4 x = __ldg(reinterpret_cast<const uint4*>(r0) + i);
-      const uint4 y = __ldg(reinterpret_cast<const uint4*>(r1) + i);
+      const uint4 x = ld.v4(r0 + 16 * i), y = ld.v4(r1 + 16 * i);
       a[4 * i] = x.x; a[4 * i + 1] = x.y; a[4 * i + 2] = x.z; a[4 * i + 3] = x.w;
       b[4 * i] = y.x; b[4 * i + 1] = y.y; b[4 * i + 2] = y.z; b[4 * i + 3] = y.w;
     }
@@ -206,13 +286,179 @@ __device__ __forceinline__ void v_pair_words(const uint8_t* r0, const uint8_t* r
   }
 }
 
+// Online-softmax state of one warp (per thread: heads 2c, 2c+1 of the group).
+template <int D>
+struct Acc {
+  float o[D / 16][4];
+  float m0, m1, l0, l1;
+};
+
+// S^T[16 tokens x 8 heads] of one page into s[4] (C fragment: tokens g, g+8 x
+// heads 2c, 2c+1).  KB bits (raw fp16 if 16); the K part is read through kl.
+template <int D, int KB, class KL>
+__device__ __forceinline__ void page_scores(const KL& kl, const uint32_t* qw, float* s, int g,
+                                            int c) {
+  constexpr int KCH = D / 4, KW = KCH / 2, NKS = D / 16;
+  constexpr int krow = KB == 16 ? 2 * D : D * KB / 8;
+  uint32_t kwa[KW], kwb[KW];
+  k_row_words<D, KB>(kl, g * krow, c, kwa);
+  k_row_words<D, KB>(kl, (g + 8) * krow, c, kwb);
+  float s1[4] = {0.f, 0.f, 0.f, 0.f};
+  s[0] = s[1] = s[2] = s[3] = 0.f;
+  if constexpr (KB < 16) {
+    // Fold the per-channel K scale into Q: q*s = hi + lo with hi = fp16(q*s) and
+    // lo = fp16(q*s - hi) from one fused multiply-add (the residual of a rounded
+    // fp16 product is itself an fp16 value).  Two MMA chains against the exact
+    // integer codes keep the logits accurate to fp32 accumulation.
+    uint32_t qh[KW], ql[KW];
+    const int so = BLOCK * D * KB / 8 + c * KCH * 2;
+#pragma unroll
+    for (int i = 0; i < KW / 4; ++i) {
+      const uint4 u = kl.v4(so + 16 * i);
+      const uint32_t sv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const __half2 hi = __hmul2(u2h(qw[4 * i + x]), u2h(sv[x]));
+        qh[4 * i + x] = h2u(hi);
+        ql[4 * i + x] = h2u(__hfma2(u2h(qw[4 * i + x]), u2h(sv[x]), __hneg2(hi)));
+      }
+    }
+#pragma unroll
+    for (int kk = 0; kk < NKS; ++kk) {
+      mma16816(s, kwa[2 * kk], kwb[2 * kk], kwa[2 * kk + 1], kwb[2 * kk + 1], qh[2 * kk],
+               qh[2 * kk + 1]);
+      mma16816(s1, kwa[2 * kk], kwb[2 * kk], kwa[2 * kk + 1], kwb[2 * kk + 1], ql[2 * kk],
+               ql[2 * kk + 1]);
+    }
+  } else {
+#pragma unroll
+    for (int kk = 0; kk < NKS; kk += 2) {
+      mma16816(s, kwa[2 * kk], kwb[2 * kk], kwa[2 * kk + 1], kwb[2 * kk + 1], qw[2 * kk],
+               qw[2 * kk + 1]);
+      mma16816(s1, kwa[2 * kk + 2], kwb[2 * kk + 2], kwa[2 * kk + 3], kwb[2 * kk + 3],
+               qw[2 * kk + 2], qw[2 * kk + 3]);
+    }
+  }
+  s[0] += s1[0]; s[1] += s1[1]; s[2] += s1[2]; s[3] += s1[3];
+}
+
+// P' = P * s_v for one page, transposed by movmatrix into the PV B fragment.
+template <int D, int VB, class VL>
+__device__ __forceinline__ void page_probs(const VL& vl, int nv, float p0, float p1, float p2,
+                                           float p3, int g, uint32_t& pb0, uint32_t& pb1) {
+  float sv0 = 1.f, sv1 = 1.f;
+  if constexpr (VB < 16) {
+    const int so = BLOCK * D * VB / 8;
+    const uint32_t w0 = vl.h1(so + 2 * g), w1 = vl.h1(so + 2 * (g + 8));
+    sv0 = g < nv ? __half2float(__ushort_as_half((unsigned short)w0)) : 0.f;
+    sv1 = g + 8 < nv ? __half2float(__ushort_as_half((unsigned short)w1)) : 0.f;
+  }
+  pb0 = movtrans(h2u(__floats2half2_rn(p0 * sv0, p1 * sv0)));
+  pb1 = movtrans(h2u(__floats2half2_rn(p2 * sv1, p3 * sv1)));
+}
+
+// O^T[d x 8] += V^T P^T for one page.
+template <int D, int VB, class VL>
+__device__ __forceinline__ void page_pv(const VL& vl, uint32_t pb0, uint32_t pb1, Acc<D>& A,
+                                        int g, int c) {
+  constexpr int VCH = D / 8, NMT = D / 16;
+  constexpr int VROW = VB == 16 ? 2 * D : D * VB / 8;
+  constexpr int VOFF = VCH * VB / 8;
+  uint32_t va[VCH], vb[VCH];
+  const int vr = g * VOFF;
+  v_pair_words<D, VB>(vl, vr + (2 * c) * VROW, vr + (2 * c + 1) * VROW, va);
+  v_pair_words<D, VB>(vl, vr + (2 * c + 8) * VROW, vr + (2 * c + 9) * VROW, vb);
+#pragma unroll
+  for (int mt = 0; mt < NMT; ++mt)
+    mma16816(A.o[mt], va[mt], va[NMT + mt], vb[mt], vb[NMT + mt], pb0, pb1);
+}
+
+// Online-softmax update over up to two pages of the same K width at once (one
+// shared max reduction); page b is skipped when nvb == 0.
+template <int D, int VB, bool FULL, int KB, class KLA, class VLA, class KLB, class VLB>
+__device__ __forceinline__ void attend_pages(const KLA& kla, const VLA& vla, int nva,
+                                             const KLB& klb, const VLB& vlb, int nvb,
+                                             const uint32_t* qw, Acc<D>& A, float sl, int g,
+                                             int c) {
+  constexpr int NMT = D / 16;
+  float sa[4], sb[4];
+  page_scores<D, KB>(kla, qw, sa, g, c);
+  if (nvb > 0) page_scores<D, KB>(klb, qw, sb, g, c);
+  float xa0 = sa[0] * sl, xa1 = sa[1] * sl, xa2 = sa[2] * sl, xa3 = sa[3] * sl;
+  if (!FULL) {  // rows past the valid count carry no token
+    if (g >= nva) xa0 = xa1 = -CUDART_INF_F;
+    if (g + 8 >= nva) xa2 = xa3 = -CUDART_INF_F;
+  }
+  float xb0 = -CUDART_INF_F, xb1 = -CUDART_INF_F, xb2 = -CUDART_INF_F, xb3 = -CUDART_INF_F;
+  if (nvb > 0) {
+    xb0 = sb[0] * sl; xb1 = sb[1] * sl; xb2 = sb[2] * sl; xb3 = sb[3] * sl;
+    if (!FULL) {
+      if (g >= nvb) xb0 = xb1 = -CUDART_INF_F;
+      if (g + 8 >= nvb) xb2 = xb3 = -CUDART_INF_F;
+    }
+  }
+  float bm0 = fmaxf(fmaxf(xa0, xa2), fmaxf(xb0, xb2));
+  float bm1 = fmaxf(fmaxf(xa1, xa3), fmaxf(xb1, xb3));
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+    bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+  }
+  const float mn0 = fmaxf(A.m0, bm0), mn1 = fmaxf(A.m1, bm1);
+  if (mn0 != A.m0 || mn1 != A.m1) {  // rescale only when a running max moved
+    const float al0 = fexp2(A.m0 - mn0), al1 = fexp2(A.m1 - mn1);
+    A.l0 *= al0;
+    A.l1 *= al1;
+#pragma unroll
+    for (int i = 0; i < NMT; ++i) {
+      A.o[i][0] *= al0; A.o[i][1] *= al1; A.o[i][2] *= al0; A.o[i][3] *= al1;
+    }
+    A.m0 = mn0;
+    A.m1 = mn1;
+  }
+  const float pa0 = fexp2(xa0 - mn0), pa1 = fexp2(xa1 - mn1);
+  const float pa2 = fexp2(xa2 - mn0), pa3 = fexp2(xa3 - mn1);
+  A.l0 += pa0 + pa2;
+  A.l1 += pa1 + pa3;
+  uint32_t qa0, qa1;
+  page_probs<D, VB>(vla, FULL ? BLOCK : nva, pa0, pa1, pa2, pa3, g, qa0, qa1);
+  if (nvb > 0) {
+    const float pb0 = fexp2(xb0 - mn0), pb1 = fexp2(xb1 - mn1);
+    const float pb2 = fexp2(xb2 - mn0), pb3 = fexp2(xb3 - mn1);
+    A.l0 += pb0 + pb2;
+    A.l1 += pb1 + pb3;
+    uint32_t qb0, qb1;
+    page_probs<D, VB>(vlb, FULL ? BLOCK : nvb, pb0, pb1, pb2, pb3, g, qb0, qb1);
+    page_pv<D, VB>(vla, qa0, qa1, A, g, c);
+    page_pv<D, VB>(vlb, qb0, qb1, A, g, c);
+  } else {
+    page_pv<D, VB>(vla, qa0, qa1, A, g, c);
+  }
+}
+
+template <int N>
+struct KBits {
+  static constexpr int value = N;
+};
+// Call f(KBits<kb>{}) with the page K width as a compile-time constant.
+template <class F>
+__device__ __forceinline__ void with_kbits(int kb, F&& f) {
+  switch (kb) {
+    case 2: f(KBits<2>{}); break;
+    case 4: f(KBits<4>{}); break;
+    case 8: f(KBits<8>{}); break;
+    default: f(KBits<16>{}); break;
+  }
+}
+
 template <int D, int VB>
-__global__ void __launch_bounds__(NT)
+__global__ void __launch_bounds__(NT, AttnCfg<VB>::CTAS)
 decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
                    const __half* __restrict__ q, __half* __restrict__ o, int splits) {
-  constexpr int KCH = D / 4, KW = KCH / 2, NKS = D / 16, VCH = D / 8, NMT = D / 16;
+  constexpr int KCH = D / 4, KW = KCH / 2, VCH = D / 8, NMT = D / 16;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[NW][NSMAX];
   __shared__ float sm_m[NW][MAX_G], sm_l[NW][MAX_G];
-  __shared__ float sm_acc[NW][MAX_G][D];
   __shared__ int s_last;
 
   const int split = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
@@ -225,6 +471,7 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   const int nb = (T + BLOCK - 1) / BLOCK;
   const int cb = (nb + splits - 1) / splits;
   const int b0 = min(nb, split * cb), b1 = min(nb, b0 + cb);
+  const bool has_open = (T % BLOCK) != 0;
 
   // Q fragment words for head g of the group (zero for padding heads)
   uint32_t qw[KW];
@@ -240,130 +487,148 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
     for (int i = 0; i < KW; ++i) qw[i] = 0u;
   }
 
-  float acc[NMT][4];
+  Acc<D> A;
 #pragma unroll
-  for (int i = 0; i < NMT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-  float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
+  for (int i = 0; i < NMT; ++i) A.o[i][0] = A.o[i][1] = A.o[i][2] = A.o[i][3] = 0.f;
+  A.m0 = A.m1 = -CUDART_INF_F;
+  A.l0 = A.l1 = 0.f;
 
   const int32_t* bt = st.bt + lsh_index(st, layer, slot_ok ? slot : 0, h) * st.maxblk;
   const __half* stg = st.staging + lsh_index(st, layer, slot_ok ? slot : 0, h) * (BLOCK * D);
   const float sl = st.scale_log2;
 
-  for (int blk = b0 + warp; blk < b1; blk += NW) {
+  // Stage geometry: sized for the widest page this layer has admitted so far.
+  const int kmax = max(2, st.kmax[layer]);
+  const int stage_bytes = (page_bytes(kmax, VB, D) + 127) & ~127;
+  constexpr int WARP_BYTES = AttnCfg<VB>::WARP_BYTES;
+  const int ns = min(NSMAX, WARP_BYTES / stage_bytes);
+  const uint8_t* wptr = smem + warp * WARP_BYTES;
+  const uint32_t wbase = (uint32_t)__cvta_generic_to_shared(wptr);
+  const uint32_t bar0 = (uint32_t)__cvta_generic_to_shared(&bars[warp][0]);
+  if (lane == 0) {
+    for (int i = 0; i < ns; ++i) mbar_init(bar0 + 8 * i, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+
+  // This warp's blocks: b0 + warp + k*NW for k < nk.  Pages of sealed blocks go
+  // through the pipeline; the open block (always the sequence's last) does not.
+  const int nk = (b1 - b0 > warp) ? (b1 - b0 - warp + NW - 1) / NW : 0;
+  auto issue = [&](int k, int sidx) {  // lane 0 only; block k goes to stage sidx
+    const int blk = b0 + warp + k * NW;
+    if (has_open && blk == nb - 1) return;
     const int32_t e = bt[blk];
+    if (e == -1) return;
+    const int fmt = entry_fmt(e);
+    const uint32_t bytes = (uint32_t)st.pool_page_bytes[fmt];
+    const uint8_t* src = st.pool_base[fmt] + (size_t)entry_idx(e) * bytes;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_expect_tx(bar0 + 8 * sidx, bytes);
+    bulk_g2s(wbase + sidx * stage_bytes, src, bytes, bar0 + 8 * sidx);
+  };
+  if (lane == 0)
+    for (int k = 0; k < min(ns, nk); ++k) issue(k, k);
+
+  // `issued`: blocks k < issued had issue() called (warp-uniform).  After a wait
+  // times out the warp stops issuing and computing but still waits, each wait
+  // bounded, for the copies already in flight, so none lands after it exits.
+  // Pipelined pages are consumed two at a time; the open block, always the
+  // sequence's last and so this warp's last, is attended alone from global memory.
+  const bool own_open = has_open && nk > 0 && (b0 + warp + (nk - 1) * NW) == nb - 1;
+  const int np = nk - (own_open ? 1 : 0);  // pipelined blocks of this warp
+  uint32_t phases = 0;
+  bool ok = true;
+  int issued = min(ns, nk);
+  int sidx = 0;  // stage of block k (= k mod ns)
+  // Wait for block k's page; returns its entry, or -1 when it has no page or the
+  // wait failed (then nothing is computed for it).
+  auto acquire = [&](int k, int si) -> int32_t {
+    const int32_t e = bt[b0 + warp + k * NW];
     if (e == -1) {
       if (lane == 0) set_error(st, EKV_ESTATE);
-      continue;
+      return -1;
     }
-    const int fmt = entry_fmt(e);
-    const int kbp = bits_of_code(fmt >> 2);
-    const uint8_t* page = st.pool_base[fmt] + (size_t)entry_idx(e) * st.pool_page_bytes[fmt];
-    const uint8_t* vpart = page + k_part_bytes(kbp, D);
-    const bool open = (blk == nb - 1) && (T % BLOCK != 0);
-    const int nv = open ? (T % BLOCK) : BLOCK;
-
-    // ---- S^T = K Q^T ----------------------------------------------------------
-    const int kb = open ? 16 : kbp;
-    const uint8_t* kbase = open ? reinterpret_cast<const uint8_t*>(stg) : page;
-    const int krow = kb == 16 ? 2 * D : D * kb / 8;
-    uint32_t kwa[KW], kwb[KW];
-    k_row_words<D>(kbase + (size_t)g * krow, kb, c, kwa);
-    k_row_words<D>(kbase + (size_t)(g + 8) * krow, kb, c, kwb);
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
-    if (kb < 16) {
-      // Fold the per-channel K scale into Q: q*s = hi + lo with hi = fp16(q*s) and
-      // lo = fp16(q*s - hi) from one fused multiply-add (the residual of a rounded
-      // fp16 product is itself an fp16 value).  Two MMAs against the exact integer
-      // codes keep the logits accurate to fp32 accumulation.
-      uint32_t qh[KW], ql[KW];
-      const uint4* sp = reinterpret_cast<const uint4*>(page + BLOCK * D * kb / 8 + c * KCH * 2);
-#pragma unroll
-      for (int i = 0; i < KW / 4; ++i) {
-        const uint4 u = __ldg(sp + i);
-        const uint32_t sv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          qh[4 * i + x] = hmul2u(qw[4 * i + x], sv[x]);
-          ql[4 * i + x] = hfma2u(qw[4 * i + x], sv[x], qh[4 * i + x] ^ 0x80008000u);
-        }
-      }
-#pragma unroll
-      for (int kk = 0; kk < NKS; ++kk)
-        mma16816(s, kwa[2 * kk], kwb[2 * kk], kwa[2 * kk + 1], kwb[2 * kk + 1], qh[2 * kk],
-                 qh[2 * kk + 1]);
-#pragma unroll
-      for (int kk = 0; kk < NKS; ++kk)
-        mma16816(s, kwa[2 * kk], kwb[2 * kk], kwa[2 * kk + 1], kwb[2 * kk + 1], ql[2 * kk],
-                 ql[2 * kk + 1]);
+    if (k >= issued) return -1;
+    if (!mbar_wait(bar0 + 8 * si, (phases >> si) & 1) && ok) {
+      ok = false;
+      if (lane == 0) set_error(st, EKV_ETIMEOUT);
+    }
+    phases ^= 1u << si;
+    return ok ? e : -1;
+  };
+  auto refill = [&](int k, int si) {  // after block k's stage is consumed
+    if (ok && k + ns < nk) {
+      if (lane == 0) issue(k + ns, si);
+      issued = k + ns + 1;
+    }
+  };
+  for (int k = 0; k < np; k += 2) {
+    const int s0 = sidx, s1 = (sidx + 1 == ns) ? 0 : sidx + 1;
+    const bool two = k + 1 < np;
+    const int32_t ea = acquire(k, s0);
+    const int32_t eb = two ? acquire(k + 1, s1) : -1;
+    const uint8_t* sa = wptr + s0 * stage_bytes;
+    const uint8_t* sb = wptr + s1 * stage_bytes;
+    const int kba = ea != -1 ? bits_of_code(entry_fmt(ea) >> 2) : 0;
+    const int kbb = eb != -1 ? bits_of_code(entry_fmt(eb) >> 2) : 0;
+    if (kba != 0 && kba == kbb) {  // the common case: both pages share a K width
+      with_kbits(kba, [&](auto kbc) {
+        constexpr int KB = decltype(kbc)::value;
+        constexpr int KP = k_part_bytes(KB, D);
+        attend_pages<D, VB, true, KB>(SLd{sa}, SLd{sa + KP}, BLOCK, SLd{sb}, SLd{sb + KP},
+                                      BLOCK, qw, A, sl, g, c);
+      });
     } else {
-#pragma unroll
-      for (int kk = 0; kk < NKS; ++kk)
-        mma16816(s, kwa[2 * kk], kwb[2 * kk], kwa[2 * kk + 1], kwb[2 * kk + 1], qw[2 * kk],
-                 qw[2 * kk + 1]);
+      if (kba != 0)
+        with_kbits(kba, [&](auto kbc) {
+          constexpr int KB = decltype(kbc)::value;
+          attend_pages<D, VB, true, KB>(SLd{sa}, SLd{sa + k_part_bytes(KB, D)}, BLOCK, SLd{sa},
+                                        SLd{sa}, 0, qw, A, sl, g, c);
+        });
+      if (kbb != 0)
+        with_kbits(kbb, [&](auto kbc) {
+          constexpr int KB = decltype(kbc)::value;
+          attend_pages<D, VB, true, KB>(SLd{sb}, SLd{sb + k_part_bytes(KB, D)}, BLOCK, SLd{sb},
+                                        SLd{sb}, 0, qw, A, sl, g, c);
+        });
     }
-
-    // ---- online softmax (log2 domain) -----------------------------------------
-    float x0 = s[0] * sl, x1 = s[1] * sl, x2 = s[2] * sl, x3 = s[3] * sl;
-    if (g >= nv) x0 = x1 = -CUDART_INF_F;
-    if (g + 8 >= nv) x2 = x3 = -CUDART_INF_F;
-    float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
-      bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
-    }
-    const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-    const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
-    const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1);
-    const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
-    l0 = l0 * al0 + (p0 + p2);
-    l1 = l1 * al1 + (p1 + p3);
-    m0 = mn0;
-    m1 = mn1;
-#pragma unroll
-    for (int i = 0; i < NMT; ++i) {
-      acc[i][0] *= al0; acc[i][1] *= al1; acc[i][2] *= al0; acc[i][3] *= al1;
-    }
-
-    // ---- P' = P * s_v, transposed into the B fragment --------------------------
-    float sv0 = 1.f, sv1 = 1.f;
-    if constexpr (VB < 16) {
-      const __half* svp = reinterpret_cast<const __half*>(vpart + BLOCK * D * VB / 8);
-      sv0 = g < nv ? __half2float(svp[g]) : 0.f;
-      sv1 = g + 8 < nv ? __half2float(svp[g + 8]) : 0.f;
-    }
-    const uint32_t plo = h2u(__floats2half2_rn(p0 * sv0, p1 * sv0));
-    const uint32_t phi = h2u(__floats2half2_rn(p2 * sv1, p3 * sv1));
-    const uint32_t pb0 = movtrans(plo), pb1 = movtrans(phi);
-
-    // ---- O^T += V^T P^T ---------------------------------------------------------
-    constexpr int VROW = VB == 16 ? 2 * D : D * VB / 8;
-    constexpr int VOFF = VCH * VB / 8;
-    uint32_t va[VCH], vb[VCH];
-    const uint8_t* vr = vpart + g * VOFF;
-    v_pair_words<D, VB>(vr + (2 * c) * VROW, vr + (2 * c + 1) * VROW, va);
-    v_pair_words<D, VB>(vr + (2 * c + 8) * VROW, vr + (2 * c + 9) * VROW, vb);
-#pragma unroll
-    for (int mt = 0; mt < NMT; ++mt)
-      mma16816(acc[mt], va[mt], va[NMT + mt], vb[mt], vb[NMT + mt], pb0, pb1);
+    __syncwarp();
+    refill(k, s0);
+    if (two) refill(k + 1, s1);
+    sidx = two ? ((s1 + 1 == ns) ? 0 : s1 + 1) : s1;
   }
+  if (own_open && ok) {
+    const int32_t e = bt[nb - 1];
+    if (e == -1) {
+      if (lane == 0) set_error(st, EKV_ESTATE);
+    } else {
+      const int fmt = entry_fmt(e);
+      const uint8_t* page = st.pool_base[fmt] + (size_t)entry_idx(e) * st.pool_page_bytes[fmt];
+      const GLd kl{reinterpret_cast<const uint8_t*>(stg)};
+      const GLd vl{page + k_part_bytes(bits_of_code(fmt >> 2), D)};
+      attend_pages<D, VB, false, 16>(kl, vl, T % BLOCK, kl, vl, 0, qw, A, sl, g, c);
+    }
+  }
+  __syncthreads();
 
-  // ---- merge the warps of this CTA ---------------------------------------------
+  // ---- merge the warps of this CTA (reusing the stage memory) ----------------------
+  float* sm_acc = reinterpret_cast<float*>(smem);  // [NW][MAX_G][D]
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    A.l0 += __shfl_xor_sync(0xffffffffu, A.l0, off);
+    A.l1 += __shfl_xor_sync(0xffffffffu, A.l1, off);
   }
   if (g == 0) {
-    sm_m[warp][2 * c] = m0; sm_m[warp][2 * c + 1] = m1;
-    sm_l[warp][2 * c] = l0; sm_l[warp][2 * c + 1] = l1;
+    sm_m[warp][2 * c] = A.m0; sm_m[warp][2 * c + 1] = A.m1;
+    sm_l[warp][2 * c] = A.l0; sm_l[warp][2 * c + 1] = A.l1;
   }
+  float* wacc = sm_acc + (size_t)warp * MAX_G * D;
 #pragma unroll
   for (int mt = 0; mt < NMT; ++mt) {
-    sm_acc[warp][2 * c][g * VCH + mt] = acc[mt][0];
-    sm_acc[warp][2 * c + 1][g * VCH + mt] = acc[mt][1];
-    sm_acc[warp][2 * c][g * VCH + NMT + mt] = acc[mt][2];
-    sm_acc[warp][2 * c + 1][g * VCH + NMT + mt] = acc[mt][3];
+    wacc[(2 * c) * D + g * VCH + mt] = A.o[mt][0];
+    wacc[(2 * c + 1) * D + g * VCH + mt] = A.o[mt][1];
+    wacc[(2 * c) * D + g * VCH + NMT + mt] = A.o[mt][2];
+    wacc[(2 * c + 1) * D + g * VCH + NMT + mt] = A.o[mt][3];
   }
   __syncthreads();
 
@@ -374,17 +639,17 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
     float M = -CUDART_INF_F;
 #pragma unroll
     for (int w = 0; w < NW; ++w) M = fmaxf(M, sm_m[w][hd]);
-    float L = 0.f, A = 0.f;
+    float L = 0.f, Ao = 0.f;
 #pragma unroll
     for (int w = 0; w < NW; ++w) {
       const float f = sm_m[w][hd] == -CUDART_INF_F ? 0.f : exp2f(sm_m[w][hd] - M);
       L += f * sm_l[w][hd];
-      A += f * sm_acc[w][hd][ch];
+      Ao += f * sm_acc[((size_t)w * MAX_G + hd) * D + ch];
     }
     if (splits == 1) {
-      o[((size_t)z * st.Hq + h * G + hd) * D + ch] = __float2half_rn(L > 0.f ? A / L : 0.f);
+      o[((size_t)z * st.Hq + h * G + hd) * D + ch] = __float2half_rn(L > 0.f ? Ao / L : 0.f);
     } else {
-      st.attn_acc[(pid * G + hd) * D + ch] = A;
+      st.attn_acc[(pid * G + hd) * D + ch] = Ao;
       if (ch == 0) {
         st.attn_ml[(pid * G + hd) * 2] = M;
         st.attn_ml[(pid * G + hd) * 2 + 1] = L;
@@ -393,7 +658,7 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   }
   if (splits == 1) return;
 
-  // ---- last CTA of this (seq, kv head) merges the splits -------------------------
+  // ---- last CTA of this (seq, kv head) merges the splits ---------------------------
   __threadfence();
   __syncthreads();
   if (tid == 0) {
@@ -405,19 +670,76 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  for (int i = tid; i < G * D; i += NT) {
-    const int hd = i / D, ch = i % D;
+  // Stage every split's (max, sum) in shared memory, turn them into per-split
+  // weights 2^(m_j - M) / L once per head, then sum the numerators with every
+  // thread streaming its own columns (many independent loads in flight).
+  float* s_w = reinterpret_cast<float*>(smem);          // [splits][MAX_G] weights
+  float* s_l = s_w + (size_t)splits * MAX_G;            // [splits][MAX_G] sums
+  for (int i = tid; i < splits * G; i += NT) {
+    const int j = i / G, hd = i % G;
+    s_w[j * MAX_G + hd] = __ldcg(st.attn_ml + ((pbase + j) * G + hd) * 2);
+    s_l[j * MAX_G + hd] = __ldcg(st.attn_ml + ((pbase + j) * G + hd) * 2 + 1);
+  }
+  __syncthreads();
+  for (int hd = warp; hd < G; hd += NW) {
     float M = -CUDART_INF_F;
-    for (int j = 0; j < splits; ++j) M = fmaxf(M, __ldcg(st.attn_ml + ((pbase + j) * G + hd) * 2));
-    float L = 0.f, A = 0.f;
-    for (int j = 0; j < splits; ++j) {
-      const float mj = __ldcg(st.attn_ml + ((pbase + j) * G + hd) * 2);
-      if (mj == -CUDART_INF_F) continue;
-      const float f = exp2f(mj - M);
-      L += f * __ldcg(st.attn_ml + ((pbase + j) * G + hd) * 2 + 1);
-      A += f * __ldcg(st.attn_acc + ((pbase + j) * G + hd) * D + ch);
+    for (int j = lane; j < splits; j += 32) M = fmaxf(M, s_w[j * MAX_G + hd]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float L = 0.f;
+    for (int j = lane; j < splits; j += 32) {
+      const float mj = s_w[j * MAX_G + hd];
+      const float f = (mj == -CUDART_INF_F) ? 0.f : exp2f(mj - M);
+      s_w[j * MAX_G + hd] = f;
+      L += f * s_l[j * MAX_G + hd];
     }
-    o[((size_t)z * st.Hq + h * G + hd) * D + ch] = __float2half_rn(L > 0.f ? A / L : 0.f);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    __syncwarp();
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    for (int j = lane; j < splits; j += 32) s_w[j * MAX_G + hd] *= inv;
+  }
+  __syncthreads();
+  constexpr int PER = (MAX_G * D + NT - 1) / NT;   // output elements per thread
+  float out_acc[PER];
+#pragma unroll
+  for (int r = 0; r < PER; ++r) out_acc[r] = 0.f;
+  // Four splits per round without predicates (the remainder runs one by one),
+  // so 4 * PER independent loads are in flight per thread.
+  const float* accp = st.attn_acc + pbase * G * D;
+  const int GD = G * D;
+  int j = 0;
+  if (GD == PER * NT) {
+    for (; j + 4 <= splits; j += 4) {
+#pragma unroll
+      for (int r = 0; r < PER; ++r) {
+        const int i = tid + r * NT;
+        const float* pa = accp + (size_t)j * GD + i;
+        const float a0 = __ldcg(pa), a1 = __ldcg(pa + GD), a2 = __ldcg(pa + 2 * GD),
+                    a3 = __ldcg(pa + 3 * GD);
+        const int hd = i / D;
+        float t = out_acc[r];
+        t = fmaf(s_w[j * MAX_G + hd], a0, t);
+        t = fmaf(s_w[(j + 1) * MAX_G + hd], a1, t);
+        t = fmaf(s_w[(j + 2) * MAX_G + hd], a2, t);
+        out_acc[r] = fmaf(s_w[(j + 3) * MAX_G + hd], a3, t);
+      }
+    }
+  }
+  for (; j < splits; ++j) {
+#pragma unroll
+    for (int r = 0; r < PER; ++r) {
+      const int i = tid + r * NT;
+      if (i < GD) out_acc[r] = fmaf(s_w[j * MAX_G + i / D], __ldcg(accp + (size_t)j * GD + i), out_acc[r]);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < PER; ++r) {
+    const int i = tid + r * NT;
+    if (i < G * D) {
+      const int hd = i / D, ch = i % D;
+      o[((size_t)z * st.Hq + h * G + hd) * D + ch] = __float2half_rn(out_acc[r]);
+    }
   }
 }
 
@@ -425,11 +747,34 @@ template <int D, int VB>
 cudaError_t launch_t(const DevState& st, int layer, int n_seqs, const int32_t* slots,
                      const __half* q, __half* o, int splits, cudaStream_t s) {
   dim3 grid(splits, st.Hkv, n_seqs);
-  decode_attn_kernel<D, VB><<<grid, NT, 0, s>>>(st, layer, slots, q, o, splits);
+  decode_attn_kernel<D, VB><<<grid, NT, AttnCfg<VB>::SMEM, s>>>(st, layer, slots, q, o, splits);
   return cudaGetLastError();
 }
 
+template <int D, int VB>
+cudaError_t init_t() {
+  cudaError_t e = cudaFuncSetAttribute(decode_attn_kernel<D, VB>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       AttnCfg<VB>::SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(decode_attn_kernel<D, VB>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+  return e;
+}
+
 }  // namespace
+
+int attn_ctas_per_sm(int vb) { return vb == 16 ? AttnCfg<16>::CTAS : AttnCfg<4>::CTAS; }
+
+cudaError_t attn_init() {
+  cudaError_t e = cudaSuccess;
+  cudaError_t (*fns[])() = {init_t<64, 2>,  init_t<64, 4>,  init_t<64, 8>,  init_t<64, 16>,
+                            init_t<128, 2>, init_t<128, 4>, init_t<128, 8>, init_t<128, 16>};
+  for (auto f : fns)
+    if (e == cudaSuccess) e = f();
+  return e;
+}
 
 cudaError_t launch_decode_attn(const DevState& st, int layer, int n_seqs, const int32_t* slots,
                                const __half* q, __half* o, int splits, int vb, cudaStream_t s) {

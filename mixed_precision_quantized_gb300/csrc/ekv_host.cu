@@ -2,6 +2,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <algorithm>
 #include <new>
 #include <vector>
 
@@ -15,7 +16,6 @@ struct ekv_cache {
   std::vector<void*> allocs;
   std::vector<int> vbits;   // host copy (fixed per layer)
   int num_sm = 0;
-  int ctas_target = 0;      // decode-attention CTAs per launch to aim for
 };
 
 namespace {
@@ -41,9 +41,10 @@ void free_all(ekv_cache* c) {
   c->allocs.clear();
 }
 
-int attn_splits(const ekv_cache* c, int n_seqs) {
+int attn_splits(const ekv_cache* c, int n_seqs, int vb) {
   const int units = n_seqs * c->st.Hkv;
-  int s = (c->ctas_target + units - 1) / units;
+  const int target = attn_ctas_per_sm(vb) * c->num_sm;
+  int s = (target + units - 1) / units;
   if (s < 1) s = 1;
   if (s > 512) s = 512;
   return s;
@@ -61,8 +62,8 @@ namespace ekv {
 int attn_plan(ekv_cache* c, int layer, int n_seqs, DevState* st, int* splits, int* vb) {
   if (!c || layer < 0 || layer >= c->st.L || n_seqs < 0 || n_seqs > c->st.S) return EKV_EINVAL;
   *st = c->st;
-  *splits = attn_splits(c, n_seqs > 0 ? n_seqs : 1);
   *vb = c->vbits[layer];
+  *splits = attn_splits(c, n_seqs > 0 ? n_seqs : 1, *vb);
   return EKV_OK;
 }
 }  // namespace ekv
@@ -130,7 +131,6 @@ int ekv_create(const ekv_config* cfg, const uint8_t* k_bits_init, const uint8_t*
     delete c;
     return EKV_ECUDA;
   }
-  c->ctas_target = 4 * c->num_sm;
 
   const size_t L = st.L, S = st.S, H = st.Hkv, D = st.D, MB = st.maxblk;
   bool ok = true;
@@ -154,6 +154,7 @@ int ekv_create(const ekv_config* cfg, const uint8_t* k_bits_init, const uint8_t*
   st.staging = (__half*)A(L * S * H * BLOCK * D * 2);
   st.ring = (__half*)A(L * S * H * RING * D * 2);
   st.tier = (int32_t*)A(L * 4);
+  st.kmax = (int32_t*)A(L * 4);
   st.vbits = (int32_t*)A(L * 4);
   st.ema = (float*)A(L * 3 * 4);
   st.ema_valid = (int32_t*)A(L * 4);
@@ -162,7 +163,7 @@ int ekv_create(const ekv_config* cfg, const uint8_t* k_bits_init, const uint8_t*
   st.append_ticket = (int32_t*)A(L * S * 4);
   int parts = 0;
   for (int n = 1; n <= k.max_seqs; ++n) {
-    const int p = n * k.num_kv_heads * attn_splits(c, n);
+    const int p = n * k.num_kv_heads * std::max(attn_splits(c, n, 4), attn_splits(c, n, 16));
     if (p > parts) parts = p;
   }
   st.attn_parts_cap = parts;
@@ -178,6 +179,7 @@ int ekv_create(const ekv_config* cfg, const uint8_t* k_bits_init, const uint8_t*
   }
 
   cudaError_t e = canary_init();
+  if (e == cudaSuccess) e = attn_init();
   auto Z = [&](void* p, size_t bytes) {
     if (e == cudaSuccess) e = cudaMemset(p, 0, bytes);
   };
@@ -197,6 +199,7 @@ int ekv_create(const ekv_config* cfg, const uint8_t* k_bits_init, const uint8_t*
   if (e == cudaSuccess) e = cudaMemcpy(st.vbits, vb.data(), L * 4, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemset(st.bt, 0xFF, L * S * H * MB * 4);
   Z(st.len, L * S * 4);
+  Z(st.kmax, L * 4);
   Z(st.staging, L * S * H * BLOCK * D * 2);
   Z(st.ring, L * S * H * RING * D * 2);
   Z(st.ema, L * 3 * 4);
@@ -247,7 +250,7 @@ int ekv_decode_attn(ekv_cache* c, int32_t layer, int32_t n_seqs, const int32_t* 
   if (n_seqs == 0) return EKV_OK;
   if (!seq_slots || !q || !o) return EKV_EINVAL;
   if (((uintptr_t)q | (uintptr_t)o) & 15) return EKV_EINVAL;
-  const int splits = attn_splits(c, n_seqs);
+  const int splits = attn_splits(c, n_seqs, c->vbits[layer]);
   if (n_seqs * c->st.Hkv * splits > c->st.attn_parts_cap) return EKV_ESTATE;
   return cuda_status(launch_decode_attn(c->st, layer, n_seqs, seq_slots,
                                         static_cast<const __half*>(q), static_cast<__half*>(o),

@@ -18,13 +18,13 @@ __host__ __device__ inline int bits_of_code(int code) { return 2 << code; }
 __host__ __device__ inline int code_of_bits(int b) {
   return b == 2 ? 0 : b == 4 ? 1 : b == 8 ? 2 : b == 16 ? 3 : -1;
 }
-__host__ __device__ inline int k_part_bytes(int kb, int d) {
+__host__ __device__ constexpr int k_part_bytes(int kb, int d) {
   return kb == 16 ? BLOCK * d * 2 : BLOCK * d * kb / 8 + 2 * d;
 }
-__host__ __device__ inline int v_part_bytes(int vb, int d) {
+__host__ __device__ constexpr int v_part_bytes(int vb, int d) {
   return vb == 16 ? BLOCK * d * 2 : BLOCK * d * vb / 8 + 2 * BLOCK;
 }
-__host__ __device__ inline int page_bytes(int kb, int vb, int d) {
+__host__ __device__ constexpr int page_bytes(int kb, int vb, int d) {
   return k_part_bytes(kb, d) + v_part_bytes(vb, d);
 }
 
@@ -49,6 +49,7 @@ struct DevState {
   __half* staging;          // [L][S][Hkv][16][D]  open-block K rows
   __half* ring;             // [L][S][Hkv][64][D]  FP16 K_ref ring
   int32_t* tier;            // [L] current K tier (bits)
+  int32_t* kmax;            // [L] widest K bits any page of the layer was admitted with
   int32_t* vbits;           // [L]
   float* ema;               // [L][3]
   int32_t* ema_valid;       // [L]
@@ -75,6 +76,8 @@ __host__ __device__ inline size_t lsh_index(const DevState& st, int l, int s, in
 // ---- launchers (defined in the kernel translation units) ----------------------
 cudaError_t launch_append(const DevState& st, int layer, int n_seqs, const int32_t* slots,
                           int n_new, const __half* k, const __half* v, cudaStream_t s);
+cudaError_t attn_init();   // once per process, before any launch
+int attn_ctas_per_sm(int vb);  // resident decode-attention CTAs per SM for V width vb
 cudaError_t launch_decode_attn(const DevState& st, int layer, int n_seqs, const int32_t* slots,
                                const __half* q, __half* o, int splits, int vb, cudaStream_t s);
 cudaError_t canary_init();  // once per process, before any launch
