@@ -131,8 +131,25 @@ __device__ void seal_k(const __half* stg, const __half* kin, size_t in_row, int 
     for (int c = 0; c < 8; ++c) code[c] = quant_code(f[c], sf[c], qm) + (1 << (kb - 1));
     store_codes8(kpart + (size_t)r * (D * kb / 8) + t * kb, code, kb);
   }
-  *reinterpret_cast<uint4*>(kpart + BLOCK * D * kb / 8 + 16 * t) =
-      *reinterpret_cast<const uint4*>(s16);
+  // Scales in pair order: within each group of n = 32/kb channels (one 32-bit
+  // code word) position p holds channel p/2 + (p%2)*n/2; 8-bit pages keep the
+  // natural order.  Thread t owns channels 8t .. 8t+7.
+  __half* sdst = reinterpret_cast<__half*>(kpart + BLOCK * D * kb / 8);
+  if (kb == 8) {
+    *reinterpret_cast<uint4*>(sdst + 8 * t) = *reinterpret_cast<const uint4*>(s16);
+  } else if (kb == 4) {  // group = this thread's 8 channels: 0,4,1,5,2,6,3,7
+    __align__(16) __half o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      o[2 * i] = s16[i];
+      o[2 * i + 1] = s16[i + 4];
+    }
+    *reinterpret_cast<uint4*>(sdst + 8 * t) = *reinterpret_cast<const uint4*>(o);
+  } else {  // kb == 2: group of 16 channels = threads 2m, 2m+1
+    __half* grp = sdst + 16 * (t / 2);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) grp[2 * i + (t & 1)] = s16[i];
+  }
 }
 
 template <int D>

@@ -67,6 +67,16 @@ constexpr uint32_t H_1032 = 0x64086408u;   // 1032, 1032
 constexpr uint32_t H_1026 = 0x64026402u;   // 1026, 1026
 constexpr uint32_t H_1152 = 0x64806480u;   // 1152, 1152
 constexpr uint32_t H_MAGIC = 0x64006400u;  // 1024, 1024 exponent pattern
+constexpr uint32_t H_Q4 = 0x34003400u;     // 1/4
+constexpr uint32_t H_Q16 = 0x2C002C00u;    // 1/16
+constexpr uint32_t H_Q64 = 0x24002400u;    // 1/64
+constexpr uint32_t H_M72 = 0xD480D480u;    // -72  = -(1024 + 16*8)/16
+constexpr uint32_t H_M258 = 0xDC08DC08u;   // -258 = -(1024 + 4*2)/4
+constexpr uint32_t H_M66 = 0xD420D420u;    // -66  = -(1024 + 16*2)/16
+constexpr uint32_t H_M18 = 0xCC80CC80u;    // -18  = -(1024 + 64*2)/64
+
+// x >> 8 as a multiply-high (runs on the FMA pipe, which has spare issue slots).
+__device__ __forceinline__ uint32_t shr8(uint32_t x) { return __umulhi(x, 1u << 24); }
 
 __device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -162,6 +172,8 @@ __device__ __forceinline__ void k_row_words(const LD& ld, int row, int c, uint32
   constexpr int KCH = D / 4;
   constexpr int KW = KCH / 2;
   if constexpr (KB == 4) {
+    // Word w holds channels 8w..8w+7; out pairs (k, k+4), k = 0..3, matching the
+    // pair order of 4-bit scales.
     constexpr int NB = KCH / 2;  // bytes
     uint32_t r[NB / 4];
     if constexpr (NB == 16) {
@@ -171,16 +183,16 @@ __device__ __forceinline__ void k_row_words(const LD& ld, int row, int c, uint32
       const uint2 u = ld.v2(row + c * NB);
       r[0] = u.x; r[1] = u.y;
     }
-    const uint32_t mul = 0x2C003C00u;  // (1, 1/16)
-    const uint32_t add = 0xD480E408u;  // (-1032, -72)
 #pragma unroll
-    for (int i = 0; i < NB / 4; ++i)
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const uint32_t t = __byte_perm(r[i], 0, b * 0x1111);
-        kw[4 * i + b] = hfma2u(lop3_and_or(t, 0x00F0000Fu, H_MAGIC), mul, add);
-      }
+    for (int w = 0; w < NB / 4; ++w) {
+      const uint32_t r8 = shr8(r[w]);
+      kw[4 * w + 0] = hsub2u(lop3_and_or(r[w], 0x000F000Fu, H_MAGIC), H_1032);
+      kw[4 * w + 1] = hfma2u(lop3_and_or(r[w], 0x00F000F0u, H_MAGIC), H_Q16, H_M72);
+      kw[4 * w + 2] = hsub2u(lop3_and_or(r8, 0x000F000Fu, H_MAGIC), H_1032);
+      kw[4 * w + 3] = hfma2u(lop3_and_or(r8, 0x00F000F0u, H_MAGIC), H_Q16, H_M72);
+    }
   } else if constexpr (KB == 2) {
+    // Word w holds channels 16w..16w+15; out pairs (k, k+8), k = 0..7.
     constexpr int NB = KCH / 4;
     uint32_t r[NB / 4];
     if constexpr (NB == 8) {
@@ -189,18 +201,17 @@ __device__ __forceinline__ void k_row_words(const LD& ld, int row, int c, uint32
     } else {
       r[0] = ld.v1(row + c * NB);
     }
-    const uint32_t mul_lo = 0x34003C00u;  // (1, 1/4)
-    const uint32_t add_lo = 0xDC08E402u;  // (-1026, -258)
-    const uint32_t mul_hi = 0x24002C00u;  // (1/16, 1/64)
-    const uint32_t add_hi = 0xCC80D420u;  // (-66, -18)
 #pragma unroll
-    for (int i = 0; i < NB / 4; ++i)
+    for (int w = 0; w < NB / 4; ++w) {
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const uint32_t t = __byte_perm(r[i], 0, b * 0x1111);
-        kw[8 * i + 2 * b] = hfma2u(lop3_and_or(t, 0x000C0003u, H_MAGIC), mul_lo, add_lo);
-        kw[8 * i + 2 * b + 1] = hfma2u(lop3_and_or(t, 0x00C00030u, H_MAGIC), mul_hi, add_hi);
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t x = h ? shr8(r[w]) : r[w];
+        kw[8 * w + 4 * h + 0] = hsub2u(lop3_and_or(x, 0x00030003u, H_MAGIC), H_1026);
+        kw[8 * w + 4 * h + 1] = hfma2u(lop3_and_or(x, 0x000C000Cu, H_MAGIC), H_Q4, H_M258);
+        kw[8 * w + 4 * h + 2] = hfma2u(lop3_and_or(x, 0x00300030u, H_MAGIC), H_Q16, H_M66);
+        kw[8 * w + 4 * h + 3] = hfma2u(lop3_and_or(x, 0x00C000C0u, H_MAGIC), H_Q64, H_M18);
       }
+    }
   } else if constexpr (KB == 8) {
     constexpr int NB = KCH;
 #pragma unroll
@@ -250,24 +261,28 @@ __device__ __forceinline__ void v_pair_words(const LD& ld, int r0, int r1, uint3
   if constexpr (VB == 4) {
 #pragma unroll
     for (int w = 0; w < NWD; ++w) {
-      const uint32_t x = __byte_perm(a[w], b[w], 0x5410);
-      const uint32_t y = __byte_perm(a[w], b[w], 0x7632);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        vw[8 * w + k] = hsub2u(lop3_and_or(x >> (4 * k), 0x000F000Fu, H_MAGIC), H_1032);
-        vw[8 * w + 4 + k] = hsub2u(lop3_and_or(y >> (4 * k), 0x000F000Fu, H_MAGIC), H_1032);
+      for (int h = 0; h < 2; ++h) {  // channels 8w+4h .. 8w+4h+3
+        const uint32_t x = __byte_perm(a[w], b[w], h ? 0x7632 : 0x5410);
+        const uint32_t x8 = shr8(x);
+        vw[8 * w + 4 * h + 0] = hsub2u(lop3_and_or(x, 0x000F000Fu, H_MAGIC), H_1032);
+        vw[8 * w + 4 * h + 1] = hfma2u(lop3_and_or(x, 0x00F000F0u, H_MAGIC), H_Q16, H_M72);
+        vw[8 * w + 4 * h + 2] = hsub2u(lop3_and_or(x8, 0x000F000Fu, H_MAGIC), H_1032);
+        vw[8 * w + 4 * h + 3] = hfma2u(lop3_and_or(x8, 0x00F000F0u, H_MAGIC), H_Q16, H_M72);
       }
     }
   } else if constexpr (VB == 2) {
-    const uint32_t x = __byte_perm(a[0], b[0], 0x5410);
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-      vw[k] = hsub2u(lop3_and_or(x >> (2 * k), 0x00030003u, H_MAGIC), H_1026);
-    if constexpr (VCH == 16) {
-      const uint32_t y = __byte_perm(a[0], b[0], 0x7632);
+    for (int h = 0; h < VCH / 8; ++h) {  // channels 8h .. 8h+7
+      const uint32_t x = __byte_perm(a[0], b[0], h ? 0x7632 : 0x5410);
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        vw[8 + k] = hsub2u(lop3_and_or(y >> (2 * k), 0x00030003u, H_MAGIC), H_1026);
+      for (int q = 0; q < 2; ++q) {
+        const uint32_t y = q ? shr8(x) : x;
+        vw[8 * h + 4 * q + 0] = hsub2u(lop3_and_or(y, 0x00030003u, H_MAGIC), H_1026);
+        vw[8 * h + 4 * q + 1] = hfma2u(lop3_and_or(y, 0x000C000Cu, H_MAGIC), H_Q4, H_M258);
+        vw[8 * h + 4 * q + 2] = hfma2u(lop3_and_or(y, 0x00300030u, H_MAGIC), H_Q16, H_M66);
+        vw[8 * h + 4 * q + 3] = hfma2u(lop3_and_or(y, 0x00C000C0u, H_MAGIC), H_Q64, H_M18);
+      }
     }
   } else if constexpr (VB == 8) {
 #pragma unroll
@@ -292,6 +307,47 @@ struct Acc {
   float o[D / 16][4];
   float m0, m1, l0, l1;
 };
+
+// K code pairing of a page format: 0 = adjacent channels (8- and 16-bit pages),
+// 1 = (k, k+4) within 8 channels (4-bit), 2 = (k, k+8) within 16 channels (2-bit).
+template <int KB>
+__host__ __device__ constexpr int pair_class() { return KB == 4 ? 1 : KB == 2 ? 2 : 0; }
+
+// Q words of head g over this thread's channel chunk, paired like the K codes of
+// pairing class pc (zero for padding heads).
+template <int D>
+__device__ __forceinline__ void load_q(const __half* qp, bool valid, int pc, uint32_t* qw) {
+  constexpr int KW = D / 8;
+  uint32_t nat[KW];
+  if (valid) {
+#pragma unroll
+    for (int i = 0; i < KW / 4; ++i) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(qp) + i);
+      nat[4 * i] = u.x; nat[4 * i + 1] = u.y; nat[4 * i + 2] = u.z; nat[4 * i + 3] = u.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < KW; ++i) nat[i] = 0u;
+  }
+  if (pc == 1) {
+#pragma unroll
+    for (int w = 0; w < KW / 4; ++w)
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        qw[4 * w + k] = __byte_perm(nat[4 * w + k / 2], nat[4 * w + 2 + k / 2],
+                                    (k & 1) ? 0x7632 : 0x5410);
+  } else if (pc == 2) {
+#pragma unroll
+    for (int w = 0; w < KW / 8; ++w)
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        qw[8 * w + k] = __byte_perm(nat[8 * w + k / 2], nat[8 * w + 4 + k / 2],
+                                    (k & 1) ? 0x7632 : 0x5410);
+  } else {
+#pragma unroll
+    for (int i = 0; i < KW; ++i) qw[i] = nat[i];
+  }
+}
 
 // S^T[16 tokens x 8 heads] of one page into s[4] (C fragment: tokens g, g+8 x
 // heads 2c, 2c+1).  KB bits (raw fp16 if 16); the K part is read through kl.
@@ -451,6 +507,97 @@ __device__ __forceinline__ void with_kbits(int kb, F&& f) {
   }
 }
 
+// Merge `count` split partials at slots pbase + first + j*stride (j < count):
+// (max, sum) pairs are staged in shared memory and turned into per-slot weights
+// 2^(m_j - M), then every thread streams its own output columns, four slots per
+// round.  With `orow` set the result is normalized and written to O as fp16;
+// otherwise the unnormalized (M, L, numerator) goes to slot `dst`.
+template <int D>
+__device__ void merge_parts(const DevState& st, size_t pbase, int first, int stride, int count,
+                            int G, uint8_t* smem, int tid, int lane, int warp, __half* orow,
+                            size_t dst) {
+  constexpr int PER = (MAX_G * D + NT - 1) / NT;   // output elements per thread
+  float* s_w = reinterpret_cast<float*>(smem);     // [count][MAX_G] weights
+  float* s_l = s_w + (size_t)count * MAX_G;        // [count][MAX_G] sums
+  float* s_ml = s_l + (size_t)count * MAX_G;       // [MAX_G][2] merged (max, sum)
+  for (int i = tid; i < count * G; i += NT) {
+    const int j = i / G, hd = i % G;
+    const size_t pid = pbase + first + (size_t)j * stride;
+    s_w[j * MAX_G + hd] = __ldcg(st.attn_ml + (pid * G + hd) * 2);
+    s_l[j * MAX_G + hd] = __ldcg(st.attn_ml + (pid * G + hd) * 2 + 1);
+  }
+  __syncthreads();
+  for (int hd = warp; hd < G; hd += NW) {
+    float M = -CUDART_INF_F;
+    for (int j = lane; j < count; j += 32) M = fmaxf(M, s_w[j * MAX_G + hd]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float L = 0.f;
+    for (int j = lane; j < count; j += 32) {
+      const float mj = s_w[j * MAX_G + hd];
+      const float f = (mj == -CUDART_INF_F) ? 0.f : exp2f(mj - M);
+      s_w[j * MAX_G + hd] = f;
+      L += f * s_l[j * MAX_G + hd];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    __syncwarp();
+    if (orow) {
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      for (int j = lane; j < count; j += 32) s_w[j * MAX_G + hd] *= inv;
+    } else if (lane == 0) {
+      s_ml[2 * hd] = M;
+      s_ml[2 * hd + 1] = L;
+    }
+  }
+  __syncthreads();
+  float acc[PER];
+#pragma unroll
+  for (int r = 0; r < PER; ++r) acc[r] = 0.f;
+  const int GD = G * D;
+  const float* accp = st.attn_acc + (pbase + first) * GD;
+  const size_t step = (size_t)stride * GD;
+  int j = 0;
+  if (GD == PER * NT) {
+    for (; j + 4 <= count; j += 4) {
+#pragma unroll
+      for (int r = 0; r < PER; ++r) {
+        const int i = tid + r * NT;
+        const float* pa = accp + (size_t)j * step + i;
+        const float a0 = __ldcg(pa), a1 = __ldcg(pa + step), a2 = __ldcg(pa + 2 * step),
+                    a3 = __ldcg(pa + 3 * step);
+        const int hd = i / D;
+        float t = acc[r];
+        t = fmaf(s_w[j * MAX_G + hd], a0, t);
+        t = fmaf(s_w[(j + 1) * MAX_G + hd], a1, t);
+        t = fmaf(s_w[(j + 2) * MAX_G + hd], a2, t);
+        acc[r] = fmaf(s_w[(j + 3) * MAX_G + hd], a3, t);
+      }
+    }
+  }
+  for (; j < count; ++j) {
+#pragma unroll
+    for (int r = 0; r < PER; ++r) {
+      const int i = tid + r * NT;
+      if (i < GD) acc[r] = fmaf(s_w[j * MAX_G + i / D], __ldcg(accp + (size_t)j * step + i), acc[r]);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < PER; ++r) {
+    const int i = tid + r * NT;
+    if (i >= GD) continue;
+    if (orow) {
+      orow[i] = __float2half_rn(acc[r]);
+    } else {
+      st.attn_acc[dst * GD + i] = acc[r];
+      if (i % D == 0) {
+        st.attn_ml[(dst * G + i / D) * 2] = s_ml[2 * (i / D)];
+        st.attn_ml[(dst * G + i / D) * 2 + 1] = s_ml[2 * (i / D) + 1];
+      }
+    }
+  }
+}
+
 template <int D, int VB>
 __global__ void __launch_bounds__(NT, AttnCfg<VB>::CTAS)
 decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
@@ -473,19 +620,19 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   const int b0 = min(nb, split * cb), b1 = min(nb, b0 + cb);
   const bool has_open = (T % BLOCK) != 0;
 
-  // Q fragment words for head g of the group (zero for padding heads)
+  // Q fragment words for head g of the group, paired like the K codes of the
+  // page format in use (re-paired when a page of another pairing class comes).
+  const __half* qrow = q + ((size_t)z * st.Hq + h * G + (g < G ? g : 0)) * D + c * KCH;
   uint32_t qw[KW];
-  if (g < G) {
-    const uint4* qp = reinterpret_cast<const uint4*>(q + ((size_t)z * st.Hq + h * G + g) * D + c * KCH);
-#pragma unroll
-    for (int i = 0; i < KW / 4; ++i) {
-      const uint4 u = __ldg(qp + i);
-      qw[4 * i] = u.x; qw[4 * i + 1] = u.y; qw[4 * i + 2] = u.z; qw[4 * i + 3] = u.w;
+  int qpc = 0;
+  load_q<D>(qrow, g < G, 0, qw);
+  auto pair_q = [&](auto kbc) {
+    constexpr int PC = pair_class<decltype(kbc)::value>();
+    if (qpc != PC) {
+      load_q<D>(qrow, g < G, PC, qw);
+      qpc = PC;
     }
-  } else {
-#pragma unroll
-    for (int i = 0; i < KW; ++i) qw[i] = 0u;
-  }
+  };
 
   Acc<D> A;
 #pragma unroll
@@ -514,11 +661,18 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   // This warp's blocks: b0 + warp + k*NW for k < nk.  Pages of sealed blocks go
   // through the pipeline; the open block (always the sequence's last) does not.
   const int nk = (b1 - b0 > warp) ? (b1 - b0 - warp + NW - 1) / NW : 0;
-  auto issue = [&](int k, int sidx) {  // lane 0 only; block k goes to stage sidx
+  // Page-table entries of this warp's blocks, a window of 64 ahead in two lane
+  // registers (lane j: blocks wb + j and wb + 32 + j), read with one shuffle.
+  auto bt_at = [&](int k) -> int32_t { return k < nk ? bt[b0 + warp + k * NW] : -1; };
+  int wb = 0;
+  int32_t ecur = bt_at(lane), enext = bt_at(32 + lane);
+  auto entry = [&](int k) -> int32_t {  // warp-uniform k in [wb, wb + 64)
+    const int j = k - wb;
+    return __shfl_sync(0xffffffffu, j < 32 ? ecur : enext, j & 31);
+  };
+  auto issue = [&](int k, int sidx, int32_t e) {  // lane 0 only; block k -> stage sidx
     const int blk = b0 + warp + k * NW;
-    if (has_open && blk == nb - 1) return;
-    const int32_t e = bt[blk];
-    if (e == -1) return;
+    if ((has_open && blk == nb - 1) || e == -1) return;
     const int fmt = entry_fmt(e);
     const uint32_t bytes = (uint32_t)st.pool_page_bytes[fmt];
     const uint8_t* src = st.pool_base[fmt] + (size_t)entry_idx(e) * bytes;
@@ -526,8 +680,10 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
     mbar_expect_tx(bar0 + 8 * sidx, bytes);
     bulk_g2s(wbase + sidx * stage_bytes, src, bytes, bar0 + 8 * sidx);
   };
-  if (lane == 0)
-    for (int k = 0; k < min(ns, nk); ++k) issue(k, k);
+  for (int k = 0; k < min(ns, nk); ++k) {
+    const int32_t e = entry(k);
+    if (lane == 0) issue(k, k, e);
+  }
 
   // `issued`: blocks k < issued had issue() called (warp-uniform).  After a wait
   // times out the warp stops issuing and computing but still waits, each wait
@@ -543,7 +699,7 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   // Wait for block k's page; returns its entry, or -1 when it has no page or the
   // wait failed (then nothing is computed for it).
   auto acquire = [&](int k, int si) -> int32_t {
-    const int32_t e = bt[b0 + warp + k * NW];
+    const int32_t e = entry(k);
     if (e == -1) {
       if (lane == 0) set_error(st, EKV_ESTATE);
       return -1;
@@ -558,11 +714,17 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   };
   auto refill = [&](int k, int si) {  // after block k's stage is consumed
     if (ok && k + ns < nk) {
-      if (lane == 0) issue(k + ns, si);
+      const int32_t e = entry(k + ns);
+      if (lane == 0) issue(k + ns, si, e);
       issued = k + ns + 1;
     }
   };
   for (int k = 0; k < np; k += 2) {
+    if (k >= wb + 32) {  // slide the entry window; the next half was loaded 32 blocks ago
+      wb += 32;
+      ecur = enext;
+      enext = bt_at(wb + 32 + lane);
+    }
     const int s0 = sidx, s1 = (sidx + 1 == ns) ? 0 : sidx + 1;
     const bool two = k + 1 < np;
     const int32_t ea = acquire(k, s0);
@@ -575,6 +737,7 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
       with_kbits(kba, [&](auto kbc) {
         constexpr int KB = decltype(kbc)::value;
         constexpr int KP = k_part_bytes(KB, D);
+        pair_q(kbc);
         attend_pages<D, VB, true, KB>(SLd{sa}, SLd{sa + KP}, BLOCK, SLd{sb}, SLd{sb + KP},
                                       BLOCK, qw, A, sl, g, c);
       });
@@ -582,12 +745,14 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
       if (kba != 0)
         with_kbits(kba, [&](auto kbc) {
           constexpr int KB = decltype(kbc)::value;
+          pair_q(kbc);
           attend_pages<D, VB, true, KB>(SLd{sa}, SLd{sa + k_part_bytes(KB, D)}, BLOCK, SLd{sa},
                                         SLd{sa}, 0, qw, A, sl, g, c);
         });
       if (kbb != 0)
         with_kbits(kbb, [&](auto kbc) {
           constexpr int KB = decltype(kbc)::value;
+          pair_q(kbc);
           attend_pages<D, VB, true, KB>(SLd{sb}, SLd{sb + k_part_bytes(KB, D)}, BLOCK, SLd{sb},
                                         SLd{sb}, 0, qw, A, sl, g, c);
         });
@@ -606,6 +771,7 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
       const uint8_t* page = st.pool_base[fmt] + (size_t)entry_idx(e) * st.pool_page_bytes[fmt];
       const GLd kl{reinterpret_cast<const uint8_t*>(stg)};
       const GLd vl{page + k_part_bytes(bits_of_code(fmt >> 2), D)};
+      pair_q(KBits<16>{});
       attend_pages<D, VB, false, 16>(kl, vl, T % BLOCK, kl, vl, 0, qw, A, sl, g, c);
     }
   }
@@ -658,89 +824,42 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   }
   if (splits == 1) return;
 
-  // ---- last CTA of this (seq, kv head) merges the splits ---------------------------
+  // ---- two-level merge of the splits --------------------------------------------------
+  // Splits form groups of ATTN_GROUP; the last CTA of a group to finish merges the
+  // group into the slot of its first split, and the last group merger merges the
+  // group results into O.  Each merge reads at most ATTN_GROUP or ATTN_MAXGRP
+  // partials, so no single CTA streams all of them.  Tickets never wait.
+  const int grp = split / ATTN_GROUP, ngrp = (splits + ATTN_GROUP - 1) / ATTN_GROUP;
+  const int gsize = min(ATTN_GROUP, splits - grp * ATTN_GROUP);
+  int* tk = st.attn_ticket + ((size_t)z * st.Hkv + h) * ATTN_TICKETS;
   __threadfence();
   __syncthreads();
   if (tid == 0) {
-    int* tk = st.attn_ticket + (size_t)z * st.Hkv + h;
-    const int t = atomicAdd(tk, 1);
-    s_last = (t == splits - 1);
-    if (s_last) *tk = 0;
+    const int t = atomicAdd(tk + 1 + grp, 1);
+    s_last = (t == gsize - 1);
+    if (s_last) tk[1 + grp] = 0;
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  // Stage every split's (max, sum) in shared memory, turn them into per-split
-  // weights 2^(m_j - M) / L once per head, then sum the numerators with every
-  // thread streaming its own columns (many independent loads in flight).
-  float* s_w = reinterpret_cast<float*>(smem);          // [splits][MAX_G] weights
-  float* s_l = s_w + (size_t)splits * MAX_G;            // [splits][MAX_G] sums
-  for (int i = tid; i < splits * G; i += NT) {
-    const int j = i / G, hd = i % G;
-    s_w[j * MAX_G + hd] = __ldcg(st.attn_ml + ((pbase + j) * G + hd) * 2);
-    s_l[j * MAX_G + hd] = __ldcg(st.attn_ml + ((pbase + j) * G + hd) * 2 + 1);
+  __half* orow = o + ((size_t)z * st.Hq + h * G) * D;
+  if (ngrp == 1) {
+    merge_parts<D>(st, pbase, 0, 1, splits, G, smem, tid, lane, warp, orow, 0);
+    return;
+  }
+  merge_parts<D>(st, pbase, grp * ATTN_GROUP, 1, gsize, G, smem, tid, lane, warp, nullptr,
+                 pbase + grp * ATTN_GROUP);
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int t = atomicAdd(tk, 1);
+    s_last = (t == ngrp - 1);
+    if (s_last) tk[0] = 0;
   }
   __syncthreads();
-  for (int hd = warp; hd < G; hd += NW) {
-    float M = -CUDART_INF_F;
-    for (int j = lane; j < splits; j += 32) M = fmaxf(M, s_w[j * MAX_G + hd]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float L = 0.f;
-    for (int j = lane; j < splits; j += 32) {
-      const float mj = s_w[j * MAX_G + hd];
-      const float f = (mj == -CUDART_INF_F) ? 0.f : exp2f(mj - M);
-      s_w[j * MAX_G + hd] = f;
-      L += f * s_l[j * MAX_G + hd];
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-    __syncwarp();
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    for (int j = lane; j < splits; j += 32) s_w[j * MAX_G + hd] *= inv;
-  }
-  __syncthreads();
-  constexpr int PER = (MAX_G * D + NT - 1) / NT;   // output elements per thread
-  float out_acc[PER];
-#pragma unroll
-  for (int r = 0; r < PER; ++r) out_acc[r] = 0.f;
-  // Four splits per round without predicates (the remainder runs one by one),
-  // so 4 * PER independent loads are in flight per thread.
-  const float* accp = st.attn_acc + pbase * G * D;
-  const int GD = G * D;
-  int j = 0;
-  if (GD == PER * NT) {
-    for (; j + 4 <= splits; j += 4) {
-#pragma unroll
-      for (int r = 0; r < PER; ++r) {
-        const int i = tid + r * NT;
-        const float* pa = accp + (size_t)j * GD + i;
-        const float a0 = __ldcg(pa), a1 = __ldcg(pa + GD), a2 = __ldcg(pa + 2 * GD),
-                    a3 = __ldcg(pa + 3 * GD);
-        const int hd = i / D;
-        float t = out_acc[r];
-        t = fmaf(s_w[j * MAX_G + hd], a0, t);
-        t = fmaf(s_w[(j + 1) * MAX_G + hd], a1, t);
-        t = fmaf(s_w[(j + 2) * MAX_G + hd], a2, t);
-        out_acc[r] = fmaf(s_w[(j + 3) * MAX_G + hd], a3, t);
-      }
-    }
-  }
-  for (; j < splits; ++j) {
-#pragma unroll
-    for (int r = 0; r < PER; ++r) {
-      const int i = tid + r * NT;
-      if (i < GD) out_acc[r] = fmaf(s_w[j * MAX_G + i / D], __ldcg(accp + (size_t)j * GD + i), out_acc[r]);
-    }
-  }
-#pragma unroll
-  for (int r = 0; r < PER; ++r) {
-    const int i = tid + r * NT;
-    if (i < G * D) {
-      const int hd = i / D, ch = i % D;
-      o[((size_t)z * st.Hq + h * G + hd) * D + ch] = __float2half_rn(out_acc[r]);
-    }
-  }
+  if (!s_last) return;
+  __threadfence();
+  merge_parts<D>(st, pbase, 0, ATTN_GROUP, ngrp, G, smem, tid, lane, warp, orow, 0);
 }
 
 template <int D, int VB>

@@ -46,7 +46,7 @@ int attn_splits(const ekv_cache* c, int n_seqs, int vb) {
   const int target = attn_ctas_per_sm(vb) * c->num_sm;
   int s = (target + units - 1) / units;
   if (s < 1) s = 1;
-  if (s > 512) s = 512;
+  if (s > ATTN_MAX_SPLITS) s = ATTN_MAX_SPLITS;
   return s;
 }
 
@@ -169,7 +169,7 @@ int ekv_create(const ekv_config* cfg, const uint8_t* k_bits_init, const uint8_t*
   st.attn_parts_cap = parts;
   st.attn_acc = (float*)A((size_t)parts * MAX_G * D * 4);
   st.attn_ml = (float*)A((size_t)parts * MAX_G * 2 * 4);
-  st.attn_ticket = (int32_t*)A(S * H * 4);
+  st.attn_ticket = (int32_t*)A(S * H * ATTN_TICKETS * 4);
   st.canary_part = (float*)A(S * H * 3 * 4);
   st.canary_ticket = (int32_t*)A(L * 4);
   if (!ok) {
@@ -207,7 +207,7 @@ int ekv_create(const ekv_config* cfg, const uint8_t* k_bits_init, const uint8_t*
   Z(st.delta, L * 3 * 4);
   Z(st.err, 4);
   Z(st.append_ticket, L * S * 4);
-  Z(st.attn_ticket, S * H * 4);
+  Z(st.attn_ticket, S * H * ATTN_TICKETS * 4);
   Z(st.canary_ticket, L * 4);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {

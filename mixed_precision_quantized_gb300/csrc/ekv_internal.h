@@ -13,6 +13,10 @@ constexpr int BLOCK = EKV_BLOCK_TOKENS;  // tokens per page
 constexpr int RING = EKV_RING_LEN;       // K vectors per ring
 constexpr int NFMT = EKV_NUM_FORMATS;
 constexpr int MAX_G = 8;                  // query heads per KV head handled by one CTA
+constexpr int ATTN_MAX_SPLITS = 512;      // decode-attention splits per (sequence, KV head)
+constexpr int ATTN_GROUP = 8;             // splits merged together at the first level
+constexpr int ATTN_MAXGRP = ATTN_MAX_SPLITS / ATTN_GROUP;
+constexpr int ATTN_TICKETS = 1 + ATTN_MAXGRP;  // merge tickets per (sequence, KV head)
 
 __host__ __device__ inline int bits_of_code(int code) { return 2 << code; }
 __host__ __device__ inline int code_of_bits(int b) {
@@ -58,7 +62,7 @@ struct DevState {
   int32_t* append_ticket;   // [L][S]
   float* attn_acc;          // [parts][G][D]   split partial numerators
   float* attn_ml;           // [parts][G][2]   split partial (max, sum), log2 domain
-  int32_t* attn_ticket;     // [S][Hkv]
+  int32_t* attn_ticket;     // [S][Hkv][ATTN_TICKETS] merge tickets (head, then groups)
   int32_t attn_parts_cap;
   float* canary_part;       // [S*Hkv][3]
   int32_t* canary_ticket;   // [L]

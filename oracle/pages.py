@@ -15,6 +15,12 @@ Layout (our storage reading; the pages only say "packed low-bit storage"):
     V part  vb < 16 : codes [16][d*vb/8]  then scales [16] fp16 (per token)
             vb = 16 : raw fp16 [16][d]
     page  = K part || V part            (little-endian fp16)
+
+The K scales of 2- and 4-bit pages are stored in "pair order": within each
+group of n = 32/kb channels (the channels of one 32-bit code word), scale
+position p holds channel p // 2 + (p % 2) * n / 2, i.e. 0, n/2, 1, n/2+1, ...
+(4 bits: 0,4,1,5,2,6,3,7; 2 bits: 0,8,1,9,...,7,15).  8-bit pages keep the
+natural channel order.
 """
 from __future__ import annotations
 
@@ -54,6 +60,15 @@ def regions(kb: int, vb: int, d: int) -> dict:
     return r
 
 
+def scale_order(kb: int, d: int) -> np.ndarray:
+    """Channel stored at each K-scale position of a kb-bit page."""
+    if kb not in (2, 4):
+        return np.arange(d)
+    n = 32 // kb
+    p = np.arange(d)
+    return (p // n) * n + (p % n) // 2 + (p % 2) * (n // 2)
+
+
 def sealed_k_bytes(kb: int, k16: np.ndarray) -> dict:
     """Expected bytes of a full page's K part from its 16 raw fp16 rows [16, d]."""
     k16 = np.asarray(k16, dtype=np.float16)
@@ -61,6 +76,7 @@ def sealed_k_bytes(kb: int, k16: np.ndarray) -> dict:
     if kb == 16:
         return {"k_raw": k16.view(np.uint8).reshape(BLOCK, -1)}
     q, s = quant.quantize(k16, kb, axis=0)          # one group per channel
+    s = s[scale_order(kb, k16.shape[1])]
     return {"k_codes": quant.pack(q, kb), "k_scales": s.astype(np.float16).view(np.uint8)[None, :]}
 
 

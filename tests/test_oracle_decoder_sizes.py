@@ -86,8 +86,24 @@ def test_page_expect_regions_decode():
     q = quant.unpack(e["k_codes"], 4, 64)
     s = np.frombuffer(e["k_scales"].tobytes(), dtype=F16)
     q2, s2 = quant.quantize(k[:, 1], 4, axis=0)
-    assert np.array_equal(q, q2) and np.array_equal(s, s2)
+    assert np.array_equal(q, q2)
+    # 4-bit pages store each 8-channel group's scales as 0,4,1,5,2,6,3,7
+    for grp in range(8):
+        want = [8 * grp + c for c in (0, 4, 1, 5, 2, 6, 3, 7)]
+        assert np.array_equal(s[8 * grp:8 * grp + 8], s2[want])
     assert e["v_codes"].shape == (16, 64) and e["v_scales"].shape == (16, 2)
+
+
+def test_scale_pair_order():
+    # position p of a group of n = 32/b channels holds channel p//2 + (p%2)*n/2
+    assert pages.scale_order(4, 16).tolist() == [0, 4, 1, 5, 2, 6, 3, 7,
+                                                   8, 12, 9, 13, 10, 14, 11, 15]
+    assert pages.scale_order(2, 16).tolist() == [0, 8, 1, 9, 2, 10, 3, 11,
+                                                   4, 12, 5, 13, 6, 14, 7, 15]
+    assert pages.scale_order(8, 8).tolist() == list(range(8))
+    for b in (2, 4):
+        o = pages.scale_order(b, 128)
+        assert sorted(o.tolist()) == list(range(128))     # a permutation
 
 
 def test_tiny_trace_properties():
