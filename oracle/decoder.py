@@ -33,61 +33,104 @@ RING = 64
 
 
 class SeqState:
-    """Cache of one (layer, sequence) restricted to a list of KV heads."""
+    """Cache of one (layer, sequence) restricted to a list of KV heads.
+
+    Raw fp16 K/V of every token are kept in arrays that grow by doubling.
+    Dequantized values of sealed K blocks and of V rows are computed once
+    from the raw rows and kept (both are pure functions of rows that never
+    change once written).
+    """
 
     def __init__(self, n_heads: int, d: int, vbits: int):
-        self.k = np.zeros((0, n_heads, d), dtype=np.float16)
-        self.v = np.zeros((0, n_heads, d), dtype=np.float16)
+        self.H, self.d = n_heads, d
+        self._k = np.zeros((0, n_heads, d), dtype=np.float16)
+        self._v = np.zeros((0, n_heads, d), dtype=np.float16)
+        self._kh = np.zeros((0, n_heads, d), dtype=np.float32)   # sealed K, dequantized
+        self._vh = np.zeros((0, n_heads, d), dtype=np.float32)   # V, dequantized
+        self.n = 0
+        self._sealed_upto = 0      # blocks [0, _sealed_upto) hold dequantized K in _kh
+        self._vh_upto = 0          # tokens [0, _vh_upto) hold dequantized V in _vh
         self.kbits: list = []      # admit-time K bits per block
         self.vbits = vbits
-        self._sealed = {}          # block -> dequantized K of a sealed block (never changes)
 
     @property
     def T(self) -> int:
-        return self.k.shape[0]
+        return self.n
+
+    @property
+    def k(self) -> np.ndarray:
+        return self._k[:self.n]
+
+    @property
+    def v(self) -> np.ndarray:
+        return self._v[:self.n]
+
+    def _grow(self, need: int):
+        cap = self._k.shape[0]
+        if need <= cap:
+            return
+        cap = max(need, 2 * cap, 64)
+        for name, dt in (("_k", np.float16), ("_v", np.float16), ("_kh", np.float32),
+                         ("_vh", np.float32)):
+            old = getattr(self, name)
+            new = np.zeros((cap, self.H, self.d), dtype=dt)
+            new[:old.shape[0]] = old
+            setattr(self, name, new)
 
     def append(self, k16: np.ndarray, v16: np.ndarray, tier: int):
         k16 = np.asarray(k16, dtype=np.float16)
         v16 = np.asarray(v16, dtype=np.float16)
-        for p in range(self.T, self.T + k16.shape[0]):
+        n = k16.shape[0]
+        for p in range(self.n, self.n + n):
             if p % BLOCK == 0:
                 self.kbits.append(int(tier))
-        self.k = np.concatenate([self.k, k16], axis=0)
-        self.v = np.concatenate([self.v, v16], axis=0)
+        self._grow(self.n + n)
+        self._k[self.n:self.n + n] = k16
+        self._v[self.n:self.n + n] = v16
+        self.n += n
 
     def khat(self) -> np.ndarray:
         """Stored K values [T, H, d] fp32: sealed blocks dequantized, open rows raw."""
-        out = self.k.astype(np.float32)
-        T = self.T
-        for j, kb in enumerate(self.kbits):
+        T = self.n
+        full = T // BLOCK
+        for j in range(self._sealed_upto, full):
             lo, hi = j * BLOCK, (j + 1) * BLOCK
-            if hi > T or kb == 16:
-                continue
-            if j not in self._sealed:
-                q, s = quant.quantize(self.k[lo:hi], kb, axis=0)
-                self._sealed[j] = quant.dequantize(q, s, axis=0)
-            out[lo:hi] = self._sealed[j]
+            kb = self.kbits[j]
+            if kb == 16:
+                self._kh[lo:hi] = self._k[lo:hi].astype(np.float32)
+            else:
+                q, s = quant.quantize(self._k[lo:hi], kb, axis=0)
+                self._kh[lo:hi] = quant.dequantize(q, s, axis=0)
+        self._sealed_upto = max(self._sealed_upto, full)
+        out = self._kh[:T].copy()
+        out[full * BLOCK:T] = self._k[full * BLOCK:T].astype(np.float32)
         return out
 
     def vhat(self) -> np.ndarray:
-        if self.vbits == 16:
-            return self.v.astype(np.float32)
-        q, s = quant.quantize(self.v, self.vbits, axis=2)
-        return quant.dequantize(q, s, axis=2)
+        T = self.n
+        lo = self._vh_upto
+        if T > lo:
+            if self.vbits == 16:
+                self._vh[lo:T] = self._v[lo:T].astype(np.float32)
+            else:
+                q, s = quant.quantize(self._v[lo:T], self.vbits, axis=2)
+                self._vh[lo:T] = quant.dequantize(q, s, axis=2)
+            self._vh_upto = T
+        return self._vh[:T]
 
     def window(self) -> np.ndarray:
         """The K_ref ring contents [n, H, d], oldest first (n = min(T, 64))."""
-        return self.k[max(0, self.T - RING):self.T]
+        return self.k[max(0, self.n - RING):self.n]
 
     def page_expect(self, j: int, h: int) -> dict:
         """Expected bytes of the defined regions of page j, head index h."""
         kb = self.kbits[j]
         lo = j * BLOCK
-        hi = min(lo + BLOCK, self.T)
+        hi = min(lo + BLOCK, self.n)
         exp = {}
         if hi - lo == BLOCK:
-            exp.update(pages.sealed_k_bytes(kb, self.k[lo:hi, h]))
-        exp.update(pages.v_rows_bytes(self.vbits, self.v[lo:hi, h]))
+            exp.update(pages.sealed_k_bytes(kb, self._k[lo:hi, h]))
+        exp.update(pages.v_rows_bytes(self.vbits, self._v[lo:hi, h]))
         return exp
 
 
