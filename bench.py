@@ -39,6 +39,13 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "quantized-KV decode attn HBM GB/s (% of peak), tokens/s; canary µs/firing"
+
+# DRAM bytes (read + write) per decode-attention launch from one ncu capture
+# (profiles/decode_attn_llama70b_128k.md: 2-layer case, the same per-launch
+# work as one layer of the full workload), valid only for the kernel source it
+# was taken on: any change to that source reports null until re-captured.
+TRAFFIC_BYTES = 157.5e6
+TRAFFIC_SOURCE_SHA = "497cffd04d4bcf8d"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -56,6 +63,15 @@ def parse():
                    help="run only the first N layers of the workload (profiling cases)")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     return p.parse_args()
+
+
+def attn_source_sha() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("ekv_attn.cu", "ekv_internal.h"):
+        with open(os.path.join(ROOT, "mixed_precision_quantized_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 def peaks():
@@ -421,7 +437,10 @@ def main():
         "canary_overhead_frac_at_1_in_64": canary_us * 1e-6 / 64 / (tA / K),
         "prefill_s": prefill_s,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak if achieved else None, "traffic": None,
+                     "frac": achieved / peak if achieved else None,
+                     "traffic": (TRAFFIC_BYTES if attn_source_sha() == TRAFFIC_SOURCE_SHA
+                                 and w.name == "llama70b_128k" and not a.layers else None),
+                     "traffic_unit": "bytes per launch",
                      "kernel": "decode_attn_kernel", "peak_kind": peak_kind,
                      "bytes_per_launch": bytes_per_launch,
                      "avg_launch_us": attn_avg_s * 1e6 if attn_avg_s else None,
