@@ -234,7 +234,20 @@ __device__ __forceinline__ void k_row_words(const LD& ld, int row, int c, uint32
 }
 
 // ---- V: token pair (t, t+1), chunk of VCH = D/8 channels -> VCH words -------------
-// Word i = (v[t][ch i], v[t+1][ch i]) as exact fp16 integers (raw for 16 bits).
+// Word i = (v[t][ch i], v[t+1][ch i]).  For quantized V the words hold the
+// *biased* codes the exponent trick yields, A_i = vmul(i) * q + vbias(i) (exact
+// fp16 integers); the bias is removed once per warp at the end (see Acc::ps).
+// Raw fp16 for 16-bit V.
+template <int VB>
+__host__ __device__ constexpr float vmul(int i) {
+  return VB == 4 ? ((i & 1) ? 16.f : 1.f) : VB == 2 ? (float)(1 << (2 * (i & 3))) : 1.f;
+}
+template <int VB>
+__host__ __device__ constexpr float vbias(int i) {
+  // 1024 (the exponent pattern) + vmul(i) * 2^(VB-1) (the code offset)
+  return 1024.f + vmul<VB>(i) * (float)(1 << (VB - 1));
+}
+
 template <int D, int VB, class LD>
 __device__ __forceinline__ void v_pair_words(const LD& ld, int r0, int r1, uint32_t* vw) {
   constexpr int VCH = D / 8;
@@ -265,10 +278,10 @@ __device__ __forceinline__ void v_pair_words(const LD& ld, int r0, int r1, uint3
       for (int h = 0; h < 2; ++h) {  // channels 8w+4h .. 8w+4h+3
         const uint32_t x = __byte_perm(a[w], b[w], h ? 0x7632 : 0x5410);
         const uint32_t x8 = shr8(x);
-        vw[8 * w + 4 * h + 0] = hsub2u(lop3_and_or(x, 0x000F000Fu, H_MAGIC), H_1032);
-        vw[8 * w + 4 * h + 1] = hfma2u(lop3_and_or(x, 0x00F000F0u, H_MAGIC), H_Q16, H_M72);
-        vw[8 * w + 4 * h + 2] = hsub2u(lop3_and_or(x8, 0x000F000Fu, H_MAGIC), H_1032);
-        vw[8 * w + 4 * h + 3] = hfma2u(lop3_and_or(x8, 0x00F000F0u, H_MAGIC), H_Q16, H_M72);
+        vw[8 * w + 4 * h + 0] = lop3_and_or(x, 0x000F000Fu, H_MAGIC);
+        vw[8 * w + 4 * h + 1] = lop3_and_or(x, 0x00F000F0u, H_MAGIC);
+        vw[8 * w + 4 * h + 2] = lop3_and_or(x8, 0x000F000Fu, H_MAGIC);
+        vw[8 * w + 4 * h + 3] = lop3_and_or(x8, 0x00F000F0u, H_MAGIC);
       }
     }
   } else if constexpr (VB == 2) {
@@ -278,10 +291,10 @@ __device__ __forceinline__ void v_pair_words(const LD& ld, int r0, int r1, uint3
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         const uint32_t y = q ? shr8(x) : x;
-        vw[8 * h + 4 * q + 0] = hsub2u(lop3_and_or(y, 0x00030003u, H_MAGIC), H_1026);
-        vw[8 * h + 4 * q + 1] = hfma2u(lop3_and_or(y, 0x000C000Cu, H_MAGIC), H_Q4, H_M258);
-        vw[8 * h + 4 * q + 2] = hfma2u(lop3_and_or(y, 0x00300030u, H_MAGIC), H_Q16, H_M66);
-        vw[8 * h + 4 * q + 3] = hfma2u(lop3_and_or(y, 0x00C000C0u, H_MAGIC), H_Q64, H_M18);
+        vw[8 * h + 4 * q + 0] = lop3_and_or(y, 0x00030003u, H_MAGIC);
+        vw[8 * h + 4 * q + 1] = lop3_and_or(y, 0x000C000Cu, H_MAGIC);
+        vw[8 * h + 4 * q + 2] = lop3_and_or(y, 0x00300030u, H_MAGIC);
+        vw[8 * h + 4 * q + 3] = lop3_and_or(y, 0x00C000C0u, H_MAGIC);
       }
     }
   } else if constexpr (VB == 8) {
@@ -290,7 +303,7 @@ __device__ __forceinline__ void v_pair_words(const LD& ld, int r0, int r1, uint3
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const uint32_t x = __byte_perm(a[w], b[w], k | ((4 + k) << 8));
-        vw[4 * w + k] = hsub2u(lop3_and_or(x, 0x00FF00FFu, H_MAGIC), H_1152);
+        vw[4 * w + k] = lop3_and_or(x, 0x00FF00FFu, H_MAGIC);
       }
   } else {
 #pragma unroll
@@ -302,9 +315,13 @@ __device__ __forceinline__ void v_pair_words(const LD& ld, int r0, int r1, uint3
 }
 
 // Online-softmax state of one warp (per thread: heads 2c, 2c+1 of the group).
+// o: O^T fragments (biased for quantized V); ps: running sum of the fp16 P'
+// that entered the PV products, per head (C fragment of P'^T summed over its
+// 16 rows by an MMA with an all-ones A), used to remove the V code bias.
 template <int D>
 struct Acc {
   float o[D / 16][4];
+  float ps[4];
   float m0, m1, l0, l1;
 };
 
@@ -427,6 +444,10 @@ __device__ __forceinline__ void page_pv(const VL& vl, uint32_t pb0, uint32_t pb1
 #pragma unroll
   for (int mt = 0; mt < NMT; ++mt)
     mma16816(A.o[mt], va[mt], va[NMT + mt], vb[mt], vb[NMT + mt], pb0, pb1);
+  if constexpr (VB < 16) {
+    constexpr uint32_t ONES = 0x3C003C00u;  // fp16 (1, 1)
+    mma16816(A.ps, ONES, ONES, ONES, ONES, pb0, pb1);
+  }
 }
 
 // Online-softmax update over up to two pages of the same K width at once (one
@@ -468,6 +489,9 @@ __device__ __forceinline__ void attend_pages(const KLA& kla, const VLA& vla, int
 #pragma unroll
     for (int i = 0; i < NMT; ++i) {
       A.o[i][0] *= al0; A.o[i][1] *= al1; A.o[i][2] *= al0; A.o[i][3] *= al1;
+    }
+    if constexpr (VB < 16) {
+      A.ps[0] *= al0; A.ps[1] *= al1; A.ps[2] *= al0; A.ps[3] *= al1;
     }
     A.m0 = mn0;
     A.m1 = mn1;
@@ -637,6 +661,7 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   Acc<D> A;
 #pragma unroll
   for (int i = 0; i < NMT; ++i) A.o[i][0] = A.o[i][1] = A.o[i][2] = A.o[i][3] = 0.f;
+  A.ps[0] = A.ps[1] = A.ps[2] = A.ps[3] = 0.f;
   A.m0 = A.m1 = -CUDART_INF_F;
   A.l0 = A.l1 = 0.f;
 
@@ -712,12 +737,15 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
     phases ^= 1u << si;
     return ok ? e : -1;
   };
-  auto refill = [&](int k, int si) {  // after block k's stage is consumed
-    if (ok && k + ns < nk) {
-      const int32_t e = entry(k + ns);
-      if (lane == 0) issue(k + ns, si, e);
-      issued = k + ns + 1;
-    }
+  // After blocks k (and k+1 if `two`) are consumed, lanes 0 and 1 refill their
+  // stages with blocks k+ns and k+1+ns in one pass.
+  auto refill = [&](int k, int si0, int si1, bool two) {
+    if (!ok || k + ns >= nk) return;
+    const int32_t e0 = entry(k + ns), e1 = entry(k + 1 + ns);
+    const bool second = two && k + 1 + ns < nk;
+    if (lane == 0) issue(k + ns, si0, e0);
+    if (lane == 1 && second) issue(k + 1 + ns, si1, e1);
+    issued = k + ns + (second ? 2 : 1);
   };
   for (int k = 0; k < np; k += 2) {
     if (k >= wb + 32) {  // slide the entry window; the next half was loaded 32 blocks ago
@@ -758,8 +786,7 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
         });
     }
     __syncwarp();
-    refill(k, s0);
-    if (two) refill(k + 1, s1);
+    refill(k, s0, s1, two);
     sidx = two ? ((s1 + 1 == ns) ? 0 : s1 + 1) : s1;
   }
   if (own_open && ok) {
@@ -776,6 +803,20 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
     }
   }
   __syncthreads();
+
+  // ---- remove the V code bias: o_c = (o_c - vbias(c) * sum P') / vmul(c) ------------
+  // Channel c of m-tile mt, rows g and g+8, has chunk index mt or NMT + mt, whose
+  // class (position of its code in the word) depends on mt only.
+  if constexpr (VB < 16) {
+#pragma unroll
+    for (int mt = 0; mt < NMT; ++mt) {
+      const float bias = vbias<VB>(mt), inv = 1.f / vmul<VB>(mt);
+      A.o[mt][0] = (A.o[mt][0] - bias * A.ps[0]) * inv;
+      A.o[mt][1] = (A.o[mt][1] - bias * A.ps[1]) * inv;
+      A.o[mt][2] = (A.o[mt][2] - bias * A.ps[0]) * inv;
+      A.o[mt][3] = (A.o[mt][3] - bias * A.ps[1]) * inv;
+    }
+  }
 
   // ---- merge the warps of this CTA (reusing the stage memory) ----------------------
   float* sm_acc = reinterpret_cast<float*>(smem);  // [NW][MAX_G][D]
