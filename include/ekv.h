@@ -155,7 +155,7 @@ EKV_API int ekv_decode_attn(ekv_cache* cache, int32_t layer, int32_t n_seqs, con
  * built into the library instead of the handle's scratch.  It calls no
  * allocator.
  *   - Limit: n_seqs * Hkv * splits * G * (d + 2) * 4 bytes of partials plus
- *     n_seqs * Hkv * 65 * 4 bytes of tickets (each part 256-byte aligned) must fit
+ *     n_seqs * Hkv * 17 * 4 bytes of tickets (each part 256-byte aligned) must fit
  *     in EKV_NOALLOC_SCRATCH_BYTES; larger requests return EKV_EINVAL and
  *     enqueue nothing.  splits is the split count ekv_decode_attn uses for
  *     n_seqs on this handle.

@@ -10,12 +10,13 @@
 // (Behavior-Guided KV-Cache Quantization, "Storage savings, with a
 // conditional speed trade-off").
 //
-// Work split: grid (split, kv_head, seq).  A split owns a contiguous range of
-// 16-token blocks; warp w of the CTA takes every NW-th block of it.  Each warp
-// runs its own pipeline of shared-memory stages: lane 0 issues one TMA bulk
-// copy (cp.async.bulk, completion counted on the stage's mbarrier) per page,
-// `ns` pages ahead of the page being computed, so the warp's HBM requests stay
-// in flight while it computes.  Per page the warp
+// Work split: grid (split, kv_head, seq), one CTA per SM.  A split owns a
+// contiguous range of 16-token blocks; its warps take the range's pages two at a
+// time from a counter in shared memory, so the work evens out between warps that
+// the SM's scheduler serves unequally.  Each warp runs its own pipeline of
+// shared-memory stages: one TMA bulk copy (cp.async.bulk, completion counted on
+// the stage's mbarrier) per page, `ns` pages ahead of the page being computed, so
+// the warp's HBM requests stay in flight while it computes.  Per page the warp
 //   1. unpacks K codes to exact fp16 integers in registers (PRMT/LOP3/HFMA2)
 //      and folds the per-channel K scales into Q as an fp16 hi + lo pair,
 //   2. S^T[16 tokens x 8 heads] = K . Q^T with mma.sync m16n8k16 (fp32 acc):
@@ -24,9 +25,11 @@
 //      into its probability and transposes P with movmatrix,
 //   4. O^T[d x 8] += V^T . P^T with mma.sync (channels are M, tokens K).
 // The still-open last block (raw fp16 K rows in the staging buffer) is read
-// straight from global memory.  Warps merge in shared memory; splits write
-// (max, sum, numerator) partials and the last CTA of a (sequence, KV head) —
-// found with an atomic ticket, no waiting — merges them by log-sum-exp.
+// straight from global memory, first, by one warp.  Warps merge in shared
+// memory; splits write (max, sum, numerator) partials and the last CTA of a
+// (sequence, KV head) — found with an atomic ticket, no waiting — merges them by
+// log-sum-exp.  Which warp takes which page depends on timing, so the fp32
+// summation order (not the set of terms) varies from launch to launch.
 #include <math_constants.h>
 
 #include "ekv_internal.h"
@@ -34,17 +37,19 @@
 namespace ekv {
 namespace {
 
-constexpr int NW = 4;  // warps per CTA
-constexpr int NT = NW * 32;
-constexpr int NSMAX = 8;                 // stages per warp at most
-// Resident CTAs per SM and dynamic shared memory per CTA.  Quantized V: 4 CTAs
-// (16 warps, registers capped at 128) with 54 KB each.  FP16 V pages are 3.5x
-// larger and need more registers: 3 CTAs with 72 KB each.
+constexpr int NSMAX = 8;  // stages per warp at most
+// One CTA per SM.  Its warps share the split's pages through a counter in shared
+// memory, so a warp that runs ahead takes more pages.  Stage memory: 200 KB,
+// split evenly between the warps (quantized V: 16 warps, five K4/V4 pages each,
+// registers capped at 128; FP16 V pages are 3.5x larger and need more registers:
+// 12 warps).  After the stages come the split's page-table entries.
 template <int VB>
 struct AttnCfg {
-  static constexpr int CTAS = VB == 16 ? 3 : 4;
-  static constexpr int SMEM = VB == 16 ? 72 * 1024 : 54 * 1024;
-  static constexpr int WARP_BYTES = SMEM / NW;
+  static constexpr int NW = VB == 16 ? 12 : 16;
+  static constexpr int NT = NW * 32;
+  static constexpr int STAGE_SMEM = 200 * 1024;
+  static constexpr int WARP_BYTES = (STAGE_SMEM / NW) & ~127;
+  static constexpr int SMEM = STAGE_SMEM + ATTN_BT_CAP * 4;
 };
 constexpr int WAIT_LIMIT = 1 << 22;      // bounded mbarrier polls before giving up
 
@@ -531,106 +536,157 @@ __device__ __forceinline__ void with_kbits(int kb, F&& f) {
   }
 }
 
-// Merge `count` split partials at slots pbase + first + j*stride (j < count):
-// (max, sum) pairs are staged in shared memory and turned into per-slot weights
-// 2^(m_j - M), then every thread streams its own output columns, four slots per
-// round.  With `orow` set the result is normalized and written to O as fp16;
-// otherwise the unnormalized (M, L, numerator) goes to slot `dst`.
-template <int D>
-__device__ void merge_parts(const DevState& st, size_t pbase, int first, int stride, int count,
-                            int G, uint8_t* smem, int tid, int lane, int warp, __half* orow,
-                            size_t dst) {
-  constexpr int PER = (MAX_G * D + NT - 1) / NT;   // output elements per thread
-  float* s_w = reinterpret_cast<float*>(smem);     // [count][MAX_G] weights
-  float* s_l = s_w + (size_t)count * MAX_G;        // [count][MAX_G] sums
-  float* s_ml = s_l + (size_t)count * MAX_G;       // [MAX_G][2] merged (max, sum)
-  for (int i = tid; i < count * G; i += NT) {
-    const int j = i / G, hd = i % G;
-    const size_t pid = pbase + first + (size_t)j * stride;
-    s_w[j * MAX_G + hd] = __ldcg(st.attn_ml + (pid * G + hd) * 2);
-    s_l[j * MAX_G + hd] = __ldcg(st.attn_ml + (pid * G + hd) * 2 + 1);
-  }
-  __syncthreads();
-  for (int hd = warp; hd < G; hd += NW) {
-    float M = -CUDART_INF_F;
-    for (int j = lane; j < count; j += 32) M = fmaxf(M, s_w[j * MAX_G + hd]);
+// Outputs of one (sequence, KV head) owned by each thread in the merges: thread
+// t holds the PT consecutive elements [t*PT, t*PT + PT) of the [G][D] block, all
+// of one query head (PT, a power of two, divides D).  MCH partials are loaded per
+// round, as many as fit the registers without spilling.
+template <int D, int NT>
+struct MergeShape {
+  static constexpr int RAW = (MAX_G * D + NT - 1) / NT;
+  static constexpr int PT = RAW <= 1 ? 1 : RAW <= 2 ? 2 : RAW <= 4 ? 4 : 8;
+  static constexpr int MCH = 72 / (PT + 4);
+};
+
+// PT consecutive floats from global memory (L2, not L1: written by other CTAs).
+template <int PT>
+__device__ __forceinline__ void ld_part(const float* p, float* r) {
+  if constexpr (PT == 1) {
+    r[0] = __ldcg(p);
+  } else if constexpr (PT == 2) {
+    const float2 x = __ldcg(reinterpret_cast<const float2*>(p));
+    r[0] = x.x; r[1] = x.y;
+  } else {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float L = 0.f;
-    for (int j = lane; j < count; j += 32) {
-      const float mj = s_w[j * MAX_G + hd];
-      const float f = (mj == -CUDART_INF_F) ? 0.f : exp2f(mj - M);
-      s_w[j * MAX_G + hd] = f;
-      L += f * s_l[j * MAX_G + hd];
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-    __syncwarp();
-    if (orow) {
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-      for (int j = lane; j < count; j += 32) s_w[j * MAX_G + hd] *= inv;
-    } else if (lane == 0) {
-      s_ml[2 * hd] = M;
-      s_ml[2 * hd + 1] = L;
-    }
-  }
-  __syncthreads();
-  float acc[PER];
-#pragma unroll
-  for (int r = 0; r < PER; ++r) acc[r] = 0.f;
-  const int GD = G * D;
-  const float* accp = st.attn_acc + (pbase + first) * GD;
-  const size_t step = (size_t)stride * GD;
-  int j = 0;
-  if (GD == PER * NT) {
-    for (; j + 4 <= count; j += 4) {
-#pragma unroll
-      for (int r = 0; r < PER; ++r) {
-        const int i = tid + r * NT;
-        const float* pa = accp + (size_t)j * step + i;
-        const float a0 = __ldcg(pa), a1 = __ldcg(pa + step), a2 = __ldcg(pa + 2 * step),
-                    a3 = __ldcg(pa + 3 * step);
-        const int hd = i / D;
-        float t = acc[r];
-        t = fmaf(s_w[j * MAX_G + hd], a0, t);
-        t = fmaf(s_w[(j + 1) * MAX_G + hd], a1, t);
-        t = fmaf(s_w[(j + 2) * MAX_G + hd], a2, t);
-        acc[r] = fmaf(s_w[(j + 3) * MAX_G + hd], a3, t);
-      }
-    }
-  }
-  for (; j < count; ++j) {
-#pragma unroll
-    for (int r = 0; r < PER; ++r) {
-      const int i = tid + r * NT;
-      if (i < GD) acc[r] = fmaf(s_w[j * MAX_G + i / D], __ldcg(accp + (size_t)j * step + i), acc[r]);
-    }
-  }
-#pragma unroll
-  for (int r = 0; r < PER; ++r) {
-    const int i = tid + r * NT;
-    if (i >= GD) continue;
-    if (orow) {
-      orow[i] = __float2half_rn(acc[r]);
-    } else {
-      st.attn_acc[dst * GD + i] = acc[r];
-      if (i % D == 0) {
-        st.attn_ml[(dst * G + i / D) * 2] = s_ml[2 * (i / D)];
-        st.attn_ml[(dst * G + i / D) * 2 + 1] = s_ml[2 * (i / D) + 1];
-      }
+    for (int v = 0; v < PT / 4; ++v) {
+      const float4 x = __ldcg(reinterpret_cast<const float4*>(p) + v);
+      r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
     }
   }
 }
+template <int PT>
+__device__ __forceinline__ void st_part(float* p, const float* r) {
+  if constexpr (PT == 1) {
+    p[0] = r[0];
+  } else if constexpr (PT == 2) {
+    *reinterpret_cast<float2*>(p) = make_float2(r[0], r[1]);
+  } else {
+#pragma unroll
+    for (int v = 0; v < PT / 4; ++v)
+      reinterpret_cast<float4*>(p)[v] = make_float4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+  }
+}
+// PT floats (already divided by the softmax sum) to O as fp16.
+template <int PT>
+__device__ __forceinline__ void store_o(__half* dst, const float* r) {
+  if constexpr (PT == 1) {
+    dst[0] = __float2half_rn(r[0]);
+  } else {
+    uint32_t w[PT / 2];
+#pragma unroll
+    for (int i = 0; i < PT / 2; ++i) w[i] = h2u(__floats2half2_rn(r[2 * i], r[2 * i + 1]));
+    if constexpr (PT == 2) *reinterpret_cast<uint32_t*>(dst) = w[0];
+    else if constexpr (PT == 4) *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+    else *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// Merge `count` split partials at slots pbase + first + j*stride (j < count) by
+// log-sum-exp.  Every thread merges its own PT outputs straight from global
+// memory: the (max, sum) pair of its head and its numerator words of up to MCH
+// partials are loaded in one round, then folded into a running (M, L, acc).
+// With `orow` set the result is normalized and written to O as fp16; otherwise
+// the unnormalized (M, L, numerator) goes to slot `dst`, which may be one of the
+// slots read (a barrier separates the reads from the writes).  Called by every
+// thread of the CTA.
+template <int D, int NT>
+__device__ void merge_parts(const DevState& st, size_t pbase, int first, int stride, int count,
+                            int G, int tid, __half* orow, size_t dst) {
+  constexpr int PT = MergeShape<D, NT>::PT, MCH = MergeShape<D, NT>::MCH;
+  const int GD = G * D;
+  const int i0 = tid * PT;
+  const bool active = i0 < GD;
+  const int hd = i0 / D;
+  float M = -CUDART_INF_F, L = 0.f;
+  float acc[PT];
+#pragma unroll
+  for (int r = 0; r < PT; ++r) acc[r] = 0.f;
+  if (active) {
+    for (int j0 = 0; j0 < count; j0 += MCH) {
+      float2 ml[MCH];
+      float a[MCH][PT];
+#pragma unroll
+      for (int u = 0; u < MCH; ++u) {
+        ml[u] = make_float2(-CUDART_INF_F, 0.f);
+#pragma unroll
+        for (int r = 0; r < PT; ++r) a[u][r] = 0.f;
+        if (j0 + u < count) {
+          const size_t pid = pbase + first + (size_t)(j0 + u) * stride;
+          ml[u] = __ldcg(reinterpret_cast<const float2*>(st.attn_ml + (pid * G + hd) * 2));
+          ld_part<PT>(st.attn_acc + pid * GD + i0, a[u]);
+        }
+      }
+      float Mn = M;
+#pragma unroll
+      for (int u = 0; u < MCH; ++u) Mn = fmaxf(Mn, ml[u].x);
+      if (Mn == -CUDART_INF_F) continue;  // nothing attended so far
+      const float al = M == -CUDART_INF_F ? 0.f : exp2f(M - Mn);
+      L *= al;
+#pragma unroll
+      for (int r = 0; r < PT; ++r) acc[r] *= al;
+#pragma unroll
+      for (int u = 0; u < MCH; ++u) {
+        const float f = ml[u].x == -CUDART_INF_F ? 0.f : exp2f(ml[u].x - Mn);
+        L = fmaf(f, ml[u].y, L);
+#pragma unroll
+        for (int r = 0; r < PT; ++r) acc[r] = fmaf(f, a[u][r], acc[r]);
+      }
+      M = Mn;
+    }
+  }
+  if (orow) {
+    if (active) {
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+      for (int r = 0; r < PT; ++r) acc[r] *= inv;
+      store_o<PT>(orow + i0, acc);
+    }
+    return;
+  }
+  __syncthreads();  // every read of the slots is done before `dst` is overwritten
+  if (active) {
+    st_part<PT>(st.attn_acc + dst * GD + i0, acc);
+    if (i0 % D == 0)
+      *reinterpret_cast<float2*>(st.attn_ml + (dst * G + hd) * 2) = make_float2(M, L);
+  }
+}
+
+// Arrive on a merge ticket that `expected` CTAs share: publish this CTA's
+// writes, count it in, and return (to every thread) whether it came last.  The
+// last one resets the ticket for the next launch and sees all the others' writes.
+__device__ __forceinline__ bool last_arrival(int* ticket, int expected, int tid, int* s_flag) {
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const int t = atomicAdd(ticket, 1);
+    *s_flag = (t == expected - 1);
+    if (*s_flag) *ticket = 0;
+    __threadfence();
+  }
+  __syncthreads();
+  return *s_flag != 0;
+}
 
 template <int D, int VB>
-__global__ void __launch_bounds__(NT, AttnCfg<VB>::CTAS)
+__global__ void __launch_bounds__(AttnCfg<VB>::NT, 1)
 decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
                    const __half* __restrict__ q, __half* __restrict__ o, int splits) {
+  constexpr int NW = AttnCfg<VB>::NW, NT = AttnCfg<VB>::NT;
   constexpr int KCH = D / 4, KW = KCH / 2, VCH = D / 8, NMT = D / 16;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[NW][NSMAX];
-  __shared__ float sm_m[NW][MAX_G], sm_l[NW][MAX_G];
-  __shared__ int s_last;
+  __shared__ float sm_m[NW][MAX_G], sm_l[NW][MAX_G], sm_f[NW][MAX_G], sm_ml[MAX_G][2];
+  __shared__ int s_next, s_last;
+  int32_t* s_bt = reinterpret_cast<int32_t*>(smem + AttnCfg<VB>::STAGE_SMEM);
 
   const int split = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -642,7 +698,20 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   const int nb = (T + BLOCK - 1) / BLOCK;
   const int cb = (nb + splits - 1) / splits;
   const int b0 = min(nb, split * cb), b1 = min(nb, b0 + cb);
-  const bool has_open = (T % BLOCK) != 0;
+  // Sealed blocks of this split go through the pipelines; the open block (the
+  // sequence's last, raw K rows in the staging buffer) is attended from global
+  // memory by the split that holds it.
+  const bool open_here = (T % BLOCK) != 0 && b1 == nb && b1 > b0;
+  int np = b1 - b0 - (open_here ? 1 : 0);  // pipelined pages of this split
+  if (np > ATTN_BT_CAP) {  // the host sizes splits so that this never happens
+    if (tid == 0) set_error(st, EKV_ESTATE);
+    np = 0;
+  }
+
+  const int32_t* bt = st.bt + lsh_index(st, layer, slot_ok ? slot : 0, h) * st.maxblk;
+  const __half* stg = st.staging + lsh_index(st, layer, slot_ok ? slot : 0, h) * (BLOCK * D);
+  for (int i = tid; i < np; i += NT) s_bt[i] = bt[b0 + i];
+  if (tid == 0) s_next = 0;
 
   // Q fragment words for head g of the group, paired like the K codes of the
   // page format in use (re-paired when a page of another pairing class comes).
@@ -664,12 +733,10 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   A.ps[0] = A.ps[1] = A.ps[2] = A.ps[3] = 0.f;
   A.m0 = A.m1 = -CUDART_INF_F;
   A.l0 = A.l1 = 0.f;
-
-  const int32_t* bt = st.bt + lsh_index(st, layer, slot_ok ? slot : 0, h) * st.maxblk;
-  const __half* stg = st.staging + lsh_index(st, layer, slot_ok ? slot : 0, h) * (BLOCK * D);
   const float sl = st.scale_log2;
 
-  // Stage geometry: sized for the widest page this layer has admitted so far.
+  // Stage geometry: sized for the widest page this layer has admitted so far
+  // (at least two stages for every format).
   const int kmax = max(2, st.kmax[layer]);
   const int stage_bytes = (page_bytes(kmax, VB, D) + 127) & ~127;
   constexpr int WARP_BYTES = AttnCfg<VB>::WARP_BYTES;
@@ -681,82 +748,76 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
     for (int i = 0; i < ns; ++i) mbar_init(bar0 + 8 * i, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  __syncwarp();
+  __syncthreads();  // page-table copy, counter and barriers ready
 
-  // This warp's blocks: b0 + warp + k*NW for k < nk.  Pages of sealed blocks go
-  // through the pipeline; the open block (always the sequence's last) does not.
-  const int nk = (b1 - b0 > warp) ? (b1 - b0 - warp + NW - 1) / NW : 0;
-  // Page-table entries of this warp's blocks, a window of 64 ahead in two lane
-  // registers (lane j: blocks wb + j and wb + 32 + j), read with one shuffle.
-  auto bt_at = [&](int k) -> int32_t { return k < nk ? bt[b0 + warp + k * NW] : -1; };
-  int wb = 0;
-  int32_t ecur = bt_at(lane), enext = bt_at(32 + lane);
-  auto entry = [&](int k) -> int32_t {  // warp-uniform k in [wb, wb + 64)
-    const int j = k - wb;
-    return __shfl_sync(0xffffffffu, j < 32 ? ecur : enext, j & 31);
-  };
-  auto issue = [&](int k, int sidx, int32_t e) {  // lane 0 only; block k -> stage sidx
-    const int blk = b0 + warp + k * NW;
-    if ((has_open && blk == nb - 1) || e == -1) return;
+  // Lane i < ns holds `pg`, the split page index in stage i (-1: none).  Stages
+  // are filled in the order the counter hands pages out and consumed in the same
+  // ring order, so the pages still to come are a prefix of the ring.  A page
+  // whose table entry is missing (-1) is flagged and neither copied nor read.
+  auto issue = [&](int si, int k) {  // one lane: page k -> stage si
+    const int32_t e = s_bt[k];
+    if (e == -1) {
+      set_error(st, EKV_ESTATE);
+      return;
+    }
     const int fmt = entry_fmt(e);
     const uint32_t bytes = (uint32_t)st.pool_page_bytes[fmt];
     const uint8_t* src = st.pool_base[fmt] + (size_t)entry_idx(e) * bytes;
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    mbar_expect_tx(bar0 + 8 * sidx, bytes);
-    bulk_g2s(wbase + sidx * stage_bytes, src, bytes, bar0 + 8 * sidx);
+    mbar_expect_tx(bar0 + 8 * si, bytes);
+    bulk_g2s(wbase + si * stage_bytes, src, bytes, bar0 + 8 * si);
   };
-  for (int k = 0; k < min(ns, nk); ++k) {
-    const int32_t e = entry(k);
-    if (lane == 0) issue(k, k, e);
+  int pg = -1;
+  {
+    int k0 = 0;
+    if (lane == 0) k0 = atomicAdd(&s_next, ns);
+    k0 = __shfl_sync(0xffffffffu, k0, 0);
+    if (lane < ns && k0 + lane < np) {
+      pg = k0 + lane;
+      issue(lane, pg);
+    }
   }
 
-  // `issued`: blocks k < issued had issue() called (warp-uniform).  After a wait
-  // times out the warp stops issuing and computing but still waits, each wait
-  // bounded, for the copies already in flight, so none lands after it exits.
-  // Pipelined pages are consumed two at a time; the open block, always the
-  // sequence's last and so this warp's last, is attended alone from global memory.
-  const bool own_open = has_open && nk > 0 && (b0 + warp + (nk - 1) * NW) == nb - 1;
-  const int np = nk - (own_open ? 1 : 0);  // pipelined blocks of this warp
-  uint32_t phases = 0;
-  bool ok = true;
-  int issued = min(ns, nk);
-  int sidx = 0;  // stage of block k (= k mod ns)
-  // Wait for block k's page; returns its entry, or -1 when it has no page or the
-  // wait failed (then nothing is computed for it).
-  auto acquire = [&](int k, int si) -> int32_t {
-    const int32_t e = entry(k);
+  // The open block first, while this warp's copies are in flight.
+  if (open_here && warp == NW - 1) {
+    const int32_t e = bt[nb - 1];
     if (e == -1) {
       if (lane == 0) set_error(st, EKV_ESTATE);
-      return -1;
+    } else {
+      const int fmt = entry_fmt(e);
+      const uint8_t* page = st.pool_base[fmt] + (size_t)entry_idx(e) * st.pool_page_bytes[fmt];
+      const GLd kl{reinterpret_cast<const uint8_t*>(stg)};
+      const GLd vl{page + k_part_bytes(bits_of_code(fmt >> 2), D)};
+      pair_q(KBits<16>{});
+      attend_pages<D, VB, false, 16>(kl, vl, T % BLOCK, kl, vl, 0, qw, A, sl, g, c);
     }
-    if (k >= issued) return -1;
-    if (!mbar_wait(bar0 + 8 * si, (phases >> si) & 1) && ok) {
+  }
+
+  // Two stages per iteration.  After a wait times out the warp computes and
+  // takes nothing more but still waits, each wait bounded, for the copies
+  // already in flight, so none lands after it exits.
+  uint32_t phases = 0;
+  bool ok = true;
+  auto ready = [&](int k, int si) -> int32_t {  // entry of page k once its stage landed
+    if (k < 0) return -1;
+    const int32_t e = s_bt[k];
+    if (e == -1) return -1;
+    // warp-uniform outcome: the MMAs that follow need every lane
+    if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * si, (phases >> si) & 1)) && ok) {
       ok = false;
       if (lane == 0) set_error(st, EKV_ETIMEOUT);
     }
     phases ^= 1u << si;
     return ok ? e : -1;
   };
-  // After blocks k (and k+1 if `two`) are consumed, lanes 0 and 1 refill their
-  // stages with blocks k+ns and k+1+ns in one pass.
-  auto refill = [&](int k, int si0, int si1, bool two) {
-    if (!ok || k + ns >= nk) return;
-    const int32_t e0 = entry(k + ns), e1 = entry(k + 1 + ns);
-    const bool second = two && k + 1 + ns < nk;
-    if (lane == 0) issue(k + ns, si0, e0);
-    if (lane == 1 && second) issue(k + 1 + ns, si1, e1);
-    issued = k + ns + (second ? 2 : 1);
-  };
-  for (int k = 0; k < np; k += 2) {
-    if (k >= wb + 32) {  // slide the entry window; the next half was loaded 32 blocks ago
-      wb += 32;
-      ecur = enext;
-      enext = bt_at(wb + 32 + lane);
-    }
+  int sidx = 0;
+  while (true) {
     const int s0 = sidx, s1 = (sidx + 1 == ns) ? 0 : sidx + 1;
-    const bool two = k + 1 < np;
-    const int32_t ea = acquire(k, s0);
-    const int32_t eb = two ? acquire(k + 1, s1) : -1;
+    const int ka = __shfl_sync(0xffffffffu, pg, s0);
+    if (ka < 0) break;
+    const int kb = __shfl_sync(0xffffffffu, pg, s1);
+    const int32_t ea = ready(ka, s0);
+    const int32_t eb = ready(kb, s1);
     const uint8_t* sa = wptr + s0 * stage_bytes;
     const uint8_t* sb = wptr + s1 * stage_bytes;
     const int kba = ea != -1 ? bits_of_code(entry_fmt(ea) >> 2) : 0;
@@ -786,23 +847,18 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
         });
     }
     __syncwarp();
-    refill(k, s0, s1, two);
-    sidx = two ? ((s1 + 1 == ns) ? 0 : s1 + 1) : s1;
+    // Refill both stages with the split's next two pages (none once the pages
+    // ran out or a wait failed); lanes 0 and 1 issue the two copies.
+    int kn = np;
+    if (lane == 0 && ok && kb >= 0) kn = atomicAdd(&s_next, 2);
+    kn = __shfl_sync(0xffffffffu, kn, 0);
+    if (lane == s0) pg = kn < np ? kn : -1;
+    if (lane == s1) pg = kn + 1 < np ? kn + 1 : -1;
+    if (lane == 0 && kn < np) issue(s0, kn);
+    if (lane == 1 && kn + 1 < np) issue(s1, kn + 1);
+    sidx = (s1 + 1 == ns) ? 0 : s1 + 1;
   }
-  if (own_open && ok) {
-    const int32_t e = bt[nb - 1];
-    if (e == -1) {
-      if (lane == 0) set_error(st, EKV_ESTATE);
-    } else {
-      const int fmt = entry_fmt(e);
-      const uint8_t* page = st.pool_base[fmt] + (size_t)entry_idx(e) * st.pool_page_bytes[fmt];
-      const GLd kl{reinterpret_cast<const uint8_t*>(stg)};
-      const GLd vl{page + k_part_bytes(bits_of_code(fmt >> 2), D)};
-      pair_q(KBits<16>{});
-      attend_pages<D, VB, false, 16>(kl, vl, T % BLOCK, kl, vl, 0, qw, A, sl, g, c);
-    }
-  }
-  __syncthreads();
+  __syncthreads();  // every stage drained before the stage memory is reused
 
   // ---- remove the V code bias: o_c = (o_c - vbias(c) * sum P') / vmul(c) ------------
   // Channel c of m-tile mt, rows g and g+8, has chunk index mt or NMT + mt, whose
@@ -838,76 +894,80 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
     wacc[(2 * c + 1) * D + g * VCH + NMT + mt] = A.o[mt][3];
   }
   __syncthreads();
-
-  const size_t pbase = ((size_t)z * st.Hkv + h) * splits;
-  const size_t pid = pbase + split;
-  for (int i = tid; i < G * D; i += NT) {
-    const int hd = i / D, ch = i % D;
+  // Per head: the CTA's max, each warp's weight 2^(m_w - M) and the weighted sum.
+  if (tid < G) {
     float M = -CUDART_INF_F;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, sm_m[w][hd]);
-    float L = 0.f, Ao = 0.f;
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, sm_m[w][tid]);
+    float L = 0.f;
 #pragma unroll
     for (int w = 0; w < NW; ++w) {
-      const float f = sm_m[w][hd] == -CUDART_INF_F ? 0.f : exp2f(sm_m[w][hd] - M);
-      L += f * sm_l[w][hd];
-      Ao += f * sm_acc[((size_t)w * MAX_G + hd) * D + ch];
+      const float f = sm_m[w][tid] == -CUDART_INF_F ? 0.f : exp2f(sm_m[w][tid] - M);
+      sm_f[w][tid] = f;
+      L = fmaf(f, sm_l[w][tid], L);
     }
-    if (splits == 1) {
-      o[((size_t)z * st.Hq + h * G + hd) * D + ch] = __float2half_rn(L > 0.f ? Ao / L : 0.f);
-    } else {
-      st.attn_acc[(pid * G + hd) * D + ch] = Ao;
-      if (ch == 0) {
-        st.attn_ml[(pid * G + hd) * 2] = M;
-        st.attn_ml[(pid * G + hd) * 2 + 1] = L;
+    sm_ml[tid][0] = M;
+    sm_ml[tid][1] = L;
+  }
+  __syncthreads();
+
+  constexpr int PT = MergeShape<D, NT>::PT;
+  const size_t pbase = ((size_t)z * st.Hkv + h) * splits;
+  const size_t pid = pbase + split;
+  __half* orow = o + ((size_t)z * st.Hq + h * G) * D;
+  {
+    const int i0 = tid * PT, hd = i0 / D;
+    if (i0 < G * D) {
+      float r[PT];
+#pragma unroll
+      for (int x = 0; x < PT; ++x) r[x] = 0.f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float f = sm_f[w][hd];
+        const float* src = sm_acc + (size_t)w * MAX_G * D + i0;
+#pragma unroll
+        for (int x = 0; x < PT; ++x) r[x] = fmaf(f, src[x], r[x]);
+      }
+      if (splits == 1) {
+        const float L = sm_ml[hd][1], inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+        for (int x = 0; x < PT; ++x) r[x] *= inv;
+        store_o<PT>(orow + i0, r);
+      } else {
+        st_part<PT>(st.attn_acc + pid * G * D + i0, r);
+        if (i0 % D == 0)
+          *reinterpret_cast<float2*>(st.attn_ml + (pid * G + hd) * 2) =
+              make_float2(sm_ml[hd][0], sm_ml[hd][1]);
       }
     }
   }
   if (splits == 1) return;
 
-  // ---- two-level merge of the splits --------------------------------------------------
-  // Splits form groups of ATTN_GROUP; the last CTA of a group to finish merges the
-  // group into the slot of its first split, and the last group merger merges the
-  // group results into O.  Each merge reads at most ATTN_GROUP or ATTN_MAXGRP
-  // partials, so no single CTA streams all of them.  Tickets never wait.
+  // ---- merge of the splits ------------------------------------------------------------
+  // Up to ATTN_GROUP splits: the last CTA to finish merges them all into O.  More:
+  // splits form groups of ATTN_GROUP, the last CTA of each group merges the group
+  // into the slot of its first split, and the last group merger merges the groups
+  // into O.  Tickets never wait.
   const int grp = split / ATTN_GROUP, ngrp = (splits + ATTN_GROUP - 1) / ATTN_GROUP;
   const int gsize = min(ATTN_GROUP, splits - grp * ATTN_GROUP);
   int* tk = st.attn_ticket + ((size_t)z * st.Hkv + h) * ATTN_TICKETS;
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const int t = atomicAdd(tk + 1 + grp, 1);
-    s_last = (t == gsize - 1);
-    if (s_last) tk[1 + grp] = 0;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  __half* orow = o + ((size_t)z * st.Hq + h * G) * D;
+  if (!last_arrival(tk + 1 + grp, gsize, tid, &s_last)) return;
   if (ngrp == 1) {
-    merge_parts<D>(st, pbase, 0, 1, splits, G, smem, tid, lane, warp, orow, 0);
+    merge_parts<D, NT>(st, pbase, 0, 1, splits, G, tid, orow, 0);
     return;
   }
-  merge_parts<D>(st, pbase, grp * ATTN_GROUP, 1, gsize, G, smem, tid, lane, warp, nullptr,
-                 pbase + grp * ATTN_GROUP);
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const int t = atomicAdd(tk, 1);
-    s_last = (t == ngrp - 1);
-    if (s_last) tk[0] = 0;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  merge_parts<D>(st, pbase, 0, ATTN_GROUP, ngrp, G, smem, tid, lane, warp, orow, 0);
+  merge_parts<D, NT>(st, pbase, grp * ATTN_GROUP, 1, gsize, G, tid, nullptr,
+                     pbase + grp * ATTN_GROUP);
+  if (!last_arrival(tk, ngrp, tid, &s_last)) return;
+  merge_parts<D, NT>(st, pbase, 0, ATTN_GROUP, ngrp, G, tid, orow, 0);
 }
 
 template <int D, int VB>
 cudaError_t launch_t(const DevState& st, int layer, int n_seqs, const int32_t* slots,
                      const __half* q, __half* o, int splits, cudaStream_t s) {
   dim3 grid(splits, st.Hkv, n_seqs);
-  decode_attn_kernel<D, VB><<<grid, NT, AttnCfg<VB>::SMEM, s>>>(st, layer, slots, q, o, splits);
+  decode_attn_kernel<D, VB><<<grid, AttnCfg<VB>::NT, AttnCfg<VB>::SMEM, s>>>(st, layer, slots, q, o,
+                                                                           splits);
   return cudaGetLastError();
 }
 
@@ -925,7 +985,7 @@ cudaError_t init_t() {
 
 }  // namespace
 
-int attn_ctas_per_sm(int vb) { return vb == 16 ? AttnCfg<16>::CTAS : AttnCfg<4>::CTAS; }
+int attn_ctas_per_sm(int) { return 1; }
 
 cudaError_t attn_init() {
   cudaError_t e = cudaSuccess;

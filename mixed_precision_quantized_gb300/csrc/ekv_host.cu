@@ -46,6 +46,9 @@ int attn_splits(const ekv_cache* c, int n_seqs, int vb) {
   const int target = attn_ctas_per_sm(vb) * c->num_sm;
   int s = (target + units - 1) / units;
   if (s < 1) s = 1;
+  // A split's page-table entries must fit the kernel's shared-memory copy.
+  const int need = (c->st.maxblk + ATTN_BT_CAP - 1) / ATTN_BT_CAP;
+  if (s < need) s = need;
   if (s > ATTN_MAX_SPLITS) s = ATTN_MAX_SPLITS;
   return s;
 }

@@ -14,7 +14,8 @@ constexpr int RING = EKV_RING_LEN;       // K vectors per ring
 constexpr int NFMT = EKV_NUM_FORMATS;
 constexpr int MAX_G = 8;                  // query heads per KV head handled by one CTA
 constexpr int ATTN_MAX_SPLITS = 512;      // decode-attention splits per (sequence, KV head)
-constexpr int ATTN_GROUP = 8;             // splits merged together at the first level
+constexpr int ATTN_GROUP = 32;            // splits merged together at the first level
+constexpr int ATTN_BT_CAP = 4096;         // page-table entries of one split (staged in shared memory)
 constexpr int ATTN_MAXGRP = ATTN_MAX_SPLITS / ATTN_GROUP;
 constexpr int ATTN_TICKETS = 1 + ATTN_MAXGRP;  // merge tickets per (sequence, KV head)
 
