@@ -154,7 +154,7 @@ EKV_API int ekv_decode_attn(ekv_cache* cache, int32_t layer, int32_t n_seqs, con
  * tickets) comes from one static device array of EKV_NOALLOC_SCRATCH_BYTES
  * built into the library instead of the handle's scratch.  It calls no
  * allocator.
- *   - Limit: n_seqs * Hkv * splits * G * (d + 2) * 4 bytes of partials plus
+ *   - Limit: n_seqs * Hkv * splits * 8 * (d + 2) * 4 bytes of partials plus
  *     n_seqs * Hkv * 17 * 4 bytes of tickets (each part 256-byte aligned) must fit
  *     in EKV_NOALLOC_SCRATCH_BYTES; larger requests return EKV_EINVAL and
  *     enqueue nothing.  splits is the split count ekv_decode_attn uses for

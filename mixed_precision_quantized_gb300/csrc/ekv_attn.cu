@@ -253,8 +253,11 @@ __host__ __device__ constexpr float vbias(int i) {
   return 1024.f + vmul<VB>(i) * (float)(1 << (VB - 1));
 }
 
+// `flip` (0 or 0x4444) marks lanes that loaded the pair's rows in swapped order
+// (row t+1 from offset r0): it swaps the two sources of every byte permute.
 template <int D, int VB, class LD>
-__device__ __forceinline__ void v_pair_words(const LD& ld, int r0, int r1, uint32_t* vw) {
+__device__ __forceinline__ void v_pair_words(const LD& ld, int r0, int r1, uint32_t flip,
+                                             uint32_t* vw) {
   constexpr int VCH = D / 8;
   constexpr int NB = VCH * VB / 8;  // bytes per row chunk
   constexpr int NWD = NB >= 4 ? NB / 4 : 1;
@@ -281,7 +284,7 @@ __device__ __forceinline__ void v_pair_words(const LD& ld, int r0, int r1, uint3
     for (int w = 0; w < NWD; ++w) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {  // channels 8w+4h .. 8w+4h+3
-        const uint32_t x = __byte_perm(a[w], b[w], h ? 0x7632 : 0x5410);
+        const uint32_t x = __byte_perm(a[w], b[w], (h ? 0x7632u : 0x5410u) ^ flip);
         const uint32_t x8 = shr8(x);
         vw[8 * w + 4 * h + 0] = lop3_and_or(x, 0x000F000Fu, H_MAGIC);
         vw[8 * w + 4 * h + 1] = lop3_and_or(x, 0x00F000F0u, H_MAGIC);
@@ -292,7 +295,7 @@ __device__ __forceinline__ void v_pair_words(const LD& ld, int r0, int r1, uint3
   } else if constexpr (VB == 2) {
 #pragma unroll
     for (int h = 0; h < VCH / 8; ++h) {  // channels 8h .. 8h+7
-      const uint32_t x = __byte_perm(a[0], b[0], h ? 0x7632 : 0x5410);
+      const uint32_t x = __byte_perm(a[0], b[0], (h ? 0x7632u : 0x5410u) ^ flip);
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         const uint32_t y = q ? shr8(x) : x;
@@ -307,14 +310,14 @@ __device__ __forceinline__ void v_pair_words(const LD& ld, int r0, int r1, uint3
     for (int w = 0; w < NWD; ++w)
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const uint32_t x = __byte_perm(a[w], b[w], k | ((4 + k) << 8));
+        const uint32_t x = __byte_perm(a[w], b[w], (k | ((4 + k) << 8)) ^ flip);
         vw[4 * w + k] = lop3_and_or(x, 0x00FF00FFu, H_MAGIC);
       }
   } else {
 #pragma unroll
     for (int w = 0; w < NWD; ++w) {
-      vw[2 * w] = __byte_perm(a[w], b[w], 0x5410);
-      vw[2 * w + 1] = __byte_perm(a[w], b[w], 0x7632);
+      vw[2 * w] = __byte_perm(a[w], b[w], 0x5410u ^ flip);
+      vw[2 * w + 1] = __byte_perm(a[w], b[w], 0x7632u ^ flip);
     }
   }
 }
@@ -383,7 +386,7 @@ __device__ __forceinline__ void page_scores(const KL& kl, const uint32_t* qw, fl
   k_row_words<D, KB>(kl, (g + 8) * krow, c, kwb);
   float s1[4] = {0.f, 0.f, 0.f, 0.f};
   s[0] = s[1] = s[2] = s[3] = 0.f;
-  if constexpr (KB < 16) {
+  if constexpr (KB == 8) {
     // Fold the per-channel K scale into Q: q*s = hi + lo with hi = fp16(q*s) and
     // lo = fp16(q*s - hi) from one fused multiply-add (the residual of a rounded
     // fp16 product is itself an fp16 value).  Two MMA chains against the exact
@@ -409,6 +412,22 @@ __device__ __forceinline__ void page_scores(const KL& kl, const uint32_t* qw, fl
                ql[2 * kk + 1]);
     }
   } else {
+    if constexpr (KB < 16) {
+      // 2- and 4-bit codes times their (pair-ordered) channel scales are exact in
+      // fp16: 2-bit codes are 0 or +-1, +-2, and 4-bit pages store scales with 8
+      // significant bits against codes of at most 3.  One MMA chain with plain Q.
+      const int so = BLOCK * D * KB / 8 + c * KCH * 2;
+#pragma unroll
+      for (int i = 0; i < KW / 4; ++i) {
+        const uint4 u = kl.v4(so + 16 * i);
+        const uint32_t sv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          kwa[4 * i + x] = h2u(__hmul2(u2h(kwa[4 * i + x]), u2h(sv[x])));
+          kwb[4 * i + x] = h2u(__hmul2(u2h(kwb[4 * i + x]), u2h(sv[x])));
+        }
+      }
+    }
 #pragma unroll
     for (int kk = 0; kk < NKS; kk += 2) {
       mma16816(s, kwa[2 * kk], kwb[2 * kk], kwa[2 * kk + 1], kwb[2 * kk + 1], qw[2 * kk],
@@ -443,9 +462,13 @@ __device__ __forceinline__ void page_pv(const VL& vl, uint32_t pb0, uint32_t pb1
   constexpr int VROW = VB == 16 ? 2 * D : D * VB / 8;
   constexpr int VOFF = VCH * VB / 8;
   uint32_t va[VCH], vb[VCH];
+  // Lanes with odd c read row 2c+1 first: rows 2c of the four c fall on the same
+  // banks, so alternating the order halves the bank conflicts of each load.
+  const int odd = c & 1;
+  const uint32_t flip = odd ? 0x4444u : 0u;
   const int vr = g * VOFF;
-  v_pair_words<D, VB>(vl, vr + (2 * c) * VROW, vr + (2 * c + 1) * VROW, va);
-  v_pair_words<D, VB>(vl, vr + (2 * c + 8) * VROW, vr + (2 * c + 9) * VROW, vb);
+  v_pair_words<D, VB>(vl, vr + (2 * c + odd) * VROW, vr + (2 * c + 1 - odd) * VROW, flip, va);
+  v_pair_words<D, VB>(vl, vr + (2 * c + 8 + odd) * VROW, vr + (2 * c + 9 - odd) * VROW, flip, vb);
 #pragma unroll
   for (int mt = 0; mt < NMT; ++mt)
     mma16816(A.o[mt], va[mt], va[NMT + mt], vb[mt], vb[NMT + mt], pb0, pb1);
@@ -479,28 +502,36 @@ __device__ __forceinline__ void attend_pages(const KLA& kla, const VLA& vla, int
       if (g + 8 >= nvb) xb2 = xb3 = -CUDART_INF_F;
     }
   }
+  // Lazy max: the reference A.m moves only when a score passes it by more than
+  // SLACK (log2 units), so most pages skip the cross-lane reduction.  Then
+  // p = 2^(x - m) <= 2^SLACK, and P' = p * s_v stays below the fp16 maximum for
+  // any stored V scale (s_v <= 65504 / qmax).
+  constexpr float SLACK = VB == 2 ? 0.f : VB == 4 ? 2.f : VB == 8 ? 6.f : 8.f;
   float bm0 = fmaxf(fmaxf(xa0, xa2), fmaxf(xb0, xb2));
   float bm1 = fmaxf(fmaxf(xa1, xa3), fmaxf(xb1, xb3));
+  if (__any_sync(0xffffffffu, bm0 > A.m0 + SLACK || bm1 > A.m1 + SLACK)) {
 #pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
-    bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
-  }
-  const float mn0 = fmaxf(A.m0, bm0), mn1 = fmaxf(A.m1, bm1);
-  if (mn0 != A.m0 || mn1 != A.m1) {  // rescale only when a running max moved
-    const float al0 = fexp2(A.m0 - mn0), al1 = fexp2(A.m1 - mn1);
-    A.l0 *= al0;
-    A.l1 *= al1;
+    for (int off = 4; off < 32; off <<= 1) {
+      bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+      bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+    }
+    const float mn0 = fmaxf(A.m0, bm0), mn1 = fmaxf(A.m1, bm1);
+    if (mn0 != A.m0 || mn1 != A.m1) {  // rescale only when a reference moved
+      const float al0 = fexp2(A.m0 - mn0), al1 = fexp2(A.m1 - mn1);
+      A.l0 *= al0;
+      A.l1 *= al1;
 #pragma unroll
-    for (int i = 0; i < NMT; ++i) {
-      A.o[i][0] *= al0; A.o[i][1] *= al1; A.o[i][2] *= al0; A.o[i][3] *= al1;
+      for (int i = 0; i < NMT; ++i) {
+        A.o[i][0] *= al0; A.o[i][1] *= al1; A.o[i][2] *= al0; A.o[i][3] *= al1;
+      }
+      if constexpr (VB < 16) {
+        A.ps[0] *= al0; A.ps[1] *= al1; A.ps[2] *= al0; A.ps[3] *= al1;
+      }
+      A.m0 = mn0;
+      A.m1 = mn1;
     }
-    if constexpr (VB < 16) {
-      A.ps[0] *= al0; A.ps[1] *= al1; A.ps[2] *= al0; A.ps[3] *= al1;
-    }
-    A.m0 = mn0;
-    A.m1 = mn1;
   }
+  const float mn0 = A.m0, mn1 = A.m1;
   const float pa0 = fexp2(xa0 - mn0), pa1 = fexp2(xa1 - mn1);
   const float pa2 = fexp2(xa2 - mn0), pa3 = fexp2(xa3 - mn1);
   A.l0 += pa0 + pa2;
@@ -536,93 +567,64 @@ __device__ __forceinline__ void with_kbits(int kb, F&& f) {
   }
 }
 
-// Outputs of one (sequence, KV head) owned by each thread in the merges: thread
-// t holds the PT consecutive elements [t*PT, t*PT + PT) of the [G][D] block, all
-// of one query head (PT, a power of two, divides D).  MCH partials are loaded per
-// round, as many as fit the registers without spilling.
+// A split partial holds the CTA's O^T fragments in "slot" order: element j of
+// m-tile mt of lane's fragment goes to slot (mt*4 + j)*32 + lane, so a warp
+// stores and loads whole 128-byte rows.  Slot -> (query head of the group, channel):
+template <int D>
+__device__ __forceinline__ int slot_head(int s) { return 2 * (s & 3) + ((s >> 5) & 1); }
+template <int D>
+__device__ __forceinline__ int slot_ch(int s) {
+  constexpr int VCH = D / 8, NMT = D / 16;
+  return ((s & 31) >> 2) * VCH + ((s >> 6) & 1) * NMT + (s >> 7);
+}
+// Thread t of a CTA of NT threads owns slots t + k*NT (k < PTS); NT is a multiple
+// of 64, so they share the slot bits that pick the head: all of head slot_head(t).  MCH partials are loaded per
+// merge round, as many as fit the registers without spilling.
 template <int D, int NT>
 struct MergeShape {
-  static constexpr int RAW = (MAX_G * D + NT - 1) / NT;
-  static constexpr int PT = RAW <= 1 ? 1 : RAW <= 2 ? 2 : RAW <= 4 ? 4 : 8;
-  static constexpr int MCH = 72 / (PT + 4);
+  static_assert(NT % 64 == 0, "slots of a thread must share a head");
+  static constexpr int SLOTS = MAX_G * D;
+  static constexpr int PTS = (SLOTS + NT - 1) / NT;
+  static constexpr int MCH = 80 / (PTS + 2) < 20 ? 80 / (PTS + 2) : 20;
 };
 
-// PT consecutive floats from global memory (L2, not L1: written by other CTAs).
-template <int PT>
-__device__ __forceinline__ void ld_part(const float* p, float* r) {
-  if constexpr (PT == 1) {
-    r[0] = __ldcg(p);
-  } else if constexpr (PT == 2) {
-    const float2 x = __ldcg(reinterpret_cast<const float2*>(p));
-    r[0] = x.x; r[1] = x.y;
-  } else {
-#pragma unroll
-    for (int v = 0; v < PT / 4; ++v) {
-      const float4 x = __ldcg(reinterpret_cast<const float4*>(p) + v);
-      r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
-    }
-  }
-}
-template <int PT>
-__device__ __forceinline__ void st_part(float* p, const float* r) {
-  if constexpr (PT == 1) {
-    p[0] = r[0];
-  } else if constexpr (PT == 2) {
-    *reinterpret_cast<float2*>(p) = make_float2(r[0], r[1]);
-  } else {
-#pragma unroll
-    for (int v = 0; v < PT / 4; ++v)
-      reinterpret_cast<float4*>(p)[v] = make_float4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
-  }
-}
-// PT floats (already divided by the softmax sum) to O as fp16.
-template <int PT>
-__device__ __forceinline__ void store_o(__half* dst, const float* r) {
-  if constexpr (PT == 1) {
-    dst[0] = __float2half_rn(r[0]);
-  } else {
-    uint32_t w[PT / 2];
-#pragma unroll
-    for (int i = 0; i < PT / 2; ++i) w[i] = h2u(__floats2half2_rn(r[2 * i], r[2 * i + 1]));
-    if constexpr (PT == 2) *reinterpret_cast<uint32_t*>(dst) = w[0];
-    else if constexpr (PT == 4) *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
-    else *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
-
 // Merge `count` split partials at slots pbase + first + j*stride (j < count) by
-// log-sum-exp.  Every thread merges its own PT outputs straight from global
-// memory: the (max, sum) pair of its head and its numerator words of up to MCH
-// partials are loaded in one round, then folded into a running (M, L, acc).
-// With `orow` set the result is normalized and written to O as fp16; otherwise
-// the unnormalized (M, L, numerator) goes to slot `dst`, which may be one of the
-// slots read (a barrier separates the reads from the writes).  Called by every
-// thread of the CTA.
+// log-sum-exp.  Every thread merges its own slots straight from global memory
+// (L2: other CTAs wrote them): the (max, sum) pair of its head and its slot
+// values of up to MCH partials are loaded in one round, then folded into a
+// running (M, L, acc).  With `orow` set the result is normalized and written to
+// O as fp16; otherwise the unnormalized (M, L, values) go to slot `dst`, which
+// may be one of the slots read (a barrier separates the reads from the writes).
+// Called by every thread of the CTA.
 template <int D, int NT>
-__device__ void merge_parts(const DevState& st, size_t pbase, int first, int stride, int count,
-                            int G, int tid, __half* orow, size_t dst) {
-  constexpr int PT = MergeShape<D, NT>::PT, MCH = MergeShape<D, NT>::MCH;
-  const int GD = G * D;
-  const int i0 = tid * PT;
-  const bool active = i0 < GD;
-  const int hd = i0 / D;
+__device__ __noinline__ void merge_parts(float* __restrict__ part_acc, float* __restrict__ part_ml,
+                                         size_t pbase, int first, int stride, int count, int G,
+                                         int tid, __half* __restrict__ orow, size_t dst) {
+  constexpr int SLOTS = MergeShape<D, NT>::SLOTS, PTS = MergeShape<D, NT>::PTS;
+  constexpr int MCH = MergeShape<D, NT>::MCH;
+  const int hd = slot_head<D>(tid);
+  const bool active = hd < G;  // padding heads of the group are never read
   float M = -CUDART_INF_F, L = 0.f;
-  float acc[PT];
+  float acc[PTS];
 #pragma unroll
-  for (int r = 0; r < PT; ++r) acc[r] = 0.f;
+  for (int k = 0; k < PTS; ++k) acc[k] = 0.f;
   if (active) {
+    const float* accb = part_acc + (pbase + first) * SLOTS + tid;
+    const float* mlb = part_ml + ((pbase + first) * MAX_G + hd) * 2;
+    const size_t astep = (size_t)stride * SLOTS, mstep = (size_t)stride * MAX_G * 2;
     for (int j0 = 0; j0 < count; j0 += MCH) {
       float2 ml[MCH];
-      float a[MCH][PT];
+      float a[MCH][PTS];
 #pragma unroll
       for (int u = 0; u < MCH; ++u) {
         ml[u] = make_float2(-CUDART_INF_F, 0.f);
 #pragma unroll
-        for (int r = 0; r < PT; ++r) a[u][r] = 0.f;
+        for (int k = 0; k < PTS; ++k) a[u][k] = 0.f;
         if (j0 + u < count) {
-          const size_t pid = pbase + first + (size_t)(j0 + u) * stride;
-          ml[u] = __ldcg(reinterpret_cast<const float2*>(st.attn_ml + (pid * G + hd) * 2));
-          ld_part<PT>(st.attn_acc + pid * GD + i0, a[u]);
+          ml[u] = __ldcg(reinterpret_cast<const float2*>(mlb + (j0 + u) * mstep));
+#pragma unroll
+          for (int k = 0; k < PTS; ++k)
+            if (tid + k * NT < SLOTS) a[u][k] = __ldcg(accb + (j0 + u) * astep + k * NT);
         }
       }
       float Mn = M;
@@ -632,13 +634,13 @@ __device__ void merge_parts(const DevState& st, size_t pbase, int first, int str
       const float al = M == -CUDART_INF_F ? 0.f : exp2f(M - Mn);
       L *= al;
 #pragma unroll
-      for (int r = 0; r < PT; ++r) acc[r] *= al;
+      for (int k = 0; k < PTS; ++k) acc[k] *= al;
 #pragma unroll
       for (int u = 0; u < MCH; ++u) {
         const float f = ml[u].x == -CUDART_INF_F ? 0.f : exp2f(ml[u].x - Mn);
         L = fmaf(f, ml[u].y, L);
 #pragma unroll
-        for (int r = 0; r < PT; ++r) acc[r] = fmaf(f, a[u][r], acc[r]);
+        for (int k = 0; k < PTS; ++k) acc[k] = fmaf(f, a[u][k], acc[k]);
       }
       M = Mn;
     }
@@ -647,16 +649,19 @@ __device__ void merge_parts(const DevState& st, size_t pbase, int first, int str
     if (active) {
       const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
-      for (int r = 0; r < PT; ++r) acc[r] *= inv;
-      store_o<PT>(orow + i0, acc);
+      for (int k = 0; k < PTS; ++k)
+        if (tid + k * NT < SLOTS)
+          orow[hd * D + slot_ch<D>(tid + k * NT)] = __float2half_rn(acc[k] * inv);
     }
     return;
   }
   __syncthreads();  // every read of the slots is done before `dst` is overwritten
   if (active) {
-    st_part<PT>(st.attn_acc + dst * GD + i0, acc);
-    if (i0 % D == 0)
-      *reinterpret_cast<float2*>(st.attn_ml + (dst * G + hd) * 2) = make_float2(M, L);
+#pragma unroll
+    for (int k = 0; k < PTS; ++k)
+      if (tid + k * NT < SLOTS) part_acc[dst * SLOTS + tid + k * NT] = acc[k];
+    if ((tid & ~32) < 4)  // the first thread of each head
+      *reinterpret_cast<float2*>(part_ml + (dst * MAX_G + hd) * 2) = make_float2(M, L);
   }
 }
 
@@ -875,7 +880,7 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   }
 
   // ---- merge the warps of this CTA (reusing the stage memory) ----------------------
-  float* sm_acc = reinterpret_cast<float*>(smem);  // [NW][MAX_G][D]
+  float* sm_acc = reinterpret_cast<float*>(smem);  // [NW][SLOTS]
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
     A.l0 += __shfl_xor_sync(0xffffffffu, A.l0, off);
@@ -885,14 +890,12 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
     sm_m[warp][2 * c] = A.m0; sm_m[warp][2 * c + 1] = A.m1;
     sm_l[warp][2 * c] = A.l0; sm_l[warp][2 * c + 1] = A.l1;
   }
-  float* wacc = sm_acc + (size_t)warp * MAX_G * D;
+  constexpr int SLOTS = MergeShape<D, NT>::SLOTS, PTS = MergeShape<D, NT>::PTS;
+  float* wacc = sm_acc + (size_t)warp * SLOTS + lane;
 #pragma unroll
-  for (int mt = 0; mt < NMT; ++mt) {
-    wacc[(2 * c) * D + g * VCH + mt] = A.o[mt][0];
-    wacc[(2 * c + 1) * D + g * VCH + mt] = A.o[mt][1];
-    wacc[(2 * c) * D + g * VCH + NMT + mt] = A.o[mt][2];
-    wacc[(2 * c + 1) * D + g * VCH + NMT + mt] = A.o[mt][3];
-  }
+  for (int mt = 0; mt < NMT; ++mt)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) wacc[(mt * 4 + j) * 32] = A.o[mt][j];
   __syncthreads();
   // Per head: the CTA's max, each warp's weight 2^(m_w - M) and the weighted sum.
   if (tid < G) {
@@ -911,32 +914,34 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   }
   __syncthreads();
 
-  constexpr int PT = MergeShape<D, NT>::PT;
   const size_t pbase = ((size_t)z * st.Hkv + h) * splits;
   const size_t pid = pbase + split;
   __half* orow = o + ((size_t)z * st.Hq + h * G) * D;
   {
-    const int i0 = tid * PT, hd = i0 / D;
-    if (i0 < G * D) {
-      float r[PT];
+    const int hd = slot_head<D>(tid);
+    if (hd < G) {
+      float r[PTS];
 #pragma unroll
-      for (int x = 0; x < PT; ++x) r[x] = 0.f;
+      for (int k = 0; k < PTS; ++k) r[k] = 0.f;
 #pragma unroll
       for (int w = 0; w < NW; ++w) {
         const float f = sm_f[w][hd];
-        const float* src = sm_acc + (size_t)w * MAX_G * D + i0;
 #pragma unroll
-        for (int x = 0; x < PT; ++x) r[x] = fmaf(f, src[x], r[x]);
+        for (int k = 0; k < PTS; ++k)
+          if (tid + k * NT < SLOTS) r[k] = fmaf(f, sm_acc[(size_t)w * SLOTS + tid + k * NT], r[k]);
       }
       if (splits == 1) {
         const float L = sm_ml[hd][1], inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
-        for (int x = 0; x < PT; ++x) r[x] *= inv;
-        store_o<PT>(orow + i0, r);
+        for (int k = 0; k < PTS; ++k)
+          if (tid + k * NT < SLOTS)
+            orow[hd * D + slot_ch<D>(tid + k * NT)] = __float2half_rn(r[k] * inv);
       } else {
-        st_part<PT>(st.attn_acc + pid * G * D + i0, r);
-        if (i0 % D == 0)
-          *reinterpret_cast<float2*>(st.attn_ml + (pid * G + hd) * 2) =
+#pragma unroll
+        for (int k = 0; k < PTS; ++k)
+          if (tid + k * NT < SLOTS) st.attn_acc[pid * SLOTS + tid + k * NT] = r[k];
+        if ((tid & ~32) < 4)
+          *reinterpret_cast<float2*>(st.attn_ml + (pid * MAX_G + hd) * 2) =
               make_float2(sm_ml[hd][0], sm_ml[hd][1]);
       }
     }
@@ -953,13 +958,13 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   int* tk = st.attn_ticket + ((size_t)z * st.Hkv + h) * ATTN_TICKETS;
   if (!last_arrival(tk + 1 + grp, gsize, tid, &s_last)) return;
   if (ngrp == 1) {
-    merge_parts<D, NT>(st, pbase, 0, 1, splits, G, tid, orow, 0);
+    merge_parts<D, NT>(st.attn_acc, st.attn_ml, pbase, 0, 1, splits, G, tid, orow, 0);
     return;
   }
-  merge_parts<D, NT>(st, pbase, grp * ATTN_GROUP, 1, gsize, G, tid, nullptr,
-                     pbase + grp * ATTN_GROUP);
+  merge_parts<D, NT>(st.attn_acc, st.attn_ml, pbase, grp * ATTN_GROUP, 1, gsize, G, tid,
+                     nullptr, pbase + grp * ATTN_GROUP);
   if (!last_arrival(tk, ngrp, tid, &s_last)) return;
-  merge_parts<D, NT>(st, pbase, 0, ATTN_GROUP, ngrp, G, tid, orow, 0);
+  merge_parts<D, NT>(st.attn_acc, st.attn_ml, pbase, 0, ATTN_GROUP, ngrp, G, tid, orow, 0);
 }
 
 template <int D, int VB>

@@ -60,8 +60,8 @@ extern "C" EKV_API int ekv_decode_attn_noalloc(ekv_cache* cache, int32_t layer, 
 
   // Carve the array: [split numerators | split (max, sum) | merge tickets].
   const size_t parts = (size_t)n_seqs * st.Hkv * splits;
-  const size_t acc_bytes = parts * st.G * st.D * sizeof(float);
-  const size_t ml_bytes = parts * st.G * 2 * sizeof(float);
+  const size_t acc_bytes = parts * MAX_G * st.D * sizeof(float);
+  const size_t ml_bytes = parts * MAX_G * 2 * sizeof(float);
   const size_t tk_bytes = (size_t)n_seqs * st.Hkv * ATTN_TICKETS * sizeof(int32_t);
   const size_t acc_off = 0;
   const size_t ml_off = (acc_off + acc_bytes + 255) & ~(size_t)255;
