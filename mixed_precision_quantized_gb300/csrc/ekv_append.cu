@@ -120,7 +120,7 @@ __device__ void seal_k(const __half* stg, const __half* kin, size_t in_row, int 
   __align__(16) __half s16[8];
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
-    s16[c] = k_scale16(m[c], kb);
+    s16[c] = __float2half_rn(__fdiv_rn(m[c], (float)qm));
     sf[c] = __half2float(s16[c]);
   }
   for (int r = 0; r < BLOCK; ++r) {

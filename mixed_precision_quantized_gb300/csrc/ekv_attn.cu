@@ -386,7 +386,7 @@ __device__ __forceinline__ void page_scores(const KL& kl, const uint32_t* qw, fl
   k_row_words<D, KB>(kl, (g + 8) * krow, c, kwb);
   float s1[4] = {0.f, 0.f, 0.f, 0.f};
   s[0] = s[1] = s[2] = s[3] = 0.f;
-  if constexpr (KB == 8) {
+  if constexpr (KB == 4 || KB == 8) {
     // Fold the per-channel K scale into Q: q*s = hi + lo with hi = fp16(q*s) and
     // lo = fp16(q*s - hi) from one fused multiply-add (the residual of a rounded
     // fp16 product is itself an fp16 value).  Two MMA chains against the exact
@@ -412,10 +412,9 @@ __device__ __forceinline__ void page_scores(const KL& kl, const uint32_t* qw, fl
                ql[2 * kk + 1]);
     }
   } else {
-    if constexpr (KB < 16) {
-      // 2- and 4-bit codes times their (pair-ordered) channel scales are exact in
-      // fp16: 2-bit codes are 0 or +-1, +-2, and 4-bit pages store scales with 8
-      // significant bits against codes of at most 3.  One MMA chain with plain Q.
+    if constexpr (KB == 2) {
+      // 2-bit codes are 0, +-1 or -2, so code times its (pair-ordered) channel
+      // scale is exact in fp16: scale the codes and run one MMA chain with plain Q.
       const int so = BLOCK * D * KB / 8 + c * KCH * 2;
 #pragma unroll
       for (int i = 0; i < KW / 4; ++i) {

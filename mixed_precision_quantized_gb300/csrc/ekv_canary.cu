@@ -82,7 +82,7 @@ canary_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
     for (int bi = 0; bi < NBITS; ++bi) {
       const int b = 2 << bi;
       const int qm = (1 << (b - 1)) - 1;
-      const float sf = __half2float(k_scale16(m, b));
+      const float sf = __half2float(__float2half_rn(__fdiv_rn(m, (float)qm)));
       for (int r = r0; r < r1; ++r)
         WQ[(bi * RING + r) * P + c] = (float)quant_code(W[r * P + c], sf, qm) * sf;
     }

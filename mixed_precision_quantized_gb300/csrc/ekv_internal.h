@@ -1,7 +1,6 @@
 // ekv_internal.h — device-side state and helpers shared by the library's kernels.
 #pragma once
 
-#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -71,14 +70,6 @@ struct DevState {
 };
 
 __device__ inline void set_error(const DevState& st, int code) { atomicCAS(st.err, 0, code); }
-
-// Stored K scale of a group of b-bit codes with absmax m: fp16 of m / qmax (IEEE
-// division), for 4-bit codes rounded first to 8 significant bits (bfloat16, ties
-// to even) so that scale * code (|code| <= 7) is exact in fp16.
-__device__ inline __half k_scale16(float m, int b) {
-  const float s = __fdiv_rn(m, (float)((1 << (b - 1)) - 1));
-  return __float2half_rn(b == 4 ? __bfloat162float(__float2bfloat16_rn(s)) : s);
-}
 
 __host__ __device__ inline size_t ls_index(const DevState& st, int l, int s) {
   return (size_t)l * st.S + s;

@@ -10,10 +10,10 @@ summed over the key axis and averaged over all queries of the step.
 
 Readings where the page leaves a step open:
   (i)   the logits carry the layer's attention scale sigma = 1/sqrt(d);
-  (ii)  quant_b is the cache's own symmetric K quantizer (scale precision
-        included), per channel over consecutive 16-row groups of the window
-        starting at the oldest row (the page calls its quantizer KIVI-style
-        asymmetric; the workloads fix the symmetric one);
+  (ii)  quant_b is the cache's own symmetric quantizer, per channel over
+        consecutive 16-row groups of the window starting at the oldest row
+        (the page calls its quantizer KIVI-style asymmetric; the workloads fix
+        the symmetric one);
   (iii) the window is the newest min(count, 64) K's of the (layer, sequence,
         KV head), oldest first, including this step's K;
   (iv)  the queries are this step's Q for every query head of every sequence;
@@ -38,7 +38,7 @@ def window_dequant(w16: np.ndarray, b: int) -> np.ndarray:
     out = np.zeros(w16.shape, dtype=np.float32)
     for g0 in range(0, n, GROUP):
         grp = w16[g0:g0 + GROUP]
-        q, s = quant.quantize(grp, b, axis=0, sig=quant.k_scale_sig(b))
+        q, s = quant.quantize(grp, b, axis=0)
         out[g0:g0 + GROUP] = quant.dequantize(q, s, axis=0)
     return out
 

@@ -99,7 +99,7 @@ class SeqState:
             if kb == 16:
                 self._kh[lo:hi] = self._k[lo:hi].astype(np.float32)
             else:
-                q, s = quant.quantize(self._k[lo:hi], kb, axis=0, sig=quant.k_scale_sig(kb))
+                q, s = quant.quantize(self._k[lo:hi], kb, axis=0)
                 self._kh[lo:hi] = quant.dequantize(q, s, axis=0)
         self._sealed_upto = max(self._sealed_upto, full)
         out = self._kh[:T].copy()

@@ -16,7 +16,6 @@ Layout (our storage reading; the pages only say "packed low-bit storage"):
             vb = 16 : raw fp16 [16][d]
     page  = K part || V part            (little-endian fp16)
 
-K scales of 4-bit pages keep 8 significant bits (quant.k_scale_sig).
 The K scales of 2- and 4-bit pages are stored in "pair order": within each
 group of n = 32/kb channels (the channels of one 32-bit code word), scale
 position p holds channel p // 2 + (p % 2) * n / 2, i.e. 0, n/2, 1, n/2+1, ...
@@ -76,7 +75,7 @@ def sealed_k_bytes(kb: int, k16: np.ndarray) -> dict:
     assert k16.shape[0] == BLOCK
     if kb == 16:
         return {"k_raw": k16.view(np.uint8).reshape(BLOCK, -1)}
-    q, s = quant.quantize(k16, kb, axis=0, sig=quant.k_scale_sig(kb))  # one group per channel
+    q, s = quant.quantize(k16, kb, axis=0)          # one group per channel
     s = s[scale_order(kb, k16.shape[1])]
     return {"k_codes": quant.pack(q, kb), "k_scales": s.astype(np.float16).view(np.uint8)[None, :]}
 

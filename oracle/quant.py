@@ -16,12 +16,6 @@ All divisions are IEEE fp32 correctly rounded (numpy float32 arithmetic),
 rne is round-half-to-even (numpy.rint), and the fp32 -> fp16 conversion is
 numpy's round-to-nearest-even.
 
-Scale precision (our storage reading; the pages fix none): the K scales of
-4-bit groups keep 8 significant bits, s = fp16_rne( bf16_rne( fp32(m) /
-fp32(qmax) ) ), so that every s * q (|q| <= 7, three significant bits) is
-exact in fp16.  All other scales keep fp16's 11 bits (2-bit codes are
-powers of two or zero, so s * q is exact for them anyway).
-
 Stored code (our storage reading; the pages only say "packed low-bit
 storage"): u = q + 2**(b-1) (offset binary), b bits per element, elements
 packed along the channel axis least-significant-bits first: element c lives
@@ -41,33 +35,15 @@ def qmax(b: int) -> int:
     return (1 << (b - 1)) - 1
 
 
-def k_scale_sig(b: int) -> int:
-    """Significant bits kept in a stored K scale of b-bit codes."""
-    return 8 if b == 4 else 11
-
-
-def bf16_rne(x32: np.ndarray) -> np.ndarray:
-    """Round finite fp32 values to 8 significant bits (bfloat16), ties to even."""
-    u = np.asarray(x32, dtype=F32).view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
-    return u.astype(np.uint32).view(F32)
-
-
-def quantize(x16: np.ndarray, b: int, axis: int, sig: int = 11):
-    """Quantize fp16 `x16` in groups along `axis` -> (q int16, s fp16 with `axis` removed).
-
-    `sig` is the scale's significant bits: 11 (fp16) or 8 (bfloat16 precision)."""
+def quantize(x16: np.ndarray, b: int, axis: int):
+    """Quantize fp16 `x16` in groups along `axis` -> (q int16, s fp16 with `axis` removed)."""
     x16 = np.asarray(x16)
     if x16.dtype != F16:
         raise TypeError("quantizer input must be fp16")
-    if sig not in (8, 11):
-        raise ValueError("scale precision is 8 or 11 significant bits")
     x = x16.astype(F32)
     qm = F32(qmax(b))
     m = np.max(np.abs(x), axis=axis, keepdims=True)
     s32 = (m / qm).astype(F32)
-    if sig == 8:
-        s32 = bf16_rne(s32)
     s16 = s32.astype(F16)
     sf = s16.astype(F32)
     with np.errstate(divide="ignore", invalid="ignore"):

@@ -26,7 +26,7 @@ def test_admit_time_bits_survive_tier_change():
     assert st.kbits == [4, 2, 8]
     kh = st.khat()
     # block 0 sealed at 4 bits, block 1 sealed at 2 bits, block 2 (8 rows) still raw
-    q, s = quant.quantize(st.k[0:16], 4, axis=0, sig=8)        # 4-bit K scales: 8 bits
+    q, s = quant.quantize(st.k[0:16], 4, axis=0)
     assert np.array_equal(kh[0:16], quant.dequantize(q, s, axis=0))
     q, s = quant.quantize(st.k[16:32], 2, axis=0)
     assert np.array_equal(kh[16:32], quant.dequantize(q, s, axis=0))
@@ -85,7 +85,7 @@ def test_page_expect_regions_decode():
     e = st.page_expect(0, 1)
     q = quant.unpack(e["k_codes"], 4, 64)
     s = np.frombuffer(e["k_scales"].tobytes(), dtype=F16)
-    q2, s2 = quant.quantize(k[:, 1], 4, axis=0, sig=8)
+    q2, s2 = quant.quantize(k[:, 1], 4, axis=0)
     assert np.array_equal(q, q2)
     # 4-bit pages store each 8-channel group's scales as 0,4,1,5,2,6,3,7
     for grp in range(8):

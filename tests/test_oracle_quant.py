@@ -134,63 +134,3 @@ def test_generator_cpu_batched_matches_single():
     b1 = synth.draw16(0, 1, synth.T_K, 3, [5], [23], 4, 2, 64)
     assert torch.equal(a[0], b0[0])
     assert torch.equal(a[1, 3:], b1[0])
-
-
-# ---- K scales of 4-bit groups: 8 significant bits --------------------------------
-
-
-def _struct_scale8(m: float, b: int) -> float:
-    """fp16 of the bfloat16 (ties to even) of the fp32 of m/qmax, bit by bit."""
-    qm = (1 << (b - 1)) - 1
-    u = struct.unpack("<I", struct.pack("<f", m / qm))[0]
-    hi, lo = u >> 16, u & 0xFFFF
-    if lo > 0x8000 or (lo == 0x8000 and hi & 1):
-        hi += 1
-    s = struct.unpack("<f", struct.pack("<I", hi << 16))[0]
-    return struct.unpack("<e", struct.pack("<e", s))[0]
-
-
-def test_k_scale_sig_by_width():
-    assert [quant.k_scale_sig(b) for b in (2, 4, 8)] == [11, 8, 11]
-
-
-def test_bf16_rounding_ties_to_even():
-    x = np.array([1 + 2.0**-8, 1 + 3 * 2.0**-8, 1 + 2.0**-8 + 2.0**-20, 1 - 2.0**-9, 0.0],
-                 dtype=np.float32)
-    assert quant.bf16_rne(x).tolist() == [1.0, 1 + 2.0**-6, 1 + 2.0**-7, 1.0, 0.0]
-
-
-def test_k4_scale_one_seventh():
-    # fp32(1/7) = 0x3E124925; the low half 0x4925 < 0x8000 rounds down to 0x3E12 =
-    # 1.140625 * 2^-3 = 0.142578125, fp16 bits 0 01100 0010010000 = 0x3090.
-    # 1/0.142578125 = 7.0137 -> 7;  -0.5/0.142578125 = -3.5068 -> -4.
-    q, s = quant.quantize(h(1.0, -0.5), 4, axis=0, sig=8)
-    assert np.asarray(s, dtype=F16).view(np.uint16) == 0x3090
-    assert q.tolist() == [7, -4]
-
-
-@pytest.mark.parametrize("b", [2, 4, 8])
-def test_brute_force_8bit_scales(b):
-    z = synth.draw16(9, 97, synth.T_K, b, [0], [0], 60, 1, 16)[0, :, 0].numpy()
-    groups = [z[i] for i in range(40)]
-    groups += [(z[i].astype(np.float32) * 10).astype(F16) for i in range(40, 50)]
-    groups += [(z[i].astype(np.float32) * 2e-5).astype(F16) for i in range(50, 60)]
-    for g in groups:
-        q, s = quant.quantize(g, b, axis=0, sig=8)
-        m = float(np.max(np.abs(g.astype(np.float64))))
-        assert float(s) == _struct_scale8(m, b)
-        for xi, qi in zip(g.astype(np.float64), q.tolist()):
-            assert qi == _brute_q(xi, float(s), b)
-
-
-def test_k4_scaled_codes_exact_in_fp16():
-    # Every stored 4-bit K scale times every code is an fp16 value: the attention
-    # kernel scales the codes in fp16 and relies on this.
-    z = synth.draw16(11, 96, synth.T_K, 4, [0], [0], 16, 8, 128)[0].numpy()   # [16, 8, 128]
-    for gain in (1.0, 37.0, 3e-3, 1e-6):
-        x = (z.astype(np.float32) * np.float32(gain)).astype(F16)
-        _, s = quant.quantize(x, 4, axis=0, sig=quant.k_scale_sig(4))
-        sv = s.astype(np.float64)
-        for c in range(-7, 8):
-            prod = c * sv
-            assert np.array_equal(prod.astype(F16).astype(np.float64), prod)
