@@ -190,14 +190,14 @@ def main():
     import torch
     import torch.distributed as dist
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    from mixed_precision_quantized_gb300 import replicas, workloads
+
+    R = replicas.from_env()
+    world, rank, local = R.world, R.rank, R.local
     if world > 1:
         dist.init_process_group("nccl" if a.impl == "ekv" else "gloo")
-    from mixed_precision_quantized_gb300 import workloads
 
-    w = workloads.by_name(a.workload)
+    w = replicas.shard(workloads.by_name(a.workload), rank)
     if a.layers:
         w = w.scaled(num_layers=a.layers)
 
@@ -260,15 +260,13 @@ def main():
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     clk = Clocks(local).__enter__()
-    if world > 1:
-        dist.barrier()
+    replicas.barrier(R)
     with torch.cuda.stream(stream):
         ev0.record(stream)
         gA.replay()
         ev1.record(stream)
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+    replicas.barrier(R)
     tA = ev0.elapsed_time(ev1) / 1e3
     cache.sync()
     fired_A = sum(1 for i in range(W, W + K) if w.fires(i))
@@ -380,38 +378,30 @@ def main():
 
         gE = capture(e2e_steps)
         torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
+        replicas.barrier(R)
         with torch.cuda.stream(stream):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             gE.replay()
             e1.record(stream)
         torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
+        replicas.barrier(R)
         tE = e0.elapsed_time(e1) / 1e3
         cache.sync()
-        if world > 1:
-            tt = torch.tensor([tE], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            tE = float(tt)
-        e2e = {"value": world * B * K / tE, "unit": "tokens/s",
+        tE = replicas.max_over_ranks(R, tE, dev)
+        e2e = {"value": replicas.whole_job_rate(R, B * K, tE), "unit": "tokens/s",
                "h2d_bytes_per_step": int(host_in.shape[1] * 2),
                "d2h_bytes_per_step": int(out.numel() * 2)}
 
     clk.__exit__(None, None, None)
-    if world > 1:
-        tt = torch.tensor([tA], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        tA = float(tt)
+    tA = replicas.max_over_ranks(R, tA, dev)
 
     peak, peak_kind = peaks()
     achieved = bytes_per_launch / attn_avg_s / 1e9 if attn_avg_s else None
     step_bytes = sum(layer_bytes)
     line = {
         "metric": METRIC,
-        "value": world * B * K / tA,
+        "value": replicas.whole_job_rate(R, B * K, tA),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": K,
