@@ -2,8 +2,9 @@
 
 One step = one decode token for every sequence through every layer: per layer
 append (ring write, V quantization, K staging/seal, page admission at the
-layer's tier) and decode attention over the whole cache; on every 64th step the
-canary runs for every layer and the controller updates the tiers.
+layer's tier) and decode attention over the whole cache, as one fused launch
+(`--separate`: two launches); on every 64th step the canary runs for every
+layer and the controller updates the tiers.
 
 Default workload: Llama-3.1-70B shape, 80 layers, batch 1, 64 q / 8 kv heads,
 head_dim 128, 131072 cached tokens, K starting at INT4 with the canary every 64
@@ -14,8 +15,8 @@ outlier channel (x10) per head and K gain 1 + 0.05 * layer.  A step reads
 Timed regions (all on one stream, CUDA events, synchronize + barrier on both
 sides, max over ranks):
   A  K steps replayed as one CUDA graph                  -> value, ms_per_step
-  B  the next K steps, each attention launch bracketed by
-     timing events inside the graph                      -> roofline (attention)
+  B  the next K steps, each attention launch (fused: append + attention)
+     bracketed by timing events inside the graph         -> roofline (attention)
   E  the next K steps with a pinned-host -> device copy of the step's inputs
      and a device -> pinned-host copy of every layer's output per step -> e2e
 The canary cost is timed separately (all layers' canary + one controller
@@ -44,8 +45,8 @@ METRIC = "quantized-KV decode attn HBM GB/s (% of peak), tokens/s; canary µs/fi
 # (profiles/decode_attn_llama70b_128k.md: 2-layer case, the same per-launch
 # work as one layer of the full workload), valid only for the kernel source it
 # was taken on: any change to that source reports null until re-captured.
-TRAFFIC_BYTES = 157.07e6
-TRAFFIC_SOURCE_SHA = "b5fecbe25e3d4644"
+TRAFFIC_BYTES = 157.28e6
+TRAFFIC_SOURCE_SHA = "86204270f4d1932c"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -62,13 +63,15 @@ def parse():
     p.add_argument("--layers", type=int, default=0,
                    help="run only the first N layers of the workload (profiling cases)")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    p.add_argument("--separate", action="store_true",
+                   help="append and attention as two launches per layer (default: one fused launch)")
     return p.parse_args()
 
 
 def attn_source_sha() -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in ("ekv_attn.cu", "ekv_internal.h"):
+    for f in ("ekv_attn.cu", "ekv_internal.h", "ekv_quant.cuh"):
         with open(os.path.join(ROOT, "mixed_precision_quantized_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -222,6 +225,7 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     K, W = a.steps, a.warmup
+    fused = not a.separate
     if W < 3:
         raise SystemExit("at least 3 warm-up steps")
     n_steps_total = W + (3 if not a.no_e2e else 2) * K
@@ -241,7 +245,7 @@ def main():
 
     # warm-up (eager)
     for i in range(W):
-        runner.decode_step(cache, w, slots, inp, i, outs, w.fires(i))
+        runner.decode_step(cache, w, slots, inp, i, outs, w.fires(i), fused=fused)
     cache.sync()
 
     stream = torch.cuda.Stream(device=dev)
@@ -254,9 +258,10 @@ def main():
         return g
 
     # ---- A: K steps as one graph -------------------------------------------------
-    gA = capture(lambda: [runner.decode_step(cache, w, slots, inp, i, outs, w.fires(i))
-                          for i in range(W, W + K)])
-    launches = sum(2 * L + ((L + 1) if w.fires(i) else 0) for i in range(W, W + K))
+    gA = capture(lambda: [runner.decode_step(cache, w, slots, inp, i, outs, w.fires(i),
+                                             fused=fused) for i in range(W, W + K)])
+    per_layer = 1 if fused else 2
+    launches = sum(per_layer * L + ((L + 1) if w.fires(i) else 0) for i in range(W, W + K))
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     clk = Clocks(local).__enter__()
@@ -283,10 +288,14 @@ def main():
         for n, i in enumerate(range(W + K, W + 2 * K)):
             for l in range(L):
                 q, k, v = inp.layer(l, i)
-                cache.append(l, slots, k, v)
+                if not fused:
+                    cache.append(l, slots, k, v)
                 if external_ok:
                     pairs[n * L + l][0].record(stream)
-                cache.decode_attn(l, slots, q, outs[l])
+                if fused:
+                    cache.append_decode_attn(l, slots, k, v, q, outs[l])
+                else:
+                    cache.decode_attn(l, slots, q, outs[l])
                 if external_ok:
                     pairs[n * L + l][1].record(stream)
                 if w.fires(i):
@@ -325,6 +334,14 @@ def main():
         c1.record(stream)
     torch.cuda.synchronize()
     canary_us = c0.elapsed_time(c1) * 1e3 / reps
+    # With the fused step, region A holds nothing but the L fused launches of each
+    # step and its canary firings: their time, less the firings (timed just
+    # above), over the K * L launches is the launch duration inside the step
+    # (inter-launch gaps included).  Events around each launch (region B) add
+    # their own gaps; that figure is kept beside it.
+    bracketed_s = attn_avg_s
+    if fused:
+        attn_avg_s = (tA - fired_A * canary_us * 1e-6) / (K * L)
 
     # ---- attention alone, all layers back to back (read-only, replayable) ------
     def attn_only():
@@ -368,8 +385,11 @@ def main():
                 i = s0 + n
                 dbuf.copy_(host_in[n], non_blocking=True)
                 for l in range(L):
-                    cache.append(l, slots, kd[l], vd[l])
-                    cache.decode_attn(l, slots, qd[l], outs[l])
+                    if fused:
+                        cache.append_decode_attn(l, slots, kd[l], vd[l], qd[l], outs[l])
+                    else:
+                        cache.append(l, slots, kd[l], vd[l])
+                        cache.decode_attn(l, slots, qd[l], outs[l])
                     if w.fires(i):
                         cache.canary_kl(l, slots, qd[l])
                 if w.fires(i):
@@ -419,7 +439,9 @@ def main():
                                f"(tau {w.tau}), V INT{w.v_bits[0]}",
                    "l2": f"inputs larger than L2: {step_bytes / 1e9:.2f} GB of pages read per step",
                    "parallelism": f"replicas x{world} (one sequence set per GPU)",
-                   "graph": "CUDA graph of the timed steps", "canary_fires_in_timed": fired_A},
+                   "graph": "CUDA graph of the timed steps", "canary_fires_in_timed": fired_A,
+                   "step": ("one fused append + attention launch per layer" if fused
+                            else "append and attention launches per layer")},
         "attn_hbm_gbs": achieved,
         "attn_frac_of_8tbs": achieved / NOMINAL_HBM_GBS if achieved else None,
         "step_hbm_gbs": step_bytes / (tA / K) / 1e9,
@@ -429,13 +451,18 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak if achieved else None,
                      "traffic": (TRAFFIC_BYTES if attn_source_sha() == TRAFFIC_SOURCE_SHA
-                                 and w.name == "llama70b_128k" and not a.layers else None),
+                                 and w.name == "llama70b_128k" and not a.layers and fused
+                                 else None),
                      "traffic_unit": "bytes per launch",
-                     "kernel": "decode_attn_kernel", "peak_kind": peak_kind,
+                     "kernel": ("decode_attn_kernel (fused append + attention)" if fused
+                                else "decode_attn_kernel"), "peak_kind": peak_kind,
                      "bytes_per_launch": bytes_per_launch,
                      "avg_launch_us": attn_avg_s * 1e6 if attn_avg_s else None,
-                     "launches_timed": len(attn_ms),
-                     "timing": "events around each launch inside timed region B" if attn_ms
+                     "launches_timed": K * L if fused else len(attn_ms),
+                     "bracketed_launch_us": bracketed_s * 1e6 if bracketed_s else None,
+                     "timing": ("timed region A (CUDA events around the K steps) less its "
+                                "canary firings, per fused launch") if fused else
+                               "events around each launch inside timed region B" if attn_ms
                                else "attention-only graph (all layers back to back)",
                      "attn_only_avg_us": attn_only_us},
         "e2e": e2e,

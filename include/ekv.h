@@ -144,6 +144,24 @@ EKV_API int ekv_append(ekv_cache* cache, int32_t layer, int32_t n_seqs, const in
 EKV_API int ekv_decode_attn(ekv_cache* cache, int32_t layer, int32_t n_seqs, const int32_t* seq_slots,
                     const void* q, void* o, void* stream);
 
+/* One decode step of one layer in one launch: ekv_append with n_new = 1
+ * followed by ekv_decode_attn, with the same results (pages, staging rows,
+ * ring, length and o; o's fp32 summation order may differ, as it does between
+ * any two launches).  The append work of each (sequence, KV head) runs inside
+ * the attention launch, on the split that holds the sequence's last block,
+ * while the other splits stream their pages, so the step pays one launch and
+ * no separate chain of append memory round trips.  The pages define the two
+ * steps ("How EchoKV works": the step's K enters the ring and the paged cache
+ * before attention reads it); fusing them is this library's choice.
+ *   k, v [n_seqs][Hkv][d] fp16 dev — the new token of each sequence
+ *   q, o as ekv_decode_attn.  All four 16-byte aligned.
+ * Errors as the two calls: EKV_ENOMEM on the device when a pool runs empty;
+ * a sequence whose table is full gets EKV_ESTATE, no append, and attention
+ * over its old tokens. */
+EKV_API int ekv_append_decode_attn(ekv_cache* cache, int32_t layer, int32_t n_seqs,
+                                   const int32_t* seq_slots, const void* k, const void* v,
+                                   const void* q, void* o, void* stream);
+
 /* Allocation-free decode attention.  The pages have no counterpart of this
  * entry point; it exists for callers that cannot allocate device memory where
  * they run attention (a process that reserves all device memory at start-up

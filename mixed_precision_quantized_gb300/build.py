@@ -34,7 +34,8 @@ def sources() -> list:
 
 def _digest(extra: list) -> str:
     h = hashlib.sha256()
-    files = sources() + sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".h"))
+    files = sources() + sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC)
+                             if f.endswith((".h", ".cuh")))
     files.append(os.path.join(INCLUDE, "ekv.h"))
     for f in files:
         h.update(f.encode())

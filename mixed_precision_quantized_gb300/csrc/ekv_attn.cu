@@ -33,6 +33,7 @@
 #include <math_constants.h>
 
 #include "ekv_internal.h"
+#include "ekv_quant.cuh"
 
 namespace ekv {
 namespace {
@@ -134,20 +135,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   return false;
 }
 
-// ---- loads from global (open block) or shared memory (pipelined pages) ------------
+// ---- loads from global (last block) or shared memory (pipelined pages) ------------
+// The last block is read through L2 (.cg): with the fused append its newest row
+// (or the whole sealed page) was written earlier in the same launch.
 struct GLd {
   const uint8_t* p;
   __device__ __forceinline__ uint4 v4(int o) const {
-    return __ldg(reinterpret_cast<const uint4*>(p + o));
+    return __ldcg(reinterpret_cast<const uint4*>(p + o));
   }
   __device__ __forceinline__ uint2 v2(int o) const {
-    return __ldg(reinterpret_cast<const uint2*>(p + o));
+    return __ldcg(reinterpret_cast<const uint2*>(p + o));
   }
   __device__ __forceinline__ uint32_t v1(int o) const {
-    return __ldg(reinterpret_cast<const uint32_t*>(p + o));
+    return __ldcg(reinterpret_cast<const uint32_t*>(p + o));
   }
   __device__ __forceinline__ uint32_t h1(int o) const {
-    return __ldg(reinterpret_cast<const uint16_t*>(p + o));
+    return __ldcg(reinterpret_cast<const uint16_t*>(p + o));
   }
 };
 // Shared-memory loads through a pointer into the dynamic shared array: ordinary
@@ -680,10 +683,63 @@ __device__ __forceinline__ bool last_arrival(int* ticket, int expected, int tid,
   return *s_flag != 0;
 }
 
-template <int D, int VB>
+// The fused append of one token, by one warp: the same steps as the append
+// kernel for n_new = 1 ("How EchoKV works": the step's K enters the layer's
+// FP16 ring and, quantized, the paged cache; "What happens to old blocks when a
+// layer changes tier?": a block's page is admitted at the tier current when its
+// first token arrives).  Block j receives the token at row r: a page is popped
+// when r == 0, the V row is quantized into it, the K row goes to the staging
+// rows or, at r == 15, seals the block.  Returns the page entry (-1: none).
+template <int D>
+__device__ int32_t append_token(const DevState& st, int layer, int slot, int h, int j, int r,
+                                int told, const __half* kin, const __half* vin, int lane) {
+  constexpr int CH = D / 8;
+  int32_t e = -1;
+  if (lane == 0) {
+    int32_t* btp = st.bt + lsh_index(st, layer, slot, h) * st.maxblk + j;
+    if (r == 0) {  // block opens now: admit at the layer's current tier
+      const int fmt = code_of_bits(st.tier[layer]) * 4 + code_of_bits(st.vbits[layer]);
+      const int old = atomicSub(st.top + fmt, 1);
+      if (old <= 0) {
+        atomicAdd(st.top + fmt, 1);
+        set_error(st, EKV_ENOMEM);
+      } else {
+        e = (int32_t)(((uint32_t)fmt << 28) | (uint32_t)st.stack[fmt][old - 1]);
+        atomicMax(st.kmax + layer, st.tier[layer]);
+      }
+      *btp = e;
+    } else {
+      e = *btp;
+      if (e == -1) set_error(st, EKV_ESTATE);  // an existing block must have a page
+    }
+  }
+  e = __shfl_sync(0xffffffffu, e, 0);
+  const size_t lsh = lsh_index(st, layer, slot, h);
+  __half* stg = st.staging + lsh * (BLOCK * D);
+  if (e != -1) {
+    const int fmt = entry_fmt(e);
+    const int kb = bits_of_code(fmt >> 2), vb = bits_of_code(fmt & 3);
+    uint8_t* page = st.pool_base[fmt] + (size_t)entry_idx(e) * st.pool_page_bytes[fmt];
+    quant_v_row<D>(vin, page + k_part_bytes(kb, D), r, vb, lane);
+    if (r == BLOCK - 1) {
+      if (lane < CH) seal_k<D>(stg, kin, 0, j, told, kb, page, lane);
+    } else if (lane < CH) {
+      *reinterpret_cast<uint4*>(stg + (size_t)r * D + 8 * lane) =
+          *reinterpret_cast<const uint4*>(kin + 8 * lane);
+    }
+  }
+  if (lane < CH)  // ring: the newest 64 K vectors, slot p % 64
+    *reinterpret_cast<uint4*>(st.ring + lsh * (RING * D) + (size_t)(told % RING) * D + 8 * lane) =
+        *reinterpret_cast<const uint4*>(kin + 8 * lane);
+  __syncwarp();  // the block's new bytes are visible to the warp's loads that follow
+  return e;
+}
+
+template <int D, int VB, bool FUSED>
 __global__ void __launch_bounds__(AttnCfg<VB>::NT, 1)
 decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
-                   const __half* __restrict__ q, __half* __restrict__ o, int splits) {
+                   const __half* __restrict__ q, __half* __restrict__ o, int splits,
+                   const __half* __restrict__ knew, const __half* __restrict__ vnew) {
   constexpr int NW = AttnCfg<VB>::NW, NT = AttnCfg<VB>::NT;
   constexpr int KCH = D / 4, KW = KCH / 2, VCH = D / 8, NMT = D / 16;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -698,15 +754,29 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   const int G = st.G;
   const int slot = slots[z];
   const bool slot_ok = slot >= 0 && slot < st.S;
-  const int T = slot_ok ? st.len[ls_index(st, layer, slot)] : 0;
+  const int told = slot_ok ? st.len[ls_index(st, layer, slot)] : 0;
+  // Fused append: this launch adds one token to every sequence and attends over
+  // it too.  Every CTA reads the old length; the last CTA of the sequence to be
+  // done with it publishes the new one (ticket below).
+  bool app = false;
+  if constexpr (FUSED) {
+    if (!slot_ok) {
+      if (tid == 0 && split == 0 && h == 0) set_error(st, EKV_EINVAL);
+    } else if (told + 1 > st.maxblk * BLOCK) {  // would outgrow the block table
+      if (tid == 0 && split == 0 && h == 0) set_error(st, EKV_ESTATE);
+    } else {
+      app = true;
+    }
+  }
+  const int T = told + (app ? 1 : 0);
   const int nb = (T + BLOCK - 1) / BLOCK;
   const int cb = (nb + splits - 1) / splits;
   const int b0 = min(nb, split * cb), b1 = min(nb, b0 + cb);
-  // Sealed blocks of this split go through the pipelines; the open block (the
-  // sequence's last, raw K rows in the staging buffer) is attended from global
-  // memory by the split that holds it.
-  const bool open_here = (T % BLOCK) != 0 && b1 == nb && b1 > b0;
-  int np = b1 - b0 - (open_here ? 1 : 0);  // pipelined pages of this split
+  // Sealed blocks of this split go through the pipelines.  The sequence's last
+  // block is attended from global memory by the split that holds it when it is
+  // open (raw K rows in the staging buffer) or receives this launch's token.
+  const bool last_apart = ((T % BLOCK) != 0 || app) && b1 == nb && b1 > b0;
+  int np = b1 - b0 - (last_apart ? 1 : 0);  // pipelined pages of this split
   if (np > ATTN_BT_CAP) {  // the host sizes splits so that this never happens
     if (tid == 0) set_error(st, EKV_ESTATE);
     np = 0;
@@ -782,18 +852,34 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
     }
   }
 
-  // The open block first, while this warp's copies are in flight.
-  if (open_here && warp == NW - 1) {
-    const int32_t e = bt[nb - 1];
-    if (e == -1) {
-      if (lane == 0) set_error(st, EKV_ESTATE);
+  // The last block first (with the fused append, after appending to it), while
+  // this warp's copies are in flight.
+  if (last_apart && warp == NW - 1) {
+    int32_t e;
+    if (app) {
+      const size_t in = ((size_t)z * st.Hkv + h) * D;
+      e = append_token<D>(st, layer, slot, h, nb - 1, told % BLOCK, told, knew + in, vnew + in,
+                          lane);
     } else {
+      e = __ldcg(bt + nb - 1);
+      if (e == -1 && lane == 0) set_error(st, EKV_ESTATE);
+    }
+    if (e != -1) {
       const int fmt = entry_fmt(e);
       const uint8_t* page = st.pool_base[fmt] + (size_t)entry_idx(e) * st.pool_page_bytes[fmt];
-      const GLd kl{reinterpret_cast<const uint8_t*>(stg)};
-      const GLd vl{page + k_part_bytes(bits_of_code(fmt >> 2), D)};
-      pair_q(KBits<16>{});
-      attend_pages<D, VB, false, 16>(kl, vl, T % BLOCK, kl, vl, 0, qw, A, sl, g, c);
+      const int kb = bits_of_code(fmt >> 2);
+      const GLd vl{page + k_part_bytes(kb, D)};
+      if (T % BLOCK == 0) {  // sealed by this launch's token: a full page
+        with_kbits(kb, [&](auto kbc) {
+          constexpr int KB = decltype(kbc)::value;
+          pair_q(kbc);
+          attend_pages<D, VB, true, KB>(GLd{page}, vl, BLOCK, GLd{page}, vl, 0, qw, A, sl, g, c);
+        });
+      } else {
+        const GLd kl{reinterpret_cast<const uint8_t*>(stg)};
+        pair_q(KBits<16>{});
+        attend_pages<D, VB, false, 16>(kl, vl, T % BLOCK, kl, vl, 0, qw, A, sl, g, c);
+      }
     }
   }
 
@@ -834,21 +920,19 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
         attend_pages<D, VB, true, KB>(SLd{sa}, SLd{sa + KP}, BLOCK, SLd{sb}, SLd{sb + KP},
                                       BLOCK, qw, A, sl, g, c);
       });
-    } else {
-      if (kba != 0)
-        with_kbits(kba, [&](auto kbc) {
+    } else {  // one page at a time, through one call site per K width
+#pragma unroll 1
+      for (int pass = 0; pass < 2; ++pass) {
+        const int kbx = pass ? kbb : kba;
+        if (kbx == 0) continue;
+        const uint8_t* x = pass ? sb : sa;
+        with_kbits(kbx, [&](auto kbc) {
           constexpr int KB = decltype(kbc)::value;
           pair_q(kbc);
-          attend_pages<D, VB, true, KB>(SLd{sa}, SLd{sa + k_part_bytes(KB, D)}, BLOCK, SLd{sa},
-                                        SLd{sa}, 0, qw, A, sl, g, c);
+          attend_pages<D, VB, true, KB>(SLd{x}, SLd{x + k_part_bytes(KB, D)}, BLOCK, SLd{x},
+                                        SLd{x}, 0, qw, A, sl, g, c);
         });
-      if (kbb != 0)
-        with_kbits(kbb, [&](auto kbc) {
-          constexpr int KB = decltype(kbc)::value;
-          pair_q(kbc);
-          attend_pages<D, VB, true, KB>(SLd{sb}, SLd{sb + k_part_bytes(KB, D)}, BLOCK, SLd{sb},
-                                        SLd{sb}, 0, qw, A, sl, g, c);
-        });
+      }
     }
     __syncwarp();
     // Refill both stages with the split's next two pages (none once the pages
@@ -945,6 +1029,15 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
       }
     }
   }
+  if constexpr (FUSED) {
+    if (app && tid == 0) {  // every CTA of this sequence has read the old length
+      int* tk = st.append_ticket + ls_index(st, layer, slot);
+      if (atomicAdd(tk, 1) == splits * st.Hkv - 1) {
+        st.len[ls_index(st, layer, slot)] = T;
+        *tk = 0;
+      }
+    }
+  }
   if (splits == 1) return;
 
   // ---- merge of the splits ------------------------------------------------------------
@@ -968,22 +1061,29 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
 
 template <int D, int VB>
 cudaError_t launch_t(const DevState& st, int layer, int n_seqs, const int32_t* slots,
-                     const __half* q, __half* o, int splits, cudaStream_t s) {
+                     const __half* q, __half* o, int splits, const __half* knew,
+                     const __half* vnew, cudaStream_t s) {
   dim3 grid(splits, st.Hkv, n_seqs);
-  decode_attn_kernel<D, VB><<<grid, AttnCfg<VB>::NT, AttnCfg<VB>::SMEM, s>>>(st, layer, slots, q, o,
-                                                                           splits);
+  if (knew)
+    decode_attn_kernel<D, VB, true><<<grid, AttnCfg<VB>::NT, AttnCfg<VB>::SMEM, s>>>(
+        st, layer, slots, q, o, splits, knew, vnew);
+  else
+    decode_attn_kernel<D, VB, false><<<grid, AttnCfg<VB>::NT, AttnCfg<VB>::SMEM, s>>>(
+        st, layer, slots, q, o, splits, nullptr, nullptr);
   return cudaGetLastError();
 }
 
 template <int D, int VB>
 cudaError_t init_t() {
-  cudaError_t e = cudaFuncSetAttribute(decode_attn_kernel<D, VB>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       AttnCfg<VB>::SMEM);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(decode_attn_kernel<D, VB>,
-                             cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
+  cudaError_t e = cudaSuccess;
+  for (auto fn : {decode_attn_kernel<D, VB, false>, decode_attn_kernel<D, VB, true>}) {
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               AttnCfg<VB>::SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+  }
   return e;
 }
 
@@ -1001,20 +1101,21 @@ cudaError_t attn_init() {
 }
 
 cudaError_t launch_decode_attn(const DevState& st, int layer, int n_seqs, const int32_t* slots,
-                               const __half* q, __half* o, int splits, int vb, cudaStream_t s) {
+                               const __half* q, __half* o, int splits, int vb, cudaStream_t s,
+                               const __half* knew, const __half* vnew) {
   if (st.D == 64) {
     switch (vb) {
-      case 2: return launch_t<64, 2>(st, layer, n_seqs, slots, q, o, splits, s);
-      case 4: return launch_t<64, 4>(st, layer, n_seqs, slots, q, o, splits, s);
-      case 8: return launch_t<64, 8>(st, layer, n_seqs, slots, q, o, splits, s);
-      default: return launch_t<64, 16>(st, layer, n_seqs, slots, q, o, splits, s);
+      case 2: return launch_t<64, 2>(st, layer, n_seqs, slots, q, o, splits, knew, vnew, s);
+      case 4: return launch_t<64, 4>(st, layer, n_seqs, slots, q, o, splits, knew, vnew, s);
+      case 8: return launch_t<64, 8>(st, layer, n_seqs, slots, q, o, splits, knew, vnew, s);
+      default: return launch_t<64, 16>(st, layer, n_seqs, slots, q, o, splits, knew, vnew, s);
     }
   }
   switch (vb) {
-    case 2: return launch_t<128, 2>(st, layer, n_seqs, slots, q, o, splits, s);
-    case 4: return launch_t<128, 4>(st, layer, n_seqs, slots, q, o, splits, s);
-    case 8: return launch_t<128, 8>(st, layer, n_seqs, slots, q, o, splits, s);
-    default: return launch_t<128, 16>(st, layer, n_seqs, slots, q, o, splits, s);
+    case 2: return launch_t<128, 2>(st, layer, n_seqs, slots, q, o, splits, knew, vnew, s);
+    case 4: return launch_t<128, 4>(st, layer, n_seqs, slots, q, o, splits, knew, vnew, s);
+    case 8: return launch_t<128, 8>(st, layer, n_seqs, slots, q, o, splits, knew, vnew, s);
+    default: return launch_t<128, 16>(st, layer, n_seqs, slots, q, o, splits, knew, vnew, s);
   }
 }
 

@@ -260,6 +260,21 @@ int ekv_decode_attn(ekv_cache* c, int32_t layer, int32_t n_seqs, const int32_t* 
                                         splits, c->vbits[layer], as_stream(stream)));
 }
 
+int ekv_append_decode_attn(ekv_cache* c, int32_t layer, int32_t n_seqs, const int32_t* seq_slots,
+                           const void* k, const void* v, const void* q, void* o, void* stream) {
+  if (!c || layer < 0 || layer >= c->st.L || n_seqs < 0 || n_seqs > c->st.S) return EKV_EINVAL;
+  if (n_seqs == 0) return EKV_OK;
+  if (!seq_slots || !k || !v || !q || !o) return EKV_EINVAL;
+  if (((uintptr_t)k | (uintptr_t)v | (uintptr_t)q | (uintptr_t)o) & 15) return EKV_EINVAL;
+  const int splits = attn_splits(c, n_seqs, c->vbits[layer]);
+  if (n_seqs * c->st.Hkv * splits > c->st.attn_parts_cap) return EKV_ESTATE;
+  return cuda_status(launch_decode_attn(c->st, layer, n_seqs, seq_slots,
+                                        static_cast<const __half*>(q), static_cast<__half*>(o),
+                                        splits, c->vbits[layer], as_stream(stream),
+                                        static_cast<const __half*>(k),
+                                        static_cast<const __half*>(v)));
+}
+
 int ekv_canary_kl(ekv_cache* c, int32_t layer, int32_t n_seqs, const int32_t* seq_slots,
                   const void* q, float* delta_out, void* stream) {
   if (!c || layer < 0 || layer >= c->st.L || n_seqs <= 0 || n_seqs > c->st.S) return EKV_EINVAL;

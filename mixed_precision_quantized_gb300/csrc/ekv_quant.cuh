@@ -1,0 +1,148 @@
+// ekv_quant.cuh — the cache's symmetric quantizer on the device: V rows (per
+// token) and sealed K blocks (per channel over the block's 16 tokens), written
+// in the page layout.  Shared by the append kernel and the fused append +
+// attention kernel.
+//
+// Quantizer ("Behavior-Guided KV-Cache Quantization", "K/V Role-Aware Low-Bit
+// Quantization": symmetric, K per channel, V per token; KV-Kaizen, "Three
+// Non-Eviction Compression Axes", item 3: symmetric uniform):
+//   s = fp16_rne(m / qmax) with m = absmax of the group (IEEE fp32 division),
+//   q = clamp(rne(x / s), -qmax, qmax), stored offset binary q + 2^(b-1).
+#pragma once
+
+#include "ekv_internal.h"
+
+namespace ekv {
+namespace {
+
+__device__ __forceinline__ void unpack8(const uint4& u, float* f) {
+  const __half2* h = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __half22float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+// q = clamp(rne(x / s), -qmax, qmax); IEEE division, RNE conversion.
+__device__ __forceinline__ int quant_code(float x, float s, int qm) {
+  if (s == 0.f) return 0;
+  const int q = __float2int_rn(__fdiv_rn(x, s));
+  return min(max(q, -qm), qm);
+}
+
+// 8 offset-binary codes of b bits, LSB first, as one little-endian word.
+__device__ __forceinline__ void store_codes8(uint8_t* dst, const int* u, int b) {
+  if (b == 2) {
+    uint32_t w = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w |= (uint32_t)u[i] << (2 * i);
+    *reinterpret_cast<uint16_t*>(dst) = (uint16_t)w;
+  } else if (b == 4) {
+    uint32_t w = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w |= (uint32_t)u[i] << (4 * i);
+    *reinterpret_cast<uint32_t*>(dst) = w;
+  } else {
+    unsigned long long w = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w |= (unsigned long long)u[i] << (8 * i);
+    *reinterpret_cast<unsigned long long*>(dst) = w;
+  }
+}
+
+// One V row (one token of one KV head): absmax over D channels, one fp16 scale.
+// Called by a whole warp; lanes < D/8 own 8 channels each.
+template <int D>
+__device__ void quant_v_row(const __half* src, uint8_t* vpart, int r, int vb, int lane) {
+  constexpr int CH = D / 8;
+  uint4 u = make_uint4(0, 0, 0, 0);
+  float f[8];
+  float m = 0.f;
+  if (lane < CH) {
+    u = *reinterpret_cast<const uint4*>(src + 8 * lane);
+    unpack8(u, f);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) m = fmaxf(m, fabsf(f[c]));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if (lane >= CH) return;
+  if (vb == 16) {
+    *reinterpret_cast<uint4*>(vpart + (size_t)r * 2 * D + 16 * lane) = u;
+    return;
+  }
+  const int qm = (1 << (vb - 1)) - 1;
+  const __half s16 = __float2half_rn(__fdiv_rn(m, (float)qm));
+  const float sf = __half2float(s16);
+  int code[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) code[c] = quant_code(f[c], sf, qm) + (1 << (vb - 1));
+  store_codes8(vpart + (size_t)r * (D * vb / 8) + lane * vb, code, vb);
+  if (lane == 0) *reinterpret_cast<__half*>(vpart + BLOCK * D * vb / 8 + 2 * r) = s16;
+}
+
+// Seal a full K block: thread t owns channels [8t, 8t+8) over the 16 rows.
+// Rows before `told` come from the staging rows, the rest from the input.
+template <int D>
+__device__ void seal_k(const __half* stg, const __half* kin, size_t in_row, int j, int told,
+                       int kb, uint8_t* kpart, int t) {
+  float m[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) m[c] = 0.f;
+  auto row_ptr = [&](int r) -> const __half* {
+    const int p = j * BLOCK + r;
+    return p < told ? stg + (size_t)r * D + 8 * t : kin + (size_t)(p - told) * in_row + 8 * t;
+  };
+  if (kb == 16) {
+    for (int r = 0; r < BLOCK; ++r)
+      *reinterpret_cast<uint4*>(kpart + (size_t)r * 2 * D + 16 * t) =
+          *reinterpret_cast<const uint4*>(row_ptr(r));
+    return;
+  }
+  for (int r = 0; r < BLOCK; ++r) {
+    float f[8];
+    unpack8(*reinterpret_cast<const uint4*>(row_ptr(r)), f);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) m[c] = fmaxf(m[c], fabsf(f[c]));
+  }
+  const int qm = (1 << (kb - 1)) - 1;
+  float sf[8];
+  __align__(16) __half s16[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    s16[c] = __float2half_rn(__fdiv_rn(m[c], (float)qm));
+    sf[c] = __half2float(s16[c]);
+  }
+  for (int r = 0; r < BLOCK; ++r) {
+    float f[8];
+    unpack8(*reinterpret_cast<const uint4*>(row_ptr(r)), f);
+    int code[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) code[c] = quant_code(f[c], sf[c], qm) + (1 << (kb - 1));
+    store_codes8(kpart + (size_t)r * (D * kb / 8) + t * kb, code, kb);
+  }
+  // Scales in pair order: within each group of n = 32/kb channels (one 32-bit
+  // code word) position p holds channel p/2 + (p%2)*n/2; 8-bit pages keep the
+  // natural order.  Thread t owns channels 8t .. 8t+7.
+  __half* sdst = reinterpret_cast<__half*>(kpart + BLOCK * D * kb / 8);
+  if (kb == 8) {
+    *reinterpret_cast<uint4*>(sdst + 8 * t) = *reinterpret_cast<const uint4*>(s16);
+  } else if (kb == 4) {  // group = this thread's 8 channels: 0,4,1,5,2,6,3,7
+    __align__(16) __half o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      o[2 * i] = s16[i];
+      o[2 * i + 1] = s16[i + 4];
+    }
+    *reinterpret_cast<uint4*>(sdst + 8 * t) = *reinterpret_cast<const uint4*>(o);
+  } else {  // kb == 2: group of 16 channels = threads 2m, 2m+1
+    __half* grp = sdst + 16 * (t / 2);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) grp[2 * i + (t & 1)] = s16[i];
+  }
+}
+
+}  // namespace
+}  // namespace ekv

@@ -54,6 +54,7 @@ _SIGS = {
     "ekv_seq_reset": (ctypes.c_int, [_P, _I32, _P]),
     "ekv_append": (ctypes.c_int, [_P, _I32, _I32, _P, _I32, _P, _P, _P]),
     "ekv_decode_attn": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P, _P]),
+    "ekv_append_decode_attn": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P, _P, _P, _P]),
     "ekv_decode_attn_noalloc": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P, _P]),
     "ekv_canary_kl": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P, _P]),
     "ekv_tier_update": (ctypes.c_int, [_P, _P, _P, _I32, _P]),
@@ -184,6 +185,18 @@ class Cache:
             out = torch.empty_like(q)
         _check(lib().ekv_decode_attn(self._h, layer, seq_slots.numel(), _ptr(seq_slots), _ptr(q),
                                      _ptr(out), _stream(stream)), "ekv_decode_attn")
+        return out
+
+    def append_decode_attn(self, layer: int, seq_slots: torch.Tensor, k: torch.Tensor,
+                           v: torch.Tensor, q: torch.Tensor, out: torch.Tensor | None = None,
+                           stream=None) -> torch.Tensor:
+        """One decode step of a layer in one launch: append one token (k, v of shape
+        [n, 1, Hkv, d] or [n, Hkv, d]) to every sequence, then attend over it too."""
+        if out is None:
+            out = torch.empty_like(q)
+        _check(lib().ekv_append_decode_attn(self._h, layer, seq_slots.numel(), _ptr(seq_slots),
+                                            _ptr(k), _ptr(v), _ptr(q), _ptr(out),
+                                            _stream(stream)), "ekv_append_decode_attn")
         return out
 
     def decode_attn_noalloc(self, layer: int, seq_slots: torch.Tensor, q: torch.Tensor,

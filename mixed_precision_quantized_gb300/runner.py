@@ -48,12 +48,17 @@ def prefill(cache: ekv.Cache, w: workloads.Workload, slots: torch.Tensor, device
 
 
 def decode_step(cache: ekv.Cache, w: workloads.Workload, slots: torch.Tensor, inp: Inputs,
-                i: int, out: list, fires: bool, delta_out: torch.Tensor | None = None):
-    """One decode step over all layers; out[l] ([B,Hq,d]) receives each layer's O."""
+                i: int, out: list, fires: bool, delta_out: torch.Tensor | None = None,
+                fused: bool = False):
+    """One decode step over all layers; out[l] ([B,Hq,d]) receives each layer's O.
+    With `fused` each layer's append and attention run as one launch."""
     for l in range(w.num_layers):
         q, k, v = inp.layer(l, i)
-        cache.append(l, slots, k, v)
-        cache.decode_attn(l, slots, q, out[l])
+        if fused:
+            cache.append_decode_attn(l, slots, k, v, q, out[l])
+        else:
+            cache.append(l, slots, k, v)
+            cache.decode_attn(l, slots, q, out[l])
         if fires:
             cache.canary_kl(l, slots, q, None if delta_out is None else delta_out[l])
     if fires:

@@ -73,8 +73,8 @@ class Run:
     """A workload on the GPU next to its oracle."""
 
     def __init__(self, w: workloads.Workload, steps: int, layers=None, seqs=None, heads=None,
-                 gen_device="cuda", trace=None, pool_pages=None):
-        self.w, self.steps = w, steps
+                 gen_device="cuda", trace=None, pool_pages=None, fused=False):
+        self.w, self.steps, self.fused = w, steps, fused
         if pool_pages is None:
             self.cache = ekv.cache_for(w)
         else:
@@ -98,7 +98,8 @@ class Run:
     def step(self, check_attn_now: bool = True):
         w, t = self.w, self.t
         fires = w.fires(t)
-        runner.decode_step(self.cache, w, self.slots, self.inp, t, self.out, fires)
+        runner.decode_step(self.cache, w, self.slots, self.inp, t, self.out, fires,
+                           fused=self.fused)
         self.cache.sync()
         self.ref.advance()
         if check_attn_now:

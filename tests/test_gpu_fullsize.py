@@ -1,6 +1,7 @@
 """Full-size workloads, run through the C ABI exactly as bench.py runs them
-(same library, same split schedule), checked against the oracle on sampled
-outputs the oracle can compute one by one:
+(same library, same split schedule, the fused append + attention launch; the
+single-layer sweep uses the separate append and attention calls), checked
+against the oracle on sampled outputs the oracle can compute one by one:
 
   * the controller over ALL layers at every firing: canary readings within
     1e-4 and tiers bit-exact (or a flip inside the reading tolerance of tau);
@@ -23,8 +24,8 @@ def _lib():
     ekv.lib()
 
 
-def _sampled(w, steps, layers, seqs, heads, attn_steps):
-    r = Run(w, steps, layers=layers, seqs=seqs, heads=heads)
+def _sampled(w, steps, layers, seqs, heads, attn_steps, fused=True):
+    r = Run(w, steps, layers=layers, seqs=seqs, heads=heads, fused=fused)
     try:
         for t in range(steps):
             r.step(check_attn_now=t in attn_steps)
@@ -60,4 +61,5 @@ def test_llama8b_batch32_full():
 def test_llama8b_layer_full(bits):
     """One layer, 8 sequences x 4096 tokens, uniform K = V bits, 64 steps."""
     w = workloads.llama8b_layer(bits)
-    _sampled(w, 64, layers=[0], seqs=[0, 7], heads=[0, 3, 7], attn_steps={0, 31, 63})
+    _sampled(w, 64, layers=[0], seqs=[0, 7], heads=[0, 3, 7], attn_steps={0, 31, 63},
+             fused=False)

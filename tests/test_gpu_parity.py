@@ -19,8 +19,11 @@ def _lib():
     ekv.lib()
 
 
-def _full_run(w, steps, attn_steps=None):
-    r = Run(w, steps)
+FUSED = pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])
+
+
+def _full_run(w, steps, attn_steps=None, fused=False):
+    r = Run(w, steps, fused=fused)
     try:
         for t in range(steps):
             r.step(check_attn_now=attn_steps is None or t in attn_steps)
@@ -30,50 +33,58 @@ def _full_run(w, steps, attn_steps=None):
         r.close()
 
 
-def test_tiny_config_brute_force():
+@FUSED
+def test_tiny_config_brute_force(fused):
     """2 layers, d=64, K bits [4,8], V8, canary + controller every step."""
-    err, flips = _full_run(workloads.tiny(), 8)
+    err, flips = _full_run(workloads.tiny(), 8, fused=fused)
     assert flips == []
 
 
 @pytest.mark.parametrize("bits", [2, 4, 8, 16])
-def test_llama8b_layer_small(bits):
+@FUSED
+def test_llama8b_layer_small(bits, fused):
     """Uniform K=V bits, G=4, ragged prefill tail (300 = 18 blocks + 12), crosses a block."""
     w = workloads.llama8b_layer(bits).scaled(batch=2, prefill=[300, 300], steps=6)
-    _full_run(w, 6)
+    _full_run(w, 6, fused=fused)
 
 
-def test_qwen14b_mixed_small():
+@FUSED
+def test_qwen14b_mixed_small(fused):
     """G=5 (padding heads), per-layer K bits 2/4/8 mixed across layers, V4."""
     w = workloads.qwen14b_32k()
     w = w.scaled(num_layers=3, prefill=[1000], steps=4,
                  k_bits_init=[2, 4, 8], v_bits=[4, 4, 4])
-    _full_run(w, 4)
+    _full_run(w, 4, fused=fused)
 
 
-def test_llama70b_controller_small():
+@FUSED
+def test_llama70b_controller_small(fused):
     """Canary every 64 steps changes tiers mid-run: pages of several formats in one layer."""
     w = workloads.llama70b_128k().scaled(num_layers=2, prefill=[700], steps=130)
-    err, flips = _full_run(w, 130, attn_steps={0, 1, 15, 63, 64, 65, 100, 127, 128, 129})
+    err, flips = _full_run(w, 130, attn_steps={0, 1, 15, 63, 64, 65, 100, 127, 128, 129},
+                           fused=fused)
 
 
-def test_llama8b_batch_ragged_small():
+@FUSED
+def test_llama8b_batch_ragged_small(fused):
     """Ragged batch incl. a sequence shorter than the ring (37 tokens), tau 0.03."""
     w = workloads.llama8b_batch32().scaled(num_layers=2, batch=4, prefill=[37, 300, 129, 64],
                                            steps=70)
-    _full_run(w, 70, attn_steps={0, 1, 2, 26, 27, 28, 63, 64, 65, 69})
+    _full_run(w, 70, attn_steps={0, 1, 2, 26, 27, 28, 63, 64, 65, 69}, fused=fused)
 
 
 @pytest.mark.parametrize("T0,d,Hq,Hkv", [(1, 64, 2, 2), (15, 128, 8, 1), (16, 64, 8, 8),
                                          (17, 128, 16, 2), (33, 128, 40, 8)])
-def test_edge_lengths_and_groups(T0, d, Hq, Hkv):
+@FUSED
+def test_edge_lengths_and_groups(T0, d, Hq, Hkv, fused):
     """Single-token, 15/16/17-token prefills, G = 1, 2, 5, 8."""
     w = workloads.Workload("edge", 9, 1, 1, Hq, Hkv, d, [T0], 20, [4], [8],
                            outlier_frac=0.02, outlier_gain=8.0)
-    _full_run(w, 20)
+    _full_run(w, 20, fused=fused)
 
 
-def test_mixed_formats_in_one_layer_forced_tiers():
+@FUSED
+def test_mixed_formats_in_one_layer_forced_tiers(fused):
     """Tiers forced 2 -> 16 -> 8 -> 4 mid-run: one layer holds four K formats (V16)."""
     w = workloads.Workload("mixed", 10, 1, 2, 8, 2, 128, [40, 23], 70, [2], [16])
     sched = {0: 2, 10: 16, 30: 8, 50: 4}
@@ -83,7 +94,7 @@ def test_mixed_formats_in_one_layer_forced_tiers():
         cur = sched.get(t, cur)
         tr.tiers.append([cur])
     pools = {(kb, 16): 64 for kb in (2, 4, 8, 16)}
-    r = Run(w, 70, trace=tr, pool_pages=pools)
+    r = Run(w, 70, trace=tr, pool_pages=pools, fused=fused)
     try:
         for t in range(70):
             if t in sched:
