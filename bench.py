@@ -386,7 +386,8 @@ def main():
                 dbuf.copy_(host_in[n], non_blocking=True)
                 for l in range(L):
                     if fused:
-                        cache.append_decode_attn(l, slots, kd[l], vd[l], qd[l], outs[l])
+                        cache.append_decode_attn(l, slots, kd[l], vd[l], qd[l], outs[l],
+                                                 after_other_layer=l > 0 and not w.fires(i))
                     else:
                         cache.append(l, slots, kd[l], vd[l])
                         cache.decode_attn(l, slots, qd[l], outs[l])

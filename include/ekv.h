@@ -155,12 +155,20 @@ EKV_API int ekv_decode_attn(ekv_cache* cache, int32_t layer, int32_t n_seqs, con
  * before attention reads it); fusing them is this library's choice.
  *   k, v [n_seqs][Hkv][d] fp16 dev — the new token of each sequence
  *   q, o as ekv_decode_attn.  All four 16-byte aligned.
+ *   flags   0 or EKV_AFTER_OTHER_LAYER: the caller states that the work queued
+ *           on `stream` just before this call is an ekv_append_decode_attn of
+ *           another layer of the same handle, and that it writes none of this
+ *           call's seq_slots, k, v and q.  The launch then starts on the SMs the
+ *           previous launch frees and streams this layer's pages while that
+ *           launch finishes; it waits for it before writing o or the handle's
+ *           shared split scratch.  Any other flag bit: EKV_EINVAL.
  * Errors as the two calls: EKV_ENOMEM on the device when a pool runs empty;
  * a sequence whose table is full gets EKV_ESTATE, no append, and attention
  * over its old tokens. */
+#define EKV_AFTER_OTHER_LAYER 1
 EKV_API int ekv_append_decode_attn(ekv_cache* cache, int32_t layer, int32_t n_seqs,
                                    const int32_t* seq_slots, const void* k, const void* v,
-                                   const void* q, void* o, void* stream);
+                                   const void* q, void* o, int32_t flags, void* stream);
 
 /* Allocation-free decode attention.  The pages have no counterpart of this
  * entry point; it exists for callers that cannot allocate device memory where

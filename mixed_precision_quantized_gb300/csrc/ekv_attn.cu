@@ -242,18 +242,22 @@ __device__ __forceinline__ void k_row_words(const LD& ld, int row, int c, uint32
 }
 
 // ---- V: token pair (t, t+1), chunk of VCH = D/8 channels -> VCH words -------------
-// Word i = (v[t][ch i], v[t+1][ch i]).  For quantized V the words hold the
+// Word i = (v[t][ch i], v[t+1][ch i]).  For 4- and 8-bit V the words hold the
 // *biased* codes the exponent trick yields, A_i = vmul(i) * q + vbias(i) (exact
 // fp16 integers); the bias is removed once per warp at the end (see Acc::ps).
+// The bias is ~1024 times a 2-bit code, so fp32 accumulation error would grow by
+// that much: 2-bit V words are turned into the exact codes q before the MMA.
 // Raw fp16 for 16-bit V.
 template <int VB>
+__host__ __device__ constexpr bool vbias_trick() { return VB == 4 || VB == 8; }
+template <int VB>
 __host__ __device__ constexpr float vmul(int i) {
-  return VB == 4 ? ((i & 1) ? 16.f : 1.f) : VB == 2 ? (float)(1 << (2 * (i & 3))) : 1.f;
+  return VB == 4 ? ((i & 1) ? 16.f : 1.f) : 1.f;
 }
 template <int VB>
 __host__ __device__ constexpr float vbias(int i) {
   // 1024 (the exponent pattern) + vmul(i) * 2^(VB-1) (the code offset)
-  return 1024.f + vmul<VB>(i) * (float)(1 << (VB - 1));
+  return vbias_trick<VB>() ? 1024.f + vmul<VB>(i) * (float)(1 << (VB - 1)) : 0.f;
 }
 
 // `flip` (0 or 0x4444) marks lanes that loaded the pair's rows in swapped order
@@ -302,10 +306,10 @@ __device__ __forceinline__ void v_pair_words(const LD& ld, int r0, int r1, uint3
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         const uint32_t y = q ? shr8(x) : x;
-        vw[8 * h + 4 * q + 0] = lop3_and_or(y, 0x00030003u, H_MAGIC);
-        vw[8 * h + 4 * q + 1] = lop3_and_or(y, 0x000C000Cu, H_MAGIC);
-        vw[8 * h + 4 * q + 2] = lop3_and_or(y, 0x00300030u, H_MAGIC);
-        vw[8 * h + 4 * q + 3] = lop3_and_or(y, 0x00C000C0u, H_MAGIC);
+        vw[8 * h + 4 * q + 0] = hsub2u(lop3_and_or(y, 0x00030003u, H_MAGIC), H_1026);
+        vw[8 * h + 4 * q + 1] = hfma2u(lop3_and_or(y, 0x000C000Cu, H_MAGIC), H_Q4, H_M258);
+        vw[8 * h + 4 * q + 2] = hfma2u(lop3_and_or(y, 0x00300030u, H_MAGIC), H_Q16, H_M66);
+        vw[8 * h + 4 * q + 3] = hfma2u(lop3_and_or(y, 0x00C000C0u, H_MAGIC), H_Q64, H_M18);
       }
     }
   } else if constexpr (VB == 8) {
@@ -326,7 +330,7 @@ __device__ __forceinline__ void v_pair_words(const LD& ld, int r0, int r1, uint3
 }
 
 // Online-softmax state of one warp (per thread: heads 2c, 2c+1 of the group).
-// o: O^T fragments (biased for quantized V); ps: running sum of the fp16 P'
+// o: O^T fragments (biased for 4- and 8-bit V); ps: running sum of the fp16 P'
 // that entered the PV products, per head (C fragment of P'^T summed over its
 // 16 rows by an MMA with an all-ones A), used to remove the V code bias.
 template <int D>
@@ -474,7 +478,7 @@ __device__ __forceinline__ void page_pv(const VL& vl, uint32_t pb0, uint32_t pb1
 #pragma unroll
   for (int mt = 0; mt < NMT; ++mt)
     mma16816(A.o[mt], va[mt], va[NMT + mt], vb[mt], vb[NMT + mt], pb0, pb1);
-  if constexpr (VB < 16) {
+  if constexpr (vbias_trick<VB>()) {
     constexpr uint32_t ONES = 0x3C003C00u;  // fp16 (1, 1)
     mma16816(A.ps, ONES, ONES, ONES, ONES, pb0, pb1);
   }
@@ -526,7 +530,7 @@ __device__ __forceinline__ void attend_pages(const KLA& kla, const VLA& vla, int
       for (int i = 0; i < NMT; ++i) {
         A.o[i][0] *= al0; A.o[i][1] *= al1; A.o[i][2] *= al0; A.o[i][3] *= al1;
       }
-      if constexpr (VB < 16) {
+      if constexpr (vbias_trick<VB>()) {
         A.ps[0] *= al0; A.ps[1] *= al1; A.ps[2] *= al0; A.ps[3] *= al1;
       }
       A.m0 = mn0;
@@ -748,7 +752,11 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   __shared__ int s_next, s_last;
   int32_t* s_bt = reinterpret_cast<int32_t*>(smem + AttnCfg<VB>::STAGE_SMEM);
 
-  const int split = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
+  // Block order: sequence fastest, then KV head, then split, so the CTAs that
+  // start last are the last split of every (sequence, KV head).
+  const int n_seqs = gridDim.x / (splits * st.Hkv);
+  const int z = blockIdx.x % n_seqs, h = blockIdx.x / n_seqs % st.Hkv;
+  const int split = blockIdx.x / (n_seqs * st.Hkv);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
   const int G = st.G;
@@ -770,8 +778,17 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   }
   const int T = told + (app ? 1 : 0);
   const int nb = (T + BLOCK - 1) / BLOCK;
-  const int cb = (nb + splits - 1) / splits;
-  const int b0 = min(nb, split * cb), b1 = min(nb, b0 + cb);
+  // Contiguous block ranges, the last split's 1/8 short of an even share: when
+  // this launch overlaps the end of the one before (programmatic dependent), the
+  // last split's CTAs are the ones that get an SM last, after that launch's
+  // final merges.
+  int b0 = 0, b1 = nb;
+  if (splits > 1) {
+    const int rest = nb - nb * 7 / (8 * splits);
+    const int cb = (rest + splits - 2) / (splits - 1);
+    b0 = split < splits - 1 ? min(rest, split * cb) : rest;
+    b1 = split < splits - 1 ? min(rest, b0 + cb) : nb;
+  }
   // Sealed blocks of this split go through the pipelines.  The sequence's last
   // block is attended from global memory by the split that holds it when it is
   // open (raw K rows in the staging buffer) or receives this launch's token.
@@ -951,7 +968,7 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   // ---- remove the V code bias: o_c = (o_c - vbias(c) * sum P') / vmul(c) ------------
   // Channel c of m-tile mt, rows g and g+8, has chunk index mt or NMT + mt, whose
   // class (position of its code in the word) depends on mt only.
-  if constexpr (VB < 16) {
+  if constexpr (vbias_trick<VB>()) {
 #pragma unroll
     for (int mt = 0; mt < NMT; ++mt) {
       const float bias = vbias<VB>(mt), inv = 1.f / vmul<VB>(mt);
@@ -996,6 +1013,13 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
     sm_ml[tid][1] = L;
   }
   __syncthreads();
+
+  // Launched as a programmatic dependent, everything above overlapped the end of
+  // the launch before it in the stream, which may still be using the shared
+  // split scratch and O: wait for it here, then let the next launch start its
+  // own page reads on the SMs as they free up.  Both are no-ops otherwise.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const size_t pbase = ((size_t)z * st.Hkv + h) * splits;
   const size_t pid = pbase + split;
@@ -1062,8 +1086,22 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
 template <int D, int VB>
 cudaError_t launch_t(const DevState& st, int layer, int n_seqs, const int32_t* slots,
                      const __half* q, __half* o, int splits, const __half* knew,
-                     const __half* vnew, cudaStream_t s) {
-  dim3 grid(splits, st.Hkv, n_seqs);
+                     const __half* vnew, bool overlap, cudaStream_t s) {
+  dim3 grid(splits * st.Hkv * n_seqs);
+  if (knew && overlap) {  // programmatic dependent of the launch before it
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(AttnCfg<VB>::NT);
+    cfg.dynamicSmemBytes = AttnCfg<VB>::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_attn_kernel<D, VB, true>, st, layer, slots, q, o,
+                              splits, knew, vnew);
+  }
   if (knew)
     decode_attn_kernel<D, VB, true><<<grid, AttnCfg<VB>::NT, AttnCfg<VB>::SMEM, s>>>(
         st, layer, slots, q, o, splits, knew, vnew);
@@ -1102,21 +1140,15 @@ cudaError_t attn_init() {
 
 cudaError_t launch_decode_attn(const DevState& st, int layer, int n_seqs, const int32_t* slots,
                                const __half* q, __half* o, int splits, int vb, cudaStream_t s,
-                               const __half* knew, const __half* vnew) {
-  if (st.D == 64) {
-    switch (vb) {
-      case 2: return launch_t<64, 2>(st, layer, n_seqs, slots, q, o, splits, knew, vnew, s);
-      case 4: return launch_t<64, 4>(st, layer, n_seqs, slots, q, o, splits, knew, vnew, s);
-      case 8: return launch_t<64, 8>(st, layer, n_seqs, slots, q, o, splits, knew, vnew, s);
-      default: return launch_t<64, 16>(st, layer, n_seqs, slots, q, o, splits, knew, vnew, s);
-    }
-  }
-  switch (vb) {
-    case 2: return launch_t<128, 2>(st, layer, n_seqs, slots, q, o, splits, knew, vnew, s);
-    case 4: return launch_t<128, 4>(st, layer, n_seqs, slots, q, o, splits, knew, vnew, s);
-    case 8: return launch_t<128, 8>(st, layer, n_seqs, slots, q, o, splits, knew, vnew, s);
-    default: return launch_t<128, 16>(st, layer, n_seqs, slots, q, o, splits, knew, vnew, s);
-  }
+                               const __half* knew, const __half* vnew, bool overlap) {
+  using Fn = cudaError_t (*)(const DevState&, int, int, const int32_t*, const __half*, __half*,
+                             int, const __half*, const __half*, bool, cudaStream_t);
+  const int vi = vb == 2 ? 0 : vb == 4 ? 1 : vb == 8 ? 2 : 3;
+  static const Fn d64[] = {launch_t<64, 2>, launch_t<64, 4>, launch_t<64, 8>, launch_t<64, 16>};
+  static const Fn d128[] = {launch_t<128, 2>, launch_t<128, 4>, launch_t<128, 8>,
+                            launch_t<128, 16>};
+  return (st.D == 64 ? d64 : d128)[vi](st, layer, n_seqs, slots, q, o, splits, knew, vnew,
+                                       overlap, s);
 }
 
 }  // namespace ekv

@@ -46,8 +46,9 @@ int attn_splits(const ekv_cache* c, int n_seqs, int vb) {
   const int target = attn_ctas_per_sm(vb) * c->num_sm;
   int s = (target + units - 1) / units;
   if (s < 1) s = 1;
-  // A split's page-table entries must fit the kernel's shared-memory copy.
-  const int need = (c->st.maxblk + ATTN_BT_CAP - 1) / ATTN_BT_CAP;
+  // A split's page-table entries must fit the kernel's shared-memory copy (the
+  // splits but the last share the blocks, hence the one extra).
+  const int need = (c->st.maxblk + ATTN_BT_CAP - 1) / ATTN_BT_CAP + 1;
   if (s < need) s = need;
   if (s > ATTN_MAX_SPLITS) s = ATTN_MAX_SPLITS;
   return s;
@@ -261,7 +262,9 @@ int ekv_decode_attn(ekv_cache* c, int32_t layer, int32_t n_seqs, const int32_t* 
 }
 
 int ekv_append_decode_attn(ekv_cache* c, int32_t layer, int32_t n_seqs, const int32_t* seq_slots,
-                           const void* k, const void* v, const void* q, void* o, void* stream) {
+                           const void* k, const void* v, const void* q, void* o, int32_t flags,
+                           void* stream) {
+  if (flags & ~EKV_AFTER_OTHER_LAYER) return EKV_EINVAL;
   if (!c || layer < 0 || layer >= c->st.L || n_seqs < 0 || n_seqs > c->st.S) return EKV_EINVAL;
   if (n_seqs == 0) return EKV_OK;
   if (!seq_slots || !k || !v || !q || !o) return EKV_EINVAL;
@@ -272,7 +275,8 @@ int ekv_append_decode_attn(ekv_cache* c, int32_t layer, int32_t n_seqs, const in
                                         static_cast<const __half*>(q), static_cast<__half*>(o),
                                         splits, c->vbits[layer], as_stream(stream),
                                         static_cast<const __half*>(k),
-                                        static_cast<const __half*>(v)));
+                                        static_cast<const __half*>(v),
+                                        (flags & EKV_AFTER_OTHER_LAYER) != 0));
 }
 
 int ekv_canary_kl(ekv_cache* c, int32_t layer, int32_t n_seqs, const int32_t* seq_slots,

@@ -84,10 +84,13 @@ cudaError_t launch_append(const DevState& st, int layer, int n_seqs, const int32
 cudaError_t attn_init();   // once per process, before any launch
 int attn_ctas_per_sm(int vb);  // resident decode-attention CTAs per SM for V width vb
 // With knew/vnew set ([n_seqs][Hkv][d] fp16 each) the launch first appends that
-// one token to every sequence (the fused decode step), then attends over it too.
+// one token to every sequence (the fused decode step), then attends over it too;
+// `overlap` launches it as a programmatic dependent of the stream's previous
+// launch (which must be the fused step of another layer).
 cudaError_t launch_decode_attn(const DevState& st, int layer, int n_seqs, const int32_t* slots,
                                const __half* q, __half* o, int splits, int vb, cudaStream_t s,
-                               const __half* knew = nullptr, const __half* vnew = nullptr);
+                               const __half* knew = nullptr, const __half* vnew = nullptr,
+                               bool overlap = false);
 cudaError_t canary_init();  // once per process, before any launch
 cudaError_t launch_canary(const DevState& st, int layer, int n_seqs, const int32_t* slots,
                           const __half* q, float* delta_out, cudaStream_t s);

@@ -17,6 +17,7 @@ from . import build as _build
 BITS = (2, 4, 8, 16)
 _CODE = {2: 0, 4: 1, 8: 2, 16: 3}
 NUM_FORMATS = 16
+AFTER_OTHER_LAYER = 1  # ekv_append_decode_attn flag
 
 
 def fmt_index(k_bits: int, v_bits: int) -> int:
@@ -54,7 +55,7 @@ _SIGS = {
     "ekv_seq_reset": (ctypes.c_int, [_P, _I32, _P]),
     "ekv_append": (ctypes.c_int, [_P, _I32, _I32, _P, _I32, _P, _P, _P]),
     "ekv_decode_attn": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P, _P]),
-    "ekv_append_decode_attn": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P, _P, _P, _P]),
+    "ekv_append_decode_attn": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P, _P, _P, _I32, _P]),
     "ekv_decode_attn_noalloc": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P, _P]),
     "ekv_canary_kl": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P, _P]),
     "ekv_tier_update": (ctypes.c_int, [_P, _P, _P, _I32, _P]),
@@ -189,13 +190,16 @@ class Cache:
 
     def append_decode_attn(self, layer: int, seq_slots: torch.Tensor, k: torch.Tensor,
                            v: torch.Tensor, q: torch.Tensor, out: torch.Tensor | None = None,
-                           stream=None) -> torch.Tensor:
+                           after_other_layer: bool = False, stream=None) -> torch.Tensor:
         """One decode step of a layer in one launch: append one token (k, v of shape
-        [n, 1, Hkv, d] or [n, Hkv, d]) to every sequence, then attend over it too."""
+        [n, 1, Hkv, d] or [n, Hkv, d]) to every sequence, then attend over it too.
+        `after_other_layer`: the previous work on the stream is this call for
+        another layer (lets the launch overlap its start with that one's end)."""
         if out is None:
             out = torch.empty_like(q)
+        flags = AFTER_OTHER_LAYER if after_other_layer else 0
         _check(lib().ekv_append_decode_attn(self._h, layer, seq_slots.numel(), _ptr(seq_slots),
-                                            _ptr(k), _ptr(v), _ptr(q), _ptr(out),
+                                            _ptr(k), _ptr(v), _ptr(q), _ptr(out), flags,
                                             _stream(stream)), "ekv_append_decode_attn")
         return out
 

@@ -55,7 +55,10 @@ def decode_step(cache: ekv.Cache, w: workloads.Workload, slots: torch.Tensor, in
     for l in range(w.num_layers):
         q, k, v = inp.layer(l, i)
         if fused:
-            cache.append_decode_attn(l, slots, k, v, q, out[l])
+            # the previous launch is the fused step of layer l-1 unless this is
+            # the first layer or the canary ran after each layer
+            cache.append_decode_attn(l, slots, k, v, q, out[l],
+                                     after_other_layer=l > 0 and not fires)
         else:
             cache.append(l, slots, k, v)
             cache.decode_attn(l, slots, q, out[l])

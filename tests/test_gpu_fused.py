@@ -2,6 +2,8 @@
 (ekv_append, then ekv_decode_attn) on twin caches: identical lengths, block
 tables and page bytes after every step, outputs within the attention
 tolerance, through block seals (row 15), page pops (row 0) and a tier change."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -123,6 +125,10 @@ def test_fused_invalid_arguments_rejected_on_host():
         with pytest.raises(ekv.EkvError) as ei:
             cache.append_decode_attn(3, slots, good, good, q)
         assert ei.value.code == 1
+        lib = ekv.lib()
+        P = lambda t: ctypes.c_void_p(t.data_ptr())
+        assert lib.ekv_append_decode_attn(cache.handle, 0, 1, P(slots), P(good), P(good), P(q),
+                                          P(q), 2, None) == 1     # unknown flag bit
         cache.append_decode_attn(0, slots[:0], good[:0], good[:0], q[:0])   # no-op
         cache.sync()
         assert cache.seq_len(0, 0) == 0
