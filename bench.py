@@ -243,9 +243,30 @@ def main():
     out = torch.empty(L, B, w.num_q_heads, w.head_dim, dtype=torch.float16, device=dev)
     outs = [out[l] for l in range(L)]
 
+    # Several GPUs: each holds a shard of the batch; at a canary firing the ranks
+    # combine their readings (all-reduce) before the identical tier update.
+    combine, delta_buf = None, None
+    if world > 1:
+        import functools
+        nq = B * w.num_q_heads
+        delta_buf = torch.zeros(L, 3, dtype=torch.float32, device=dev)
+        combine = functools.partial(replicas.combine_readings, R, n_queries=nq,
+                                    total=replicas.total_queries(R, nq, dev))
+
+    def canary(l, q):
+        cache.canary_kl(l, slots, q, None if delta_buf is None else delta_buf[l])
+
+    def fire_end(freeze=False):
+        if combine is None:
+            cache.tier_update(freeze=freeze)
+        else:
+            combine(delta_buf)
+            cache.tier_update(delta_buf, freeze=freeze)
+
     # warm-up (eager)
     for i in range(W):
-        runner.decode_step(cache, w, slots, inp, i, outs, w.fires(i), fused=fused)
+        runner.decode_step(cache, w, slots, inp, i, outs, w.fires(i), delta_out=delta_buf,
+                           fused=fused, combine=combine)
     cache.sync()
 
     stream = torch.cuda.Stream(device=dev)
@@ -259,7 +280,8 @@ def main():
 
     # ---- A: K steps as one graph -------------------------------------------------
     gA = capture(lambda: [runner.decode_step(cache, w, slots, inp, i, outs, w.fires(i),
-                                             fused=fused) for i in range(W, W + K)])
+                                             delta_out=delta_buf, fused=fused, combine=combine)
+                          for i in range(W, W + K)])
     per_layer = 1 if fused else 2
     launches = sum(per_layer * L + ((L + 1) if w.fires(i) else 0) for i in range(W, W + K))
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -299,9 +321,9 @@ def main():
                 if external_ok:
                     pairs[n * L + l][1].record(stream)
                 if w.fires(i):
-                    cache.canary_kl(l, slots, q)
+                    canary(l, q)
             if w.fires(i):
-                cache.tier_update()
+                fire_end()
 
     gB = capture(steps_with_events)
     torch.cuda.synchronize()
@@ -320,8 +342,8 @@ def main():
 
     def firing():
         for l in range(L):
-            cache.canary_kl(l, slots, q_last[l])
-        cache.tier_update(freeze=True)
+            canary(l, q_last[l])
+        fire_end(freeze=True)
 
     gC = capture(firing)
     reps = 20
@@ -392,9 +414,9 @@ def main():
                         cache.append(l, slots, kd[l], vd[l])
                         cache.decode_attn(l, slots, qd[l], outs[l])
                     if w.fires(i):
-                        cache.canary_kl(l, slots, qd[l])
+                        canary(l, qd[l])
                 if w.fires(i):
-                    cache.tier_update()
+                    fire_end()
                 host_out[n].copy_(out, non_blocking=True)
 
         gE = capture(e2e_steps)

@@ -1,10 +1,15 @@
-"""Data-parallel replicas: one process per GPU, each with its own sequences.
+"""Data-parallel decode: one process per GPU, each with its own sequences.
 
-The decode path has no exchange step between sequences: every (layer,
-sequence, KV head) reads only its own pages.  N GPUs therefore run N
-independent replicas of the workload (weak scaling), each drawing its own
-sequences from a rank-offset seed, and the only collectives are the host-side
-barrier around each timed region and the max of the region's time over ranks.
+Attention and the append are independent per (sequence, KV head), so N GPUs
+hold N shards of the batch (weak scaling), each drawing its own sequences from
+a rank-offset seed.  The one exchange is the controller's: a layer's tier is
+shared by the whole batch ("EchoKV: watching a language model decide its own
+precision", "Show the math — what the canary actually computes": the KL is
+averaged over the step's queries), so at a canary firing the ranks add their
+per-layer readings weighted by their query counts (all-reduce of L*3 sums and
+one count) and every rank runs the identical tier update on the batch-wide
+mean.  The timing collectives are the barrier around each timed region and the
+max of its time over ranks.
 """
 from __future__ import annotations
 
@@ -50,3 +55,24 @@ def max_over_ranks(r: Ranks, seconds: float, device) -> float:
 def whole_job_rate(r: Ranks, units_per_rank: int, seconds_max: float) -> float:
     """Units all ranks processed per second of the slowest rank."""
     return r.world * units_per_rank / seconds_max
+
+
+def total_queries(r: Ranks, n_queries: int, device) -> int:
+    """Queries per step over all ranks (once, outside any captured region)."""
+    if r.world == 1:
+        return n_queries
+    n = torch.tensor([n_queries], dtype=torch.int64, device=device)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return int(n.item())
+
+
+def combine_readings(r: Ranks, delta, n_queries: int, total: int):
+    """Batch-wide canary readings from this rank's [L, 3] means over its
+    `n_queries` queries: sum over ranks of delta_r * n_r / total, in place (a
+    no-op alone).  Only a scale and one all-reduce, so it can be captured in a
+    CUDA graph."""
+    if r.world == 1:
+        return delta
+    delta.mul_(n_queries / total)
+    dist.all_reduce(delta, op=dist.ReduceOp.SUM)
+    return delta

@@ -49,9 +49,14 @@ def prefill(cache: ekv.Cache, w: workloads.Workload, slots: torch.Tensor, device
 
 def decode_step(cache: ekv.Cache, w: workloads.Workload, slots: torch.Tensor, inp: Inputs,
                 i: int, out: list, fires: bool, delta_out: torch.Tensor | None = None,
-                fused: bool = False):
+                fused: bool = False, combine=None):
     """One decode step over all layers; out[l] ([B,Hq,d]) receives each layer's O.
-    With `fused` each layer's append and attention run as one launch."""
+    With `fused` each layer's append and attention run as one launch.  With
+    `combine` (several GPUs, each holding a shard of the batch) the canary
+    readings, written to `delta_out` ([L, 3] fp32), are combined over the ranks
+    by combine(delta_out) before the tier update."""
+    if fires and combine is not None and delta_out is None:
+        raise ValueError("combining readings over ranks needs delta_out")
     for l in range(w.num_layers):
         q, k, v = inp.layer(l, i)
         if fused:
@@ -65,4 +70,8 @@ def decode_step(cache: ekv.Cache, w: workloads.Workload, slots: torch.Tensor, in
         if fires:
             cache.canary_kl(l, slots, q, None if delta_out is None else delta_out[l])
     if fires:
-        cache.tier_update()
+        if combine is not None:
+            combine(delta_out)
+            cache.tier_update(delta_out)
+        else:
+            cache.tier_update()

@@ -1,5 +1,6 @@
-"""The multi-GPU path: independent replicas, a barrier around each timed region
-and the slowest rank's time.  Run as two gloo ranks on CPU."""
+"""The multi-GPU path: a shard of the batch per rank, a barrier around each timed
+region, the slowest rank's time, and the one exchange -- the canary readings
+combined over the ranks before the tier update.  Run as two gloo ranks on CPU."""
 import os
 import socket
 
@@ -9,7 +10,8 @@ import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
 
-from mixed_precision_quantized_gb300 import replicas, workloads
+from mixed_precision_quantized_gb300 import replicas, synth, workloads
+from oracle import canary
 
 
 def _free_port() -> int:
@@ -66,3 +68,64 @@ def test_single_process_defaults(monkeypatch):
     assert replicas.whole_job_rate(R, 10, 2.0) == 5.0
     w = workloads.tiny()
     assert replicas.shard(w, 0) is w
+
+
+def _windows_and_q(B, Hq, Hkv, d, lens):
+    """Seeded canary inputs: per sequence a window [Hkv, n_s, d] and Q [B, Hq, d]."""
+    wins = [synth.draw16(21, 77, synth.T_K, 0, [s], [0], lens[s], Hkv, d)[0].numpy()
+            .transpose(1, 0, 2).copy() for s in range(B)]
+    q = synth.draw16(22, 77, synth.T_Q, 0, list(range(B)), [0] * B, 1, Hq, d)[:, 0].numpy()
+    return wins, q
+
+
+def _combine_main(rank: int, world: int, port: int, out) -> None:
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), WORLD_SIZE=str(world),
+                      RANK=str(rank), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        R = replicas.from_env()
+        B, Hq, Hkv, d = 5, 8, 2, 64
+        wins, q = _windows_and_q(B, Hq, Hkv, d, [9, 64, 33, 64, 17])
+        mine = [0, 1, 2] if rank == 0 else [3, 4]          # uneven shards
+        L = 2
+        delta = torch.zeros(L, 3, dtype=torch.float64)
+        for l in range(L):
+            delta[l] = torch.from_numpy(canary.layer_delta(q[mine] * (l + 1),
+                                                           [wins[s] for s in mine]))
+        nq = len(mine) * Hq
+        total = replicas.total_queries(R, nq, "cpu")
+        replicas.combine_readings(R, delta, nq, total)
+        out.put((rank, total, delta.numpy().copy()))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_canary_readings_combined_over_ranks():
+    """Two ranks holding 3 and 2 of 5 sequences: the combined readings equal the
+    oracle's readings over all 5 (mean over all queries), on both ranks."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    ps = [ctx.Process(target=_combine_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in ps:
+        p.start()
+    res = sorted((q.get(timeout=180) for _ in ps), key=lambda x: x[0])
+    for p in ps:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    B, Hq, Hkv, d = 5, 8, 2, 64
+    wins, qq = _windows_and_q(B, Hq, Hkv, d, [9, 64, 33, 64, 17])
+    want = np.stack([canary.layer_delta(qq * (l + 1), wins) for l in range(2)])
+    for rank, total, got in res:
+        assert total == B * Hq
+        assert np.allclose(got, want, rtol=1e-12, atol=1e-15), (rank, got, want)
+    assert np.array_equal(res[0][2], res[1][2])       # identical on every rank
+
+
+def test_combine_is_identity_alone(monkeypatch):
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    R = replicas.from_env()
+    x = torch.tensor([[0.1, 0.2, 0.3]], dtype=torch.float64)
+    assert replicas.total_queries(R, 40, "cpu") == 40
+    assert replicas.combine_readings(R, x, 40, 40) is x and x.tolist() == [[0.1, 0.2, 0.3]]
