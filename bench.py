@@ -63,6 +63,9 @@ def parse():
     p.add_argument("--layers", type=int, default=0,
                    help="run only the first N layers of the workload (profiling cases)")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    p.add_argument("--rotate", type=int, default=1,
+                   help="rotate steps over N caches of the workload, so that a workload whose "
+                        "pages fit in L2 is still read from HBM")
     p.add_argument("--separate", action="store_true",
                    help="append and attention as two launches per layer (default: one fused launch)")
     return p.parse_args()
@@ -232,12 +235,21 @@ def main():
     if n_steps_total > w.steps:
         raise SystemExit(f"workload holds {w.steps} decode steps; asked for {n_steps_total}")
 
-    cache = ekv.cache_for(w, device=dev)
+    NR = max(1, a.rotate)
+    if K % NR:
+        raise SystemExit("--steps must be a multiple of --rotate")
     slots = torch.arange(w.batch, dtype=torch.int32, device=dev)
+    caches = []
     t0 = time.perf_counter()
-    runner.prefill(cache, w, slots, device=dev)
-    cache.sync()
-    prefill_s = time.perf_counter() - t0
+    for _ in range(NR):
+        caches.append(ekv.cache_for(w, device=dev))
+        runner.prefill(caches[-1], w, slots, device=dev)
+        caches[-1].sync()
+    prefill_s = (time.perf_counter() - t0) / NR
+    cache = caches[0]
+
+    def C(i):  # the cache decode step i runs on
+        return caches[i % NR]
     inp = runner.Inputs(w, 0, W + 2 * K, device=dev)
     L, B = w.num_layers, w.batch
     out = torch.empty(L, B, w.num_q_heads, w.head_dim, dtype=torch.float16, device=dev)
@@ -253,21 +265,22 @@ def main():
         combine = functools.partial(replicas.combine_readings, R, n_queries=nq,
                                     total=replicas.total_queries(R, nq, dev))
 
-    def canary(l, q):
-        cache.canary_kl(l, slots, q, None if delta_buf is None else delta_buf[l])
+    def canary(c, l, q):
+        c.canary_kl(l, slots, q, None if delta_buf is None else delta_buf[l])
 
-    def fire_end(freeze=False):
+    def fire_end(c, freeze=False):
         if combine is None:
-            cache.tier_update(freeze=freeze)
+            c.tier_update(freeze=freeze)
         else:
             combine(delta_buf)
-            cache.tier_update(delta_buf, freeze=freeze)
+            c.tier_update(delta_buf, freeze=freeze)
 
     # warm-up (eager)
     for i in range(W):
-        runner.decode_step(cache, w, slots, inp, i, outs, w.fires(i), delta_out=delta_buf,
+        runner.decode_step(C(i), w, slots, inp, i, outs, w.fires(i), delta_out=delta_buf,
                            fused=fused, combine=combine)
-    cache.sync()
+    for c in caches:
+        c.sync()
 
     stream = torch.cuda.Stream(device=dev)
     stream.wait_stream(torch.cuda.current_stream())
@@ -279,7 +292,7 @@ def main():
         return g
 
     # ---- A: K steps as one graph -------------------------------------------------
-    gA = capture(lambda: [runner.decode_step(cache, w, slots, inp, i, outs, w.fires(i),
+    gA = capture(lambda: [runner.decode_step(C(i), w, slots, inp, i, outs, w.fires(i),
                                              delta_out=delta_buf, fused=fused, combine=combine)
                           for i in range(W, W + K)])
     per_layer = 1 if fused else 2
@@ -295,7 +308,8 @@ def main():
     torch.cuda.synchronize()
     replicas.barrier(R)
     tA = ev0.elapsed_time(ev1) / 1e3
-    cache.sync()
+    for c in caches:
+        c.sync()
     fired_A = sum(1 for i in range(W, W + K) if w.fires(i))
 
     # ---- B: next K steps, attention launches bracketed by timing events --------
@@ -308,29 +322,31 @@ def main():
 
     def steps_with_events():
         for n, i in enumerate(range(W + K, W + 2 * K)):
+            c = C(i)
             for l in range(L):
                 q, k, v = inp.layer(l, i)
                 if not fused:
-                    cache.append(l, slots, k, v)
+                    c.append(l, slots, k, v)
                 if external_ok:
                     pairs[n * L + l][0].record(stream)
                 if fused:
-                    cache.append_decode_attn(l, slots, k, v, q, outs[l])
+                    c.append_decode_attn(l, slots, k, v, q, outs[l])
                 else:
-                    cache.decode_attn(l, slots, q, outs[l])
+                    c.decode_attn(l, slots, q, outs[l])
                 if external_ok:
                     pairs[n * L + l][1].record(stream)
                 if w.fires(i):
-                    canary(l, q)
+                    canary(c, l, q)
             if w.fires(i):
-                fire_end()
+                fire_end(c)
 
     gB = capture(steps_with_events)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         gB.replay()
     torch.cuda.synchronize()
-    cache.sync()
+    for c in caches:
+        c.sync()
     attn_ms = [p[0].elapsed_time(p[1]) for p in pairs] if external_ok else []
     # algorithmic bytes per attention launch, at the state of region B's middle
     layer_bytes = [attn_bytes_per_layer(cache, w, l) for l in range(L)]
@@ -342,8 +358,8 @@ def main():
 
     def firing():
         for l in range(L):
-            canary(l, q_last[l])
-        fire_end(freeze=True)
+            canary(cache, l, q_last[l])
+        fire_end(cache, freeze=True)
 
     gC = capture(firing)
     reps = 20
@@ -367,8 +383,9 @@ def main():
 
     # ---- attention alone, all layers back to back (read-only, replayable) ------
     def attn_only():
-        for l in range(L):
-            cache.decode_attn(l, slots, q_last[l], outs[l])
+        for c in caches:
+            for l in range(L):
+                c.decode_attn(l, slots, q_last[l], outs[l])
 
     gD = capture(attn_only)
     with torch.cuda.stream(stream):
@@ -379,7 +396,7 @@ def main():
             gD.replay()
         d1.record(stream)
     torch.cuda.synchronize()
-    attn_only_us = d0.elapsed_time(d1) * 1e3 / (5 * L)
+    attn_only_us = d0.elapsed_time(d1) * 1e3 / (5 * L * NR)
     if attn_avg_s is None:
         attn_avg_s = attn_only_us * 1e-6
 
@@ -405,18 +422,19 @@ def main():
         def e2e_steps():
             for n in range(K):
                 i = s0 + n
+                c = C(i)
                 dbuf.copy_(host_in[n], non_blocking=True)
                 for l in range(L):
                     if fused:
-                        cache.append_decode_attn(l, slots, kd[l], vd[l], qd[l], outs[l],
-                                                 after_other_layer=l > 0 and not w.fires(i))
+                        c.append_decode_attn(l, slots, kd[l], vd[l], qd[l], outs[l],
+                                             after_other_layer=l > 0 and not w.fires(i))
                     else:
-                        cache.append(l, slots, kd[l], vd[l])
-                        cache.decode_attn(l, slots, qd[l], outs[l])
+                        c.append(l, slots, kd[l], vd[l])
+                        c.decode_attn(l, slots, qd[l], outs[l])
                     if w.fires(i):
-                        canary(l, qd[l])
+                        canary(c, l, qd[l])
                 if w.fires(i):
-                    fire_end()
+                    fire_end(c)
                 host_out[n].copy_(out, non_blocking=True)
 
         gE = capture(e2e_steps)
@@ -430,7 +448,8 @@ def main():
         torch.cuda.synchronize()
         replicas.barrier(R)
         tE = e0.elapsed_time(e1) / 1e3
-        cache.sync()
+        for c in caches:
+            c.sync()
         tE = replicas.max_over_ranks(R, tE, dev)
         e2e = {"value": replicas.whole_job_rate(R, B * K, tE), "unit": "tokens/s",
                "h2d_bytes_per_step": int(host_in.shape[1] * 2),
@@ -460,7 +479,10 @@ def main():
                                f"{w.prefill[0] if len(set(w.prefill)) == 1 else 'ragged'} cached "
                                f"tokens, K tier by canary every {w.canary_period} steps "
                                f"(tau {w.tau}), V INT{w.v_bits[0]}",
-                   "l2": f"inputs larger than L2: {step_bytes / 1e9:.2f} GB of pages read per step",
+                   "l2": (f"inputs larger than L2: {step_bytes / 1e9:.2f} GB of pages read per step"
+                          if NR == 1 else
+                          f"steps rotate over {NR} caches of {step_bytes / 1e9:.3f} GB of pages "
+                          f"each ({NR * step_bytes / 1e6:.0f} MB > L2)"),
                    "parallelism": f"replicas x{world} (one sequence set per GPU)",
                    "graph": "CUDA graph of the timed steps", "canary_fires_in_timed": fired_A,
                    "step": ("one fused append + attention launch per layer" if fused
@@ -497,7 +519,8 @@ def main():
             line["cpu_baseline"] = cpu_baseline(w, a.cpu_sample_layers, dev)
         except Exception as ex:  # noqa: BLE001
             line["cpu_baseline"] = {"value": None, "error": repr(ex)}
-    cache.close()
+    for c in caches:
+        c.close()
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

@@ -39,6 +39,7 @@ namespace ekv {
 namespace {
 
 constexpr int NSMAX = 8;  // stages per warp at most
+constexpr int ATTN_LATE_BLOCKS = 80;  // ~6 us of a CTA's page work
 // One CTA per SM.  Its warps share the split's pages through a counter in shared
 // memory, so a warp that runs ahead takes more pages.  Stage memory: 200 KB,
 // split evenly between the warps (quantized V: 16 warps, five K4/V4 pages each,
@@ -778,13 +779,13 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   }
   const int T = told + (app ? 1 : 0);
   const int nb = (T + BLOCK - 1) / BLOCK;
-  // Contiguous block ranges, the last split's 1/8 short of an even share: when
-  // this launch overlaps the end of the one before (programmatic dependent), the
-  // last split's CTAs are the ones that get an SM last, after that launch's
-  // final merges.
+  // Contiguous block ranges, the last split's ATTN_LATE_BLOCKS short of an even
+  // share: when this launch overlaps the end of the one before (programmatic
+  // dependent), the last split's CTAs are the ones that get an SM last, a few
+  // microseconds (that launch's final merges) after the others.
   int b0 = 0, b1 = nb;
   if (splits > 1) {
-    const int rest = nb - nb * 7 / (8 * splits);
+    const int rest = nb - max(0, nb / splits - ATTN_LATE_BLOCKS);
     const int cb = (rest + splits - 2) / (splits - 1);
     b0 = split < splits - 1 ? min(rest, split * cb) : rest;
     b1 = split < splits - 1 ? min(rest, b0 + cb) : nb;
