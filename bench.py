@@ -66,6 +66,8 @@ def parse():
     p.add_argument("--rotate", type=int, default=1,
                    help="rotate steps over N caches of the workload, so that a workload whose "
                         "pages fit in L2 is still read from HBM")
+    p.add_argument("--no-overlap-check", action="store_true",
+                   help="skip timing the fused step without the overlap of consecutive layers")
     p.add_argument("--separate", action="store_true",
                    help="append and attention as two launches per layer (default: one fused launch)")
     return p.parse_args()
@@ -231,7 +233,7 @@ def main():
     fused = not a.separate
     if W < 3:
         raise SystemExit("at least 3 warm-up steps")
-    n_steps_total = W + (3 if not a.no_e2e else 2) * K
+    n_steps_total = W + (3 if not a.no_e2e else 2) * K + (K if not a.no_overlap_check else 0)
     if n_steps_total > w.steps:
         raise SystemExit(f"workload holds {w.steps} decode steps; asked for {n_steps_total}")
 
@@ -311,6 +313,30 @@ def main():
     for c in caches:
         c.sync()
     fired_A = sum(1 for i in range(W, W + K) if w.fires(i))
+
+    # ---- A': the same steps without the overlap of consecutive layers ------------
+    # (what a model whose layer inputs come from the previous layer's output gets)
+    tA2 = None
+    if fused and not a.no_overlap_check:
+        s2 = W + 2 * K + (0 if a.no_e2e else K)
+        inpA2 = runner.Inputs(w, s2, K, device=dev)
+        gA2 = capture(lambda: [runner.decode_step(C(i), w, slots, inpA2, i - s2, outs,
+                                                  w.fires(i), delta_out=delta_buf, fused=True,
+                                                  combine=combine, overlap=False)
+                               for i in range(s2, s2 + K)])
+        torch.cuda.synchronize()
+        replicas.barrier(R)
+        with torch.cuda.stream(stream):
+            f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            f0.record(stream)
+            gA2.replay()
+            f1.record(stream)
+        torch.cuda.synchronize()
+        replicas.barrier(R)
+        tA2 = replicas.max_over_ranks(R, f0.elapsed_time(f1) / 1e3, dev)
+        for c in caches:
+            c.sync()
+        del gA2, inpA2
 
     # ---- B: next K steps, attention launches bracketed by timing events --------
     try:
@@ -511,6 +537,10 @@ def main():
                                else "attention-only graph (all layers back to back)",
                      "attn_only_avg_us": attn_only_us},
         "e2e": e2e,
+        "no_overlap": (None if tA2 is None else
+                       {"value": replicas.whole_job_rate(R, B * K, tA2), "unit": "tokens/s",
+                        "note": "same steps, each layer's launch waiting for the previous "
+                                "one (inputs that depend on the previous layer's output)"}),
         "gpu_launches": launches,
         "clocks": clk.summary(),
     }

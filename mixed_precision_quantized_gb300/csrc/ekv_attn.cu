@@ -39,7 +39,9 @@ namespace ekv {
 namespace {
 
 constexpr int NSMAX = 8;  // stages per warp at most
-constexpr int ATTN_LATE_BLOCKS = 80;  // ~6 us of a CTA's page work
+// Blocks the last split of an overlapped launch takes less (~6 us of a CTA's
+// page work: how much later its CTAs get an SM).
+constexpr int ATTN_LATE_BLOCKS = 80;
 // One CTA per SM.  Its warps share the split's pages through a counter in shared
 // memory, so a warp that runs ahead takes more pages.  Stage memory: 200 KB,
 // split evenly between the warps (quantized V: 16 warps, five K4/V4 pages each,
@@ -744,7 +746,8 @@ template <int D, int VB, bool FUSED>
 __global__ void __launch_bounds__(AttnCfg<VB>::NT, 1)
 decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
                    const __half* __restrict__ q, __half* __restrict__ o, int splits,
-                   const __half* __restrict__ knew, const __half* __restrict__ vnew) {
+                   const __half* __restrict__ knew, const __half* __restrict__ vnew,
+                   int late_blocks) {
   constexpr int NW = AttnCfg<VB>::NW, NT = AttnCfg<VB>::NT;
   constexpr int KCH = D / 4, KW = KCH / 2, VCH = D / 8, NMT = D / 16;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -779,13 +782,13 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   }
   const int T = told + (app ? 1 : 0);
   const int nb = (T + BLOCK - 1) / BLOCK;
-  // Contiguous block ranges, the last split's ATTN_LATE_BLOCKS short of an even
+  // Contiguous block ranges, the last split's `late_blocks` short of an even
   // share: when this launch overlaps the end of the one before (programmatic
   // dependent), the last split's CTAs are the ones that get an SM last, a few
   // microseconds (that launch's final merges) after the others.
   int b0 = 0, b1 = nb;
   if (splits > 1) {
-    const int rest = nb - max(0, nb / splits - ATTN_LATE_BLOCKS);
+    const int rest = nb - max(0, nb / splits - late_blocks);
     const int cb = (rest + splits - 2) / (splits - 1);
     b0 = split < splits - 1 ? min(rest, split * cb) : rest;
     b1 = split < splits - 1 ? min(rest, b0 + cb) : nb;
@@ -1101,14 +1104,14 @@ cudaError_t launch_t(const DevState& st, int layer, int n_seqs, const int32_t* s
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, decode_attn_kernel<D, VB, true>, st, layer, slots, q, o,
-                              splits, knew, vnew);
+                              splits, knew, vnew, ATTN_LATE_BLOCKS);
   }
   if (knew)
     decode_attn_kernel<D, VB, true><<<grid, AttnCfg<VB>::NT, AttnCfg<VB>::SMEM, s>>>(
-        st, layer, slots, q, o, splits, knew, vnew);
+        st, layer, slots, q, o, splits, knew, vnew, 0);
   else
     decode_attn_kernel<D, VB, false><<<grid, AttnCfg<VB>::NT, AttnCfg<VB>::SMEM, s>>>(
-        st, layer, slots, q, o, splits, nullptr, nullptr);
+        st, layer, slots, q, o, splits, nullptr, nullptr, 0);
   return cudaGetLastError();
 }
 

@@ -42,9 +42,11 @@ void free_all(ekv_cache* c) {
 }
 
 int attn_splits(const ekv_cache* c, int n_seqs, int vb) {
+  // As many splits as fit in one wave of CTAs (a partial second wave would cost
+  // a whole launch's start-up and tail again).
   const int units = n_seqs * c->st.Hkv;
   const int target = attn_ctas_per_sm(vb) * c->num_sm;
-  int s = (target + units - 1) / units;
+  int s = target / units;
   if (s < 1) s = 1;
   // A split's page-table entries must fit the kernel's shared-memory copy (the
   // splits but the last share the blocks, hence the one extra).

@@ -49,9 +49,11 @@ def prefill(cache: ekv.Cache, w: workloads.Workload, slots: torch.Tensor, device
 
 def decode_step(cache: ekv.Cache, w: workloads.Workload, slots: torch.Tensor, inp: Inputs,
                 i: int, out: list, fires: bool, delta_out: torch.Tensor | None = None,
-                fused: bool = False, combine=None):
+                fused: bool = False, combine=None, overlap: bool = True):
     """One decode step over all layers; out[l] ([B,Hq,d]) receives each layer's O.
-    With `fused` each layer's append and attention run as one launch.  With
+    With `fused` each layer's append and attention run as one launch, each but the
+    first overlapping the previous layer's (`overlap`; valid here because a
+    layer's inputs do not come from the previous layer's output).  With
     `combine` (several GPUs, each holding a shard of the batch) the canary
     readings, written to `delta_out` ([L, 3] fp32), are combined over the ranks
     by combine(delta_out) before the tier update."""
@@ -63,7 +65,7 @@ def decode_step(cache: ekv.Cache, w: workloads.Workload, slots: torch.Tensor, in
             # the previous launch is the fused step of layer l-1 unless this is
             # the first layer or the canary ran after each layer
             cache.append_decode_attn(l, slots, k, v, q, out[l],
-                                     after_other_layer=l > 0 and not fires)
+                                     after_other_layer=overlap and l > 0 and not fires)
         else:
             cache.append(l, slots, k, v)
             cache.decode_attn(l, slots, q, out[l])
