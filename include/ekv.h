@@ -85,6 +85,15 @@ typedef struct ekv_config {
   float softmax_scale;     /* 0 -> 1/sqrt(head_dim)                                    */
   float ema_alpha;         /* EMA weight of a new canary reading                        */
   float tau;               /* divergence budget of the tier pick                        */
+  /* Controller variants ("EchoKV: watching a language model decide its own
+   * precision": "The tau(L) scaling", and the hysteresis / multi-firing vote it
+   * proposes against drift).  Zero turns each off. */
+  int32_t tau_ctx0;        /* > 0: budget tau * sqrt(L / tau_ctx0), L = mean cached
+                              length of the layer's sequences with tokens          */
+  float hysteresis;        /* in [0, 1): picking fewer bits than the current tier
+                              needs ema_b < budget * (1 - hysteresis)                */
+  int32_t vote;            /* >= 2: a tier changes only after that many consecutive
+                              firings picked the same new tier                      */
   /* Device allocator.  NULL -> cudaMalloc/cudaFree.  Called only inside
    * ekv_create/ekv_destroy. */
   void* (*dev_alloc)(size_t bytes, void* ctx);
@@ -211,7 +220,13 @@ EKV_API int ekv_canary_kl(ekv_cache* cache, int32_t layer, int32_t n_seqs, const
 /* Controller update for every layer whose layer_mask entry is nonzero
  * (layer_mask dev uint8[num_layers], NULL = all layers):
  *   ema = first reading ? delta : (1-alpha)*ema + alpha*delta   (fp32, unfused)
- *   tier = min{ b in {2,4,8} : ema_b < tau }, else 8.
+ *   budget = tau, or with tau_ctx0 > 0 and sequences holding tokens:
+ *            tau * sqrt(L / tau_ctx0), L = sum of their lengths / their count
+ *            (fp32: one rounding per division, square root and product)
+ *   pick = min{ b in {2,4,8} : ema_b < (b < tier ? budget*(1-hysteresis) : budget) },
+ *          else 8
+ *   tier = pick once `vote` consecutive firings picked it (vote <= 1: at once);
+ *          a firing that picks the current tier resets the count.
  * delta (dev float[num_layers][3]) NULL = the readings stored by ekv_canary_kl.
  * freeze != 0 leaves every EMA and tier unchanged.  A new tier governs pages
  * allocated by later appends only. */

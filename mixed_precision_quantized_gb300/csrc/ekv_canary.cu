@@ -177,20 +177,52 @@ __global__ void tier_update_kernel(DevState st, const float* __restrict__ delta,
     float* e = st.ema + l * NBITS;
     const bool first = st.ema_valid[l] == 0;
     const float one_minus = __fsub_rn(1.0f, st.alpha);
-    int tier = 8;
+    // Budget: tau, or tau * sqrt(L / L0) with L the mean length of the layer's
+    // sequences that hold tokens ("The tau(L) scaling").
+    float budget = st.tau;
+    if (st.tau_ctx0 > 0) {
+      long long sum = 0;
+      int n = 0;
+      for (int s = 0; s < st.S; ++s) {
+        const int t = st.len[ls_index(st, l, s)];
+        if (t > 0) {
+          sum += t;
+          ++n;
+        }
+      }
+      if (n > 0) {
+        const float mean = __fdiv_rn((float)sum, (float)n);
+        budget = __fmul_rn(st.tau, __fsqrt_rn(__fdiv_rn(mean, (float)st.tau_ctx0)));
+      }
+    }
+    // Fewer bits than the current tier must clear the budget by the hysteresis.
+    const int cur = st.tier[l];
+    const float lower = __fmul_rn(budget, __fsub_rn(1.0f, st.hyst));
+    int pick = 8;
     bool picked = false;
 #pragma unroll
     for (int bi = 0; bi < NBITS; ++bi) {
       const float v = first ? d[bi]
                             : __fadd_rn(__fmul_rn(one_minus, e[bi]), __fmul_rn(st.alpha, d[bi]));
       e[bi] = v;
-      if (!picked && v < st.tau) {
-        tier = 2 << bi;
+      if (!picked && v < ((2 << bi) < cur ? lower : budget)) {
+        pick = 2 << bi;
         picked = true;
       }
     }
     st.ema_valid[l] = 1;
-    st.tier[l] = tier;
+    // A new tier needs `vote` consecutive firings that pick it.
+    if (pick == cur) {
+      st.cnt[l] = 0;
+    } else {
+      int n = st.cand[l] == pick ? st.cnt[l] + 1 : 1;
+      if (n >= st.vote) {
+        st.tier[l] = pick;
+        n = 0;
+      }
+      st.cand[l] = pick;
+      st.cnt[l] = n;
+    }
   }
 }
 

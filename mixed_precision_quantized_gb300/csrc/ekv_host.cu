@@ -107,6 +107,8 @@ int ekv_create(const ekv_config* cfg, const uint8_t* k_bits_init, const uint8_t*
   if (k.num_q_heads / k.num_kv_heads > MAX_G) return EKV_EUNSUPPORTED;
   if ((k.dev_alloc == nullptr) != (k.dev_free == nullptr)) return EKV_EINVAL;
   if (!(k.ema_alpha >= 0.f && k.ema_alpha <= 1.f)) return EKV_EINVAL;
+  if (k.tau_ctx0 < 0 || !(k.hysteresis >= 0.f && k.hysteresis < 1.f) || k.vote < 0)
+    return EKV_EINVAL;
   for (int l = 0; l < k.num_layers; ++l)
     if (!valid_bits(k_bits_init[l]) || !valid_bits(v_bits[l])) return EKV_EINVAL;
   for (int f = 0; f < NFMT; ++f)
@@ -128,6 +130,9 @@ int ekv_create(const ekv_config* cfg, const uint8_t* k_bits_init, const uint8_t*
   st.scale_log2 = st.scale * 1.4426950408889634f;
   st.alpha = k.ema_alpha;
   st.tau = k.tau;
+  st.tau_ctx0 = k.tau_ctx0;
+  st.hyst = k.hysteresis;
+  st.vote = k.vote < 1 ? 1 : k.vote;
   c->vbits.assign(v_bits, v_bits + k.num_layers);
 
   int dev = 0;
@@ -164,6 +169,8 @@ int ekv_create(const ekv_config* cfg, const uint8_t* k_bits_init, const uint8_t*
   st.vbits = (int32_t*)A(L * 4);
   st.ema = (float*)A(L * 3 * 4);
   st.ema_valid = (int32_t*)A(L * 4);
+  st.cand = (int32_t*)A(L * 4);
+  st.cnt = (int32_t*)A(L * 4);
   st.delta = (float*)A(L * 3 * 4);
   st.err = (int32_t*)A(4);
   st.append_ticket = (int32_t*)A(L * S * 4);
@@ -210,6 +217,8 @@ int ekv_create(const ekv_config* cfg, const uint8_t* k_bits_init, const uint8_t*
   Z(st.ring, L * S * H * RING * D * 2);
   Z(st.ema, L * 3 * 4);
   Z(st.ema_valid, L * 4);
+  Z(st.cand, L * 4);
+  Z(st.cnt, L * 4);
   Z(st.delta, L * 3 * 4);
   Z(st.err, 4);
   Z(st.append_ticket, L * S * 4);
@@ -396,14 +405,14 @@ int ekv_sync(ekv_cache* c, void* stream) {
 
 int64_t ekv_state_size(ekv_cache* c) {
   if (!c) return -1;
-  return 8 + (int64_t)c->st.L * (4 + 12 + 4 + 12);
+  return 8 + (int64_t)c->st.L * (4 + 12 + 4 + 12 + 4 + 4);
 }
 
 int ekv_state_save(ekv_cache* c, void* blob, int64_t bytes, void* stream) {
   if (!c || !blob || bytes < ekv_state_size(c)) return EKV_EINVAL;
   const int L = c->st.L;
   uint8_t* p = static_cast<uint8_t*>(blob);
-  const uint32_t magic = 0x454B5631u, nl = (uint32_t)L;
+  const uint32_t magic = 0x454B5632u, nl = (uint32_t)L;
   memcpy(p, &magic, 4);
   memcpy(p + 4, &nl, 4);
   cudaStream_t s = as_stream(stream);
@@ -411,6 +420,8 @@ int ekv_state_save(ekv_cache* c, void* blob, int64_t bytes, void* stream) {
   if (e == cudaSuccess) e = cudaMemcpyAsync(p + 8 + L * 4, c->st.ema, L * 12, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(p + 8 + L * 16, c->st.ema_valid, L * 4, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(p + 8 + L * 20, c->st.delta, L * 12, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(p + 8 + L * 32, c->st.cand, L * 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(p + 8 + L * 36, c->st.cnt, L * 4, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   return cuda_status(e);
 }
@@ -422,7 +433,7 @@ int ekv_state_load(ekv_cache* c, const void* blob, int64_t bytes, void* stream) 
   uint32_t magic = 0, nl = 0;
   memcpy(&magic, p, 4);
   memcpy(&nl, p + 4, 4);
-  if (magic != 0x454B5631u || nl != (uint32_t)L) return EKV_EINVAL;
+  if (magic != 0x454B5632u || nl != (uint32_t)L) return EKV_EINVAL;
   for (int l = 0; l < L; ++l) {
     int32_t t;
     memcpy(&t, p + 8 + 4 * l, 4);
@@ -433,6 +444,8 @@ int ekv_state_load(ekv_cache* c, const void* blob, int64_t bytes, void* stream) 
   if (e == cudaSuccess) e = cudaMemcpyAsync(c->st.ema, p + 8 + L * 4, L * 12, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(c->st.ema_valid, p + 8 + L * 16, L * 4, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(c->st.delta, p + 8 + L * 20, L * 12, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(c->st.cand, p + 8 + L * 32, L * 4, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(c->st.cnt, p + 8 + L * 36, L * 4, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   return cuda_status(e);
 }

@@ -44,6 +44,9 @@ struct DevState {
   float scale;       // softmax scale sigma
   float scale_log2;  // sigma * log2(e)
   float alpha, tau;
+  int tau_ctx0;      // > 0: budget scales with sqrt(mean length / tau_ctx0)
+  float hyst;        // demotion margin
+  int vote;          // consecutive firings a new tier needs (>= 1)
   uint8_t* pool_base[NFMT];
   int32_t pool_page_bytes[NFMT];
   int32_t pool_cap[NFMT];
@@ -58,6 +61,8 @@ struct DevState {
   int32_t* vbits;           // [L]
   float* ema;               // [L][3]
   int32_t* ema_valid;       // [L]
+  int32_t* cand;            // [L] tier the last firings picked (vote)
+  int32_t* cnt;             // [L] consecutive firings that picked `cand`
   float* delta;             // [L][3] last canary readings
   int32_t* err;             // device error word
   int32_t* append_ticket;   // [L][S]

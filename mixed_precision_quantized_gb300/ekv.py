@@ -36,6 +36,9 @@ class EkvConfig(ctypes.Structure):
         ("softmax_scale", ctypes.c_float),
         ("ema_alpha", ctypes.c_float),
         ("tau", ctypes.c_float),
+        ("tau_ctx0", ctypes.c_int32),
+        ("hysteresis", ctypes.c_float),
+        ("vote", ctypes.c_int32),
         ("dev_alloc", ctypes.c_void_p),
         ("dev_free", ctypes.c_void_p),
         ("alloc_ctx", ctypes.c_void_p),
@@ -122,7 +125,8 @@ class Cache:
     def __init__(self, num_layers: int, max_seqs: int, num_q_heads: int, num_kv_heads: int,
                  head_dim: int, max_seq_len: int, pool_pages: dict, k_bits_init, v_bits,
                  alpha: float = 0.25, tau: float = 0.05, softmax_scale: float = 0.0,
-                 device=None, torch_alloc: bool = True):
+                 device=None, torch_alloc: bool = True, tau_ctx0: int = 0,
+                 hysteresis: float = 0.0, vote: int = 1):
         L = lib()
         self.device = torch.device("cuda" if device is None else device)
         self.num_layers, self.max_seqs = num_layers, max_seqs
@@ -135,6 +139,7 @@ class Cache:
         for (kb, vb), n in pool_pages.items():
             cfg.pool_pages[fmt_index(kb, vb)] = int(n)
         cfg.softmax_scale, cfg.ema_alpha, cfg.tau = softmax_scale, alpha, tau
+        cfg.tau_ctx0, cfg.hysteresis, cfg.vote = int(tau_ctx0), float(hysteresis), int(vote)
         self._keep = []
         if torch_alloc:
             dev = self.device.index if self.device.index is not None else torch.cuda.current_device()

@@ -134,6 +134,51 @@ def test_tier_update_bit_exact_with_injected_readings():
         cache.close()
 
 
+def test_tier_update_variants_bit_exact():
+    """tau(L) with the layers' lengths, hysteresis and a 2-firing vote, against the
+    oracle controller given the same lengths and readings."""
+    w = workloads.Workload("ctlv", 13, 6, 2, 4, 2, 64, [16, 16], 1, [4] * 6, [4] * 6,
+                           alpha=0.5, tau=0.05)
+    pools = {(4, 4): 128}
+    cache = ekv.Cache(6, 2, 4, 2, 64, 256, pools, w.k_bits_init, w.v_bits,
+                      alpha=0.5, tau=0.05, tau_ctx0=48, hysteresis=0.25, vote=2)
+    try:
+        slots = torch.arange(2, dtype=torch.int32, device="cuda")
+        lengths = []
+        for l in range(6):   # layer l: slot 0 holds 16 + 8l tokens, slot 1 none or 40
+            n0 = 16 + 8 * l
+            k, v = w.prefill_kv(0, [0], device="cuda", n_tok=n0)
+            cache.append(l, slots[:1], k, v)
+            if l % 2:
+                k, v = w.prefill_kv(0, [1], device="cuda", n_tok=40)
+                cache.append(l, slots[1:], k, v)
+            lengths.append([n0, 40 if l % 2 else 0])
+        cache.sync()
+        ctl = controller.Controller(w.k_bits_init, w.alpha, w.tau, tau_ctx0=48, hysteresis=0.25,
+                                    vote=2)
+        rng = np.random.default_rng(1)
+        for it in range(16):
+            d = rng.exponential(0.03, size=(6, 3)).astype(np.float32)
+            d[:, 0] *= 3
+            cache.tier_update(torch.from_numpy(d).cuda())
+            ctl.update(d, lengths=lengths)
+            st = cache.state()
+            assert st["tiers"] == ctl.tiers, (it, st["tiers"], ctl.tiers)
+            ema_gpu = np.array(st["ema"], dtype=np.float32)
+            for l in range(6):
+                assert np.array_equal(ema_gpu[l], ctl.ema[l])
+        blob = cache.save_state()                         # the vote state travels too
+        c2 = ekv.Cache(6, 2, 4, 2, 64, 256, pools, w.k_bits_init, w.v_bits,
+                       alpha=0.5, tau=0.05, tau_ctx0=48, hysteresis=0.25, vote=2)
+        try:
+            c2.load_state(blob)
+            assert c2.save_state() == blob
+        finally:
+            c2.close()
+    finally:
+        cache.close()
+
+
 def test_state_save_load_round_trip():
     w = workloads.tiny()
     cache = ekv.cache_for(w)

@@ -174,3 +174,59 @@ def test_promote_then_demote():
     assert c.tiers == [2]                  # demote
     c.update([[0.9, 0.9, 0.9]], freeze=True)
     assert c.tiers == [2]                  # frozen
+
+
+# ---- controller variants: tau(L), hysteresis, multi-firing vote -------------------
+
+
+def test_budget_at_128k_matches_the_printed_value():
+    import json, os
+    from conftest import GOLDEN
+    g = json.load(open(os.path.join(GOLDEN, "paper_numbers.json")))["tau_128k"]
+    p = g["params"]
+    b = float(controller.budget(p["tau0"], p["ctx0"], [p["ctx"]]))
+    assert abs(b - g["value"]) <= g["tol_abs"]
+
+
+def test_budget_exact_cases():
+    t = np.float32(0.05)
+    assert controller.budget(0.05, 0, [131072]) == t                 # off
+    assert controller.budget(0.05, 4096, []) == t                    # no sequence has tokens
+    assert controller.budget(0.05, 4096, [0, 0]) == t
+    assert controller.budget(0.05, 4096, [4096]) == t                # sqrt(1)
+    assert controller.budget(0.05, 4096, [16384]) == np.float32(2) * t  # sqrt(4), exact
+    assert controller.budget(0.05, 4096, [1024]) == t / np.float32(2)   # sqrt(1/4), exact
+    # mean over the sequences holding tokens only: (8192 + 24576) / 2 = 16384
+    assert controller.budget(0.05, 4096, [8192, 0, 24576]) == np.float32(2) * t
+
+
+def test_hysteresis_needs_margin_to_demote_not_to_promote():
+    # tau 0.05, h 0.2 -> fewer bits than the current tier need ema < 0.04
+    c = controller.Controller([8], alpha=1.0, tau=0.05, hysteresis=0.2)
+    c.update([[0.2, 0.045, 0.001]])
+    assert c.tiers == [8]                       # 0.045 is under tau but not under 0.04
+    c.update([[0.2, 0.035, 0.001]])
+    assert c.tiers == [4]                       # clears the margin
+    c.update([[0.2, 0.06, 0.001]])
+    assert c.tiers == [8]                       # promotion at plain tau, at once
+    plain = controller.Controller([8], alpha=1.0, tau=0.05)
+    plain.update([[0.2, 0.045, 0.001]])
+    assert plain.tiers == [4]                   # without hysteresis the same reading demotes
+
+
+def test_vote_needs_consecutive_firings():
+    c = controller.Controller([4], alpha=1.0, tau=0.05, vote=2)
+    to8, to4, to2 = [0.3, 0.2, 0.001], [0.3, 0.01, 0.001], [0.01, 0.01, 0.001]
+    c.update([to8])
+    assert c.tiers == [4]                       # one firing for 8
+    c.update([to4])
+    assert c.tiers == [4]                       # a firing for the current tier resets
+    c.update([to8])
+    assert c.tiers == [4]
+    c.update([to8])
+    assert c.tiers == [8]                       # two in a row
+    c.update([to2])
+    c.update([to4])
+    assert c.tiers == [8]                       # 2 then 4: different candidates
+    c.update([to4])
+    assert c.tiers == [4]
