@@ -76,3 +76,33 @@ def combine_readings(r: Ranks, delta, n_queries: int, total: int):
     delta.mul_(n_queries / total)
     dist.all_reduce(delta, op=dist.ReduceOp.SUM)
     return delta
+
+
+def majority_tiers(vectors) -> list:
+    """Per-layer majority of several ranks' tier vectors; a tie goes to the
+    widest of the tied tiers (more bits: the conservative choice)."""
+    vectors = [list(v) for v in vectors]
+    out = []
+    for l in range(len(vectors[0])):
+        votes: dict = {}
+        for v in vectors:
+            votes[int(v[l])] = votes.get(int(v[l]), 0) + 1
+        top = max(votes.values())
+        out.append(max(b for b, n in votes.items() if n == top))
+    return out
+
+
+def consolidate_tiers(r: Ranks, cache, device="cpu") -> list:
+    """The pages' consolidation before a freeze ("EchoKV: watching a language
+    model decide its own precision", "Measurement protocol", phase 2): every
+    rank's per-layer tiers are gathered, each layer takes the ranks' majority,
+    and every rank sets that vector.  Returns it (this rank's own alone)."""
+    mine = [int(t) for t in cache.state()["tiers"]]
+    if r.world == 1:
+        return mine
+    t = torch.tensor(mine, dtype=torch.int32, device=device)
+    got = [torch.zeros_like(t) for _ in range(r.world)]
+    dist.all_gather(got, t)
+    voted = majority_tiers([g.cpu().tolist() for g in got])
+    cache.set_tiers(voted)
+    return voted

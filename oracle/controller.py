@@ -102,3 +102,20 @@ class Controller:
                 n = 0
             self.cand[l] = new
             self.count[l] = n
+
+
+def majority_vote(tier_vectors):
+    """Consolidation across ranks before the freeze ("Measurement protocol",
+    phase 2: "majority vote per layer").  Reading: the most frequent tier of
+    each layer; among tied tiers, the widest."""
+    L = len(tier_vectors[0])
+    result = []
+    for l in range(L):
+        column = [int(v[l]) for v in tier_vectors]
+        best, best_n = None, -1
+        for b in sorted(set(column), reverse=True):     # widest first: wins ties
+            n = column.count(b)
+            if n > best_n:
+                best, best_n = b, n
+        result.append(best)
+    return result

@@ -129,3 +129,64 @@ def test_combine_is_identity_alone(monkeypatch):
     x = torch.tensor([[0.1, 0.2, 0.3]], dtype=torch.float64)
     assert replicas.total_queries(R, 40, "cpu") == 40
     assert replicas.combine_readings(R, x, 40, 40) is x and x.tolist() == [[0.1, 0.2, 0.3]]
+
+
+# ---- consolidation of per-rank tiers before a freeze (majority vote) ---------------
+
+
+class _FakeCache:
+    """Stands in for a GPU cache: holds a tier vector."""
+
+    def __init__(self, tiers):
+        self.tiers = list(tiers)
+
+    def state(self):
+        return {"tiers": list(self.tiers)}
+
+    def set_tiers(self, tiers):
+        self.tiers = list(tiers)
+
+
+_RANK_TIERS = [[4, 8, 2, 4, 8], [4, 2, 2, 8, 8], [8, 2, 4, 2, 4]]
+
+
+def _vote_main(rank: int, world: int, port: int, out) -> None:
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), WORLD_SIZE=str(world),
+                      RANK=str(rank), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        c = _FakeCache(_RANK_TIERS[rank])
+        voted = replicas.consolidate_tiers(replicas.from_env(), c)
+        out.put((rank, voted, c.tiers))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_tiers_consolidated_by_majority_on_three_ranks():
+    from oracle import controller
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    ps = [ctx.Process(target=_vote_main, args=(r, 3, port, q)) for r in range(3)]
+    for p in ps:
+        p.start()
+    res = sorted((q.get(timeout=180) for _ in ps), key=lambda x: x[0])
+    for p in ps:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    want = controller.majority_vote(_RANK_TIERS)
+    # layer by layer: 4,4,8 -> 4; 8,2,2 -> 2; 2,2,4 -> 2; 4,8,2 -> tie -> 8; 8,8,4 -> 8
+    assert want == [4, 2, 2, 8, 8]
+    for rank, voted, tiers in res:
+        assert voted == want and tiers == want
+
+
+def test_majority_matches_oracle_on_random_vectors():
+    from oracle import controller
+    rng = np.random.default_rng(5)
+    for _ in range(200):
+        n = int(rng.integers(1, 8))
+        vecs = rng.choice([2, 4, 8, 16], size=(n, 12)).tolist()
+        assert replicas.majority_tiers(vecs) == controller.majority_vote(vecs)
+    assert controller.majority_vote([[2], [8]]) == [8]            # tie -> widest
+    assert controller.majority_vote([[2], [2], [8]]) == [2]       # majority beats width
