@@ -19,4 +19,4 @@ scale, RNE to the integer code, clamp); attention and KL are accumulated in
 fp64.  Every function names the passage it follows.  Functions whose values
 have no independent pin say "parity unpinned" in their docstring.
 """
-from . import quant, pages, attention, canary, controller, decoder, sizes  # noqa: F401
+from . import quant, pages, attention, canary, controller, decoder, sizes, artifacts  # noqa: F401

@@ -41,8 +41,10 @@ class SeqState:
     change once written).
     """
 
-    def __init__(self, n_heads: int, d: int, vbits: int):
+    def __init__(self, n_heads: int, d: int, vbits: int, kclip=None, vclip=None):
         self.H, self.d = n_heads, d
+        self.kclip = kclip         # [H, d] fp32 K thresholds or None
+        self.vclip = vclip         # [H] fp32 V thresholds or None
         self._k = np.zeros((0, n_heads, d), dtype=np.float16)
         self._v = np.zeros((0, n_heads, d), dtype=np.float16)
         self._kh = np.zeros((0, n_heads, d), dtype=np.float32)   # sealed K, dequantized
@@ -99,7 +101,7 @@ class SeqState:
             if kb == 16:
                 self._kh[lo:hi] = self._k[lo:hi].astype(np.float32)
             else:
-                q, s = quant.quantize(self._k[lo:hi], kb, axis=0)
+                q, s = quant.quantize(self._k[lo:hi], kb, axis=0, clip=self.kclip)
                 self._kh[lo:hi] = quant.dequantize(q, s, axis=0)
         self._sealed_upto = max(self._sealed_upto, full)
         out = self._kh[:T].copy()
@@ -113,7 +115,7 @@ class SeqState:
             if self.vbits == 16:
                 self._vh[lo:T] = self._v[lo:T].astype(np.float32)
             else:
-                q, s = quant.quantize(self._v[lo:T], self.vbits, axis=2)
+                q, s = quant.quantize(self._v[lo:T], self.vbits, axis=2, clip=self.vclip)
                 self._vh[lo:T] = quant.dequantize(q, s, axis=2)
             self._vh_upto = T
         return self._vh[:T]
@@ -129,8 +131,10 @@ class SeqState:
         hi = min(lo + BLOCK, self.n)
         exp = {}
         if hi - lo == BLOCK:
-            exp.update(pages.sealed_k_bytes(kb, self._k[lo:hi, h]))
-        exp.update(pages.v_rows_bytes(self.vbits, self._v[lo:hi, h]))
+            exp.update(pages.sealed_k_bytes(kb, self._k[lo:hi, h],
+                                            None if self.kclip is None else self.kclip[h]))
+        exp.update(pages.v_rows_bytes(self.vbits, self._v[lo:hi, h],
+                                      None if self.vclip is None else self.vclip[h]))
         return exp
 
 
@@ -159,8 +163,12 @@ class Trace:
         self.after = {}       # step -> tiers after the update
 
 
-def controller_trace(w, n_steps: int, device="cpu") -> Trace:
-    """Run the canary + controller over all layers for steps 0..n_steps-1."""
+def controller_trace(w, n_steps: int, device="cpu", clips=None) -> Trace:
+    """Run the canary + controller over all layers for steps 0..n_steps-1.
+
+    clips: {layer: (K thresholds [Hkv, d], V thresholds [Hkv])} for layers
+    with a frozen clipping artifact (the canary measures the cache's own
+    quantizer), or None."""
     ctl = controller.Controller(w.k_bits_init, w.alpha, w.tau)
     tr = Trace()
     for t in range(n_steps):
@@ -170,7 +178,8 @@ def controller_trace(w, n_steps: int, device="cpu") -> Trace:
         deltas = np.zeros((w.num_layers, 3), dtype=np.float64)
         for l in range(w.num_layers):
             Q = w.step_q(l, t, 1, device=device)[:, 0].cpu().numpy()
-            deltas[l] = canary.layer_delta(Q, layer_windows(w, l, t, device))
+            kc = None if not clips or l not in clips else clips[l][0]
+            deltas[l] = canary.layer_delta(Q, layer_windows(w, l, t, device), clip=kc)
         tr.delta[t] = deltas
         ctl.update(deltas.astype(np.float32))
         tr.ema[t] = np.array(ctl.ema, dtype=np.float32)
@@ -186,14 +195,19 @@ class ReferenceRun:
     workload's seeded draws for the chosen coordinates only.
     """
 
-    def __init__(self, w, trace: Trace, layers=None, seqs=None, heads=None, device="cpu"):
+    def __init__(self, w, trace: Trace, layers=None, seqs=None, heads=None, device="cpu",
+                 clips=None):
         self.w = w
         self.trace = trace
         self.layers = list(range(w.num_layers)) if layers is None else list(layers)
         self.seqs = list(range(w.batch)) if seqs is None else list(seqs)
         self.heads = list(range(w.num_kv_heads)) if heads is None else list(heads)
         self.device = device
-        self.state = {(l, s): SeqState(len(self.heads), w.head_dim, w.v_bits[l])
+        clips = clips or {}
+        sel = lambda l, i: (None if l not in clips or clips[l][i] is None
+                            else np.asarray(clips[l][i], dtype=np.float32)[self.heads])
+        self.state = {(l, s): SeqState(len(self.heads), w.head_dim, w.v_bits[l],
+                                       sel(l, 0), sel(l, 1))
                       for l in self.layers for s in self.seqs}
         self.steps_done = 0
 

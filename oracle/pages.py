@@ -69,23 +69,25 @@ def scale_order(kb: int, d: int) -> np.ndarray:
     return (p // n) * n + (p % n) // 2 + (p % 2) * (n // 2)
 
 
-def sealed_k_bytes(kb: int, k16: np.ndarray) -> dict:
-    """Expected bytes of a full page's K part from its 16 raw fp16 rows [16, d]."""
+def sealed_k_bytes(kb: int, k16: np.ndarray, clip=None) -> dict:
+    """Expected bytes of a full page's K part from its 16 raw fp16 rows [16, d]
+    (clip: per-channel thresholds [d] or None)."""
     k16 = np.asarray(k16, dtype=np.float16)
     assert k16.shape[0] == BLOCK
     if kb == 16:
         return {"k_raw": k16.view(np.uint8).reshape(BLOCK, -1)}
-    q, s = quant.quantize(k16, kb, axis=0)          # one group per channel
+    q, s = quant.quantize(k16, kb, axis=0, clip=clip)   # one group per channel
     s = s[scale_order(kb, k16.shape[1])]
     return {"k_codes": quant.pack(q, kb), "k_scales": s.astype(np.float16).view(np.uint8)[None, :]}
 
 
-def v_rows_bytes(vb: int, v16: np.ndarray) -> dict:
-    """Expected bytes of V rows [n, d] (rows 0..n-1 of the page)."""
+def v_rows_bytes(vb: int, v16: np.ndarray, clip=None) -> dict:
+    """Expected bytes of V rows [n, d] (rows 0..n-1 of the page; clip: the
+    head's threshold or None)."""
     v16 = np.asarray(v16, dtype=np.float16)
     if vb == 16:
         return {"v_raw": v16.view(np.uint8).reshape(v16.shape[0], -1)}
-    q, s = quant.quantize(v16, vb, axis=1)          # one group per token
+    q, s = quant.quantize(v16, vb, axis=1, clip=clip)   # one group per token
     return {"v_codes": quant.pack(q, vb),
             "v_scales": s.astype(np.float16).view(np.uint8).reshape(-1, 2)}
 

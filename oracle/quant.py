@@ -7,10 +7,17 @@ Behavior-Guided KV-Cache Quantization page, "K/V Role-Aware Low-Bit
 Quantization"):
 
     qmax = 2**(b-1) - 1
-    m    = max |x_i|                       over the group (exact on fp16 values)
+    m    = min( max |x_i|, c )             over the group (exact on fp16 values)
     s    = fp16_rne( fp32(m) / fp32(qmax) ) the stored scale
     q_i  = clamp( rne( fp32(x_i) / fp32(s) ), -qmax, +qmax ),  q_i = 0 if s == 0
     xhat = fp32(q_i) * fp32(s)             (exact in fp32 for b <= 8)
+
+c is the group's clipping threshold, +inf (no clipping) unless a frozen
+calibration artifact sets one ("Behavior-Guided KV-Cache Quantization",
+"Calibration protocol": the selected scales and clipping thresholds are frozen
+and reused by the cache; reading: clipping the group at c before the absmax
+makes its range min(absmax, c), and values beyond c take the end codes
++-qmax through the clamp).  With c = +inf the quantizer is the plain one.
 
 All divisions are IEEE fp32 correctly rounded (numpy float32 arithmetic),
 rne is round-half-to-even (numpy.rint), and the fp32 -> fp16 conversion is
@@ -35,14 +42,22 @@ def qmax(b: int) -> int:
     return (1 << (b - 1)) - 1
 
 
-def quantize(x16: np.ndarray, b: int, axis: int):
-    """Quantize fp16 `x16` in groups along `axis` -> (q int16, s fp16 with `axis` removed)."""
+def quantize(x16: np.ndarray, b: int, axis: int, clip=None):
+    """Quantize fp16 `x16` in groups along `axis` -> (q int16, s fp16 with `axis` removed).
+
+    `clip` (fp32, broadcast against the groups: the shape of `x16` without
+    `axis`, or a scalar) caps each group's absmax; None = no clipping."""
     x16 = np.asarray(x16)
     if x16.dtype != F16:
         raise TypeError("quantizer input must be fp16")
     x = x16.astype(F32)
     qm = F32(qmax(b))
     m = np.max(np.abs(x), axis=axis, keepdims=True)
+    if clip is not None:
+        c = np.asarray(clip, dtype=F32)
+        if np.any(np.isnan(c)) or np.any(c <= 0):
+            raise ValueError("clipping thresholds must be positive (+inf: none)")
+        m = np.expand_dims(np.minimum(np.squeeze(m, axis=axis), c), axis)
     s32 = (m / qm).astype(F32)
     s16 = s32.astype(F16)
     sf = s16.astype(F32)
