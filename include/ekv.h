@@ -95,7 +95,8 @@ typedef struct ekv_config {
   int32_t vote;            /* >= 2: a tier changes only after that many consecutive
                               firings picked the same new tier                      */
   /* Device allocator.  NULL -> cudaMalloc/cudaFree.  Called only inside
-   * ekv_create/ekv_destroy. */
+   * ekv_create/ekv_destroy; must return 16-byte aligned memory (else
+   * ekv_create fails with EKV_ENOMEM). */
   void* (*dev_alloc)(size_t bytes, void* ctx);
   void (*dev_free)(void* ptr, void* ctx);
   void* alloc_ctx;
@@ -235,6 +236,52 @@ EKV_API int ekv_tier_update(ekv_cache* cache, const float* delta, const uint8_t*
 
 /* Overwrite the tiers (host uint8[num_layers], each 2, 4, 8 or 16). */
 EKV_API int ekv_set_tiers(ekv_cache* cache, const uint8_t* tiers, void* stream);
+
+/* ---- Static-artifact mode ("Behavior-Guided KV-Cache Quantization": the
+ * framework's "Freeze & allocate" and "Online inference" stages, "Calibration
+ * protocol", "Sensitivity-Driven Budget Allocation").  Offline calibration
+ * freezes clipping thresholds (theta*) and per-layer bits (b*); online, the
+ * cache is created with b* as its tiers, the thresholds are loaded, and the
+ * controller is left unfired (read-only configuration). */
+
+/* Clipping thresholds of one layer (host float arrays; syncs stream):
+ *   k_clip [Hkv][d]  per (KV head, channel): caps each sealed K block's
+ *                    per-channel absmax, m = min(absmax, c);
+ *   v_clip [Hkv]     per KV head: caps each V token's absmax.
+ * The quantizer is otherwise unchanged (s = fp16_rne(m / qmax), codes clamped
+ * to +-qmax, so values beyond c take the end codes).  The canary quantizes the
+ * ring with the same K thresholds.  NULL = no clipping (+inf) for that part;
+ * every threshold must be > 0 (+inf allowed), else EKV_EINVAL and nothing
+ * changes.  New thresholds govern pages sealed and V rows written afterwards;
+ * pages already written keep their bytes.  A new handle has no clipping. */
+EKV_API int ekv_set_clip(ekv_cache* cache, int32_t layer, const float* k_clip,
+                         const float* v_clip, void* stream);
+/* Read one layer's thresholds back (host outputs, either may be NULL; syncs). */
+EKV_API int ekv_get_clip(ekv_cache* cache, int32_t layer, float* k_clip, float* v_clip,
+                         void* stream);
+
+/* Nearest-rank quantile of |x| per group (a calibration threshold):
+ *   x       dev fp16, 2-byte aligned; group g's elements are
+ *           x[r * row_stride + g * group_stride + i], r < n_rows, i < group_width
+ *           (strides in elements; every addressed element must lie in the buffer)
+ *   out     dev float[n_groups], 4-byte aligned
+ * With the group's n = n_rows * group_width magnitudes sorted ascending, out[g]
+ * is the one of 1-based rank max(1, ceil(q * n)) (q * n in fp64), so it is one
+ * of the group's own values.  K thresholds of [T][Hkv][d] keys: n_rows = T,
+ * row_stride = Hkv*d, n_groups = Hkv*d, group_stride = 1, group_width = 1.
+ * V thresholds per head: n_groups = Hkv, group_stride = d, group_width = d.
+ * Needs 0 <= q <= 1, n < 2^32 and finite inputs; else EKV_EINVAL (nothing enqueued). */
+EKV_API int ekv_abs_percentile(const void* x, int64_t n_rows, int64_t row_stride,
+                               int32_t n_groups, int64_t group_stride, int32_t group_width,
+                               double q, float* out, void* stream);
+
+/* AutoK: the smallest number k of layers whose sensitivities, taken largest
+ * first (equal values: lower index first), sum in fp64 to >= frac times the
+ * sum of all n.  sensitivity host double[n] (finite, >= 0); 0 <= frac <= 1.
+ * order_out (host int32[n], may be NULL) receives that order; *k_out = k.
+ * The first k layers of the order are the ones to protect with more bits. */
+EKV_API int ekv_autok(const double* sensitivity, int32_t n, double frac, int32_t* order_out,
+                      int32_t* k_out);
 
 /* Controller state (syncs stream).  Any output pointer may be NULL.
  *   tiers uint8[L], ema float[L][3], delta float[L][3], ema_valid int32[L] (host). */

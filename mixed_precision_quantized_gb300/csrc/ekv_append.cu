@@ -81,10 +81,12 @@ append_kernel(DevState st, int layer, const int32_t* __restrict__ slots, int n_n
       const int kb = bits_of_code(fmt >> 2), vb = bits_of_code(fmt & 3);
       uint8_t* page = st.pool_base[fmt] + (size_t)entry_idx(e) * st.pool_page_bytes[fmt];
       uint8_t* vpart = page + k_part_bytes(kb, D);
+      const size_t lh = (size_t)layer * st.Hkv + h;
+      const float vc = st.vclip[lh];
       for (int p = lo + warp; p < hi; p += NWARP)
-        quant_v_row<D>(vin + (size_t)(p - told) * in_row, vpart, p - j * BLOCK, vb, lane);
+        quant_v_row<D>(vin + (size_t)(p - told) * in_row, vpart, p - j * BLOCK, vb, lane, vc);
       if (hi == j * BLOCK + BLOCK) {
-        if (tid < CH) seal_k<D>(stg, kin, in_row, j, told, kb, page, tid);
+        if (tid < CH) seal_k<D>(stg, kin, in_row, j, told, kb, page, tid, st.kclip + lh * D);
       } else {
         for (int i = tid; i < (hi - lo) * CH; i += APPEND_THREADS) {
           const int p = lo + i / CH, cc = i % CH;

@@ -727,9 +727,10 @@ __device__ int32_t append_token(const DevState& st, int layer, int slot, int h, 
     const int fmt = entry_fmt(e);
     const int kb = bits_of_code(fmt >> 2), vb = bits_of_code(fmt & 3);
     uint8_t* page = st.pool_base[fmt] + (size_t)entry_idx(e) * st.pool_page_bytes[fmt];
-    quant_v_row<D>(vin, page + k_part_bytes(kb, D), r, vb, lane);
+    const size_t lh = (size_t)layer * st.Hkv + h;
+    quant_v_row<D>(vin, page + k_part_bytes(kb, D), r, vb, lane, st.vclip[lh]);
     if (r == BLOCK - 1) {
-      if (lane < CH) seal_k<D>(stg, kin, 0, j, told, kb, page, lane);
+      if (lane < CH) seal_k<D>(stg, kin, 0, j, told, kb, page, lane, st.kclip + lh * D);
     } else if (lane < CH) {
       *reinterpret_cast<uint4*>(stg + (size_t)r * D + 8 * lane) =
           *reinterpret_cast<const uint4*>(kin + 8 * lane);

@@ -78,6 +78,7 @@ canary_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
     const int r0 = gi * 16, r1 = min(r0 + 16, n);
     float m = 0.f;
     for (int r = r0; r < r1; ++r) m = fmaxf(m, fabsf(W[r * P + c]));
+    m = fminf(m, st.kclip[((size_t)layer * st.Hkv + h) * D + c]);  // the cache's own quantizer
 #pragma unroll
     for (int bi = 0; bi < NBITS; ++bi) {
       const int b = 2 << bi;

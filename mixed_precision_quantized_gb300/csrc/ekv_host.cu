@@ -30,6 +30,7 @@ void* dev_alloc(ekv_cache* c, size_t bytes) {
     p = nullptr;
   }
   if (p) c->allocs.push_back(p);
+  if (reinterpret_cast<uintptr_t>(p) & 15) return nullptr;  // every table is read in 16-byte units
   return p;
 }
 
@@ -172,6 +173,8 @@ int ekv_create(const ekv_config* cfg, const uint8_t* k_bits_init, const uint8_t*
   st.cand = (int32_t*)A(L * 4);
   st.cnt = (int32_t*)A(L * 4);
   st.delta = (float*)A(L * 3 * 4);
+  st.kclip = (float*)A(L * H * D * 4);
+  st.vclip = (float*)A(L * H * 4);
   st.err = (int32_t*)A(4);
   st.append_ticket = (int32_t*)A(L * S * 4);
   int parts = 0;
@@ -211,6 +214,11 @@ int ekv_create(const ekv_config* cfg, const uint8_t* k_bits_init, const uint8_t*
   if (e == cudaSuccess) e = cudaMemcpy(st.tier, tiers.data(), L * 4, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(st.vbits, vb.data(), L * 4, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemset(st.bt, 0xFF, L * S * H * MB * 4);
+  {
+    const std::vector<float> none((size_t)L * H * D, INFINITY);
+    if (e == cudaSuccess) e = cudaMemcpy(st.kclip, none.data(), L * H * D * 4, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(st.vclip, none.data(), L * H * 4, cudaMemcpyHostToDevice);
+  }
   Z(st.len, L * S * 4);
   Z(st.kmax, L * 4);
   Z(st.staging, L * S * H * BLOCK * D * 2);
@@ -314,6 +322,44 @@ int ekv_set_tiers(ekv_cache* c, const uint8_t* tiers, void* stream) {
   cudaStream_t s = as_stream(stream);
   cudaError_t e = cudaMemcpyAsync(c->st.tier, t.data(), t.size() * 4, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);  // t is a host temporary
+  return cuda_status(e);
+}
+
+int ekv_set_clip(ekv_cache* c, int32_t layer, const float* k_clip, const float* v_clip,
+                 void* stream) {
+  if (!c || layer < 0 || layer >= c->st.L) return EKV_EINVAL;
+  const int H = c->st.Hkv, D = c->st.D;
+  std::vector<float> kc((size_t)H * D, INFINITY), vc(H, INFINITY);
+  auto take = [](const float* src, std::vector<float>& dst) {
+    if (!src) return true;
+    for (size_t i = 0; i < dst.size(); ++i) {
+      if (!(src[i] > 0.f)) return false;  // NaN, zero and negative thresholds
+      dst[i] = src[i];
+    }
+    return true;
+  };
+  if (!take(k_clip, kc) || !take(v_clip, vc)) return EKV_EINVAL;
+  cudaStream_t s = as_stream(stream);
+  const size_t lh = (size_t)layer * H;
+  cudaError_t e = cudaMemcpyAsync(c->st.kclip + lh * D, kc.data(), kc.size() * 4,
+                                  cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(c->st.vclip + lh, vc.data(), vc.size() * 4, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);  // kc, vc are host temporaries
+  return cuda_status(e);
+}
+
+int ekv_get_clip(ekv_cache* c, int32_t layer, float* k_clip, float* v_clip, void* stream) {
+  if (!c || layer < 0 || layer >= c->st.L) return EKV_EINVAL;
+  const int H = c->st.Hkv, D = c->st.D;
+  cudaStream_t s = as_stream(stream);
+  const size_t lh = (size_t)layer * H;
+  cudaError_t e = cudaSuccess;
+  if (k_clip)
+    e = cudaMemcpyAsync(k_clip, c->st.kclip + lh * D, (size_t)H * D * 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && v_clip)
+    e = cudaMemcpyAsync(v_clip, c->st.vclip + lh, (size_t)H * 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   return cuda_status(e);
 }
 

@@ -64,6 +64,8 @@ struct DevState {
   int32_t* cand;            // [L] tier the last firings picked (vote)
   int32_t* cnt;             // [L] consecutive firings that picked `cand`
   float* delta;             // [L][3] last canary readings
+  float* kclip;             // [L][Hkv][D] K clipping thresholds (+inf: none)
+  float* vclip;             // [L][Hkv]    V clipping thresholds (+inf: none)
   int32_t* err;             // device error word
   int32_t* append_ticket;   // [L][S]
   float* attn_acc;          // [parts][G][D]   split partial numerators

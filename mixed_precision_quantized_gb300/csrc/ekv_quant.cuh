@@ -6,8 +6,12 @@
 // Quantizer ("Behavior-Guided KV-Cache Quantization", "K/V Role-Aware Low-Bit
 // Quantization": symmetric, K per channel, V per token; KV-Kaizen, "Three
 // Non-Eviction Compression Axes", item 3: symmetric uniform):
-//   s = fp16_rne(m / qmax) with m = absmax of the group (IEEE fp32 division),
-//   q = clamp(rne(x / s), -qmax, qmax), stored offset binary q + 2^(b-1).
+//   s = fp16_rne(m / qmax) with m = min(absmax of the group, c) (IEEE fp32
+//   division), q = clamp(rne(x / s), -qmax, qmax), stored offset binary
+//   q + 2^(b-1).  c is the group's frozen clipping threshold, +inf unless a
+//   calibration artifact set one ("Behavior-Guided KV-Cache Quantization",
+//   "Calibration protocol": selected scales and clipping thresholds are frozen
+//   and reused by the cache); with c = +inf the quantizer is the plain one.
 #pragma once
 
 #include "ekv_internal.h"
@@ -52,10 +56,12 @@ __device__ __forceinline__ void store_codes8(uint8_t* dst, const int* u, int b) 
   }
 }
 
-// One V row (one token of one KV head): absmax over D channels, one fp16 scale.
-// Called by a whole warp; lanes < D/8 own 8 channels each.
+// One V row (one token of one KV head): absmax over D channels, capped at the
+// head's threshold vc, one fp16 scale.  Called by a whole warp; lanes < D/8
+// own 8 channels each.
 template <int D>
-__device__ void quant_v_row(const __half* src, uint8_t* vpart, int r, int vb, int lane) {
+__device__ void quant_v_row(const __half* src, uint8_t* vpart, int r, int vb, int lane,
+                            float vc) {
   constexpr int CH = D / 8;
   uint4 u = make_uint4(0, 0, 0, 0);
   float f[8];
@@ -74,7 +80,7 @@ __device__ void quant_v_row(const __half* src, uint8_t* vpart, int r, int vb, in
     return;
   }
   const int qm = (1 << (vb - 1)) - 1;
-  const __half s16 = __float2half_rn(__fdiv_rn(m, (float)qm));
+  const __half s16 = __float2half_rn(__fdiv_rn(fminf(m, vc), (float)qm));
   const float sf = __half2float(s16);
   int code[8];
 #pragma unroll
@@ -84,10 +90,11 @@ __device__ void quant_v_row(const __half* src, uint8_t* vpart, int r, int vb, in
 }
 
 // Seal a full K block: thread t owns channels [8t, 8t+8) over the 16 rows.
-// Rows before `told` come from the staging rows, the rest from the input.
+// Rows before `told` come from the staging rows, the rest from the input;
+// kc holds the head's D per-channel thresholds.
 template <int D>
 __device__ void seal_k(const __half* stg, const __half* kin, size_t in_row, int j, int told,
-                       int kb, uint8_t* kpart, int t) {
+                       int kb, uint8_t* kpart, int t, const float* kc) {
   float m[8];
 #pragma unroll
   for (int c = 0; c < 8; ++c) m[c] = 0.f;
@@ -108,11 +115,14 @@ __device__ void seal_k(const __half* stg, const __half* kin, size_t in_row, int 
     for (int c = 0; c < 8; ++c) m[c] = fmaxf(m[c], fabsf(f[c]));
   }
   const int qm = (1 << (kb - 1)) - 1;
+  const float4 c0 = *reinterpret_cast<const float4*>(kc + 8 * t);
+  const float4 c1 = *reinterpret_cast<const float4*>(kc + 8 * t + 4);
+  const float cl[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
   float sf[8];
   __align__(16) __half s16[8];
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
-    s16[c] = __float2half_rn(__fdiv_rn(m[c], (float)qm));
+    s16[c] = __float2half_rn(__fdiv_rn(fminf(m[c], cl[c]), (float)qm));
     sf[c] = __half2float(s16[c]);
   }
   for (int r = 0; r < BLOCK; ++r) {

@@ -72,6 +72,11 @@ _SIGS = {
     "ekv_state_size": (ctypes.c_int64, [_P]),
     "ekv_state_save": (ctypes.c_int, [_P, _P, ctypes.c_int64, _P]),
     "ekv_state_load": (ctypes.c_int, [_P, _P, ctypes.c_int64, _P]),
+    "ekv_set_clip": (ctypes.c_int, [_P, _I32, _P, _P, _P]),
+    "ekv_get_clip": (ctypes.c_int, [_P, _I32, _P, _P, _P]),
+    "ekv_abs_percentile": (ctypes.c_int, [_P, ctypes.c_int64, ctypes.c_int64, _I32,
+                                          ctypes.c_int64, _I32, ctypes.c_double, _P, _P]),
+    "ekv_autok": (ctypes.c_int, [_P, _I32, ctypes.c_double, _P, _P]),
 }
 EXPORTS = tuple(_SIGS)
 
@@ -228,6 +233,31 @@ class Cache:
                                      _stream(stream)), "ekv_tier_update")
 
     # ---- control and inspection ------------------------------------------------
+    def set_clip(self, layer: int, k_clip=None, v_clip=None, stream=None):
+        """Load one layer's clipping thresholds: k_clip [Hkv, d], v_clip [Hkv]
+        (anything float-convertible; None = no clipping for that part)."""
+        H, d = self.num_kv_heads, self.head_dim
+
+        def arr(x, n):
+            if x is None:
+                return None
+            v = [float(t) for t in torch.as_tensor(x, dtype=torch.float32).reshape(-1).tolist()]
+            if len(v) != n:
+                raise ValueError(f"expected {n} thresholds, got {len(v)}")
+            return (ctypes.c_float * n)(*v)
+
+        _check(lib().ekv_set_clip(self._h, layer, arr(k_clip, H * d), arr(v_clip, H),
+                                  _stream(stream)), "ekv_set_clip")
+
+    def get_clip(self, layer: int, stream=None):
+        """(k_clip [Hkv, d], v_clip [Hkv]) float32 CPU tensors (+inf: none)."""
+        H, d = self.num_kv_heads, self.head_dim
+        k = (ctypes.c_float * (H * d))()
+        v = (ctypes.c_float * H)()
+        _check(lib().ekv_get_clip(self._h, layer, k, v, _stream(stream)), "ekv_get_clip")
+        return (torch.tensor(list(k), dtype=torch.float32).view(H, d),
+                torch.tensor(list(v), dtype=torch.float32))
+
     def set_tiers(self, tiers, stream=None):
         t = (ctypes.c_uint8 * self.num_layers)(*[int(b) for b in tiers])
         _check(lib().ekv_set_tiers(self._h, t, _stream(stream)), "ekv_set_tiers")
@@ -286,6 +316,45 @@ class Cache:
 
     def load_state(self, blob: bytes, stream=None):
         _check(lib().ekv_state_load(self._h, blob, len(blob), _stream(stream)), "ekv_state_load")
+
+
+def abs_percentile(x: torch.Tensor, q: float, n_rows: int, row_stride: int, n_groups: int,
+                   group_stride: int, group_width: int, out: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
+    """Nearest-rank q-quantile of |x| per group (ekv_abs_percentile) -> float32 [n_groups]."""
+    if x.dtype != torch.float16 or not x.is_cuda:
+        raise TypeError("x must be a CUDA fp16 tensor")
+    if out is None:
+        out = torch.empty(n_groups, dtype=torch.float32, device=x.device)
+    _check(lib().ekv_abs_percentile(_ptr(x), n_rows, row_stride, n_groups, group_stride,
+                                    group_width, float(q), _ptr(out), _stream(stream)),
+           "ekv_abs_percentile")
+    return out
+
+
+def k_thresholds(k: torch.Tensor, q: float, stream=None) -> torch.Tensor:
+    """Per (KV head, channel) thresholds [Hkv, d] of contiguous keys [T, Hkv, d]."""
+    T, H, d = k.shape
+    k = k.contiguous()
+    return abs_percentile(k, q, T, H * d, H * d, 1, 1, stream=stream).view(H, d)
+
+
+def v_thresholds(v: torch.Tensor, q: float, stream=None) -> torch.Tensor:
+    """Per KV head thresholds [Hkv] of contiguous values [T, Hkv, d]."""
+    T, H, d = v.shape
+    v = v.contiguous()
+    return abs_percentile(v, q, T, H * d, H, d, d, stream=stream)
+
+
+def autok(sensitivity, frac: float):
+    """(k, order): the fewest most-sensitive layers holding >= frac of the total."""
+    s = [float(x) for x in sensitivity]
+    n = len(s)
+    arr = (ctypes.c_double * max(1, n))(*s)
+    order = (ctypes.c_int32 * max(1, n))()
+    k = ctypes.c_int32()
+    _check(lib().ekv_autok(arr, n, float(frac), order, ctypes.byref(k)), "ekv_autok")
+    return k.value, list(order[:n])
 
 
 def cache_for(w, device=None, max_seqs: int | None = None, torch_alloc: bool = True) -> Cache:

@@ -73,7 +73,9 @@ class Run:
     """A workload on the GPU next to its oracle."""
 
     def __init__(self, w: workloads.Workload, steps: int, layers=None, seqs=None, heads=None,
-                 gen_device="cuda", trace=None, pool_pages=None, fused=False):
+                 gen_device="cuda", trace=None, pool_pages=None, fused=False, clips=None):
+        """clips: {layer: (K thresholds [Hkv, d], V thresholds [Hkv])} loaded into
+        the cache before the prefill and given to the oracle."""
         self.w, self.steps, self.fused = w, steps, fused
         if pool_pages is None:
             self.cache = ekv.cache_for(w)
@@ -81,12 +83,15 @@ class Run:
             self.cache = ekv.Cache(w.num_layers, w.batch, w.num_q_heads, w.num_kv_heads,
                                    w.head_dim, w.max_seq_len, pool_pages, w.k_bits_init,
                                    w.v_bits, alpha=w.alpha, tau=w.tau)
+        for l, (kc, vc) in (clips or {}).items():
+            self.cache.set_clip(l, kc, vc)
         self.slots = torch.arange(w.batch, dtype=torch.int32, device="cuda")
         runner.prefill(self.cache, w, self.slots)
         self.cache.sync()
-        self.trace = trace if trace is not None else decoder.controller_trace(w, steps,
-                                                                              device=gen_device)
-        self.ref = decoder.ReferenceRun(w, self.trace, layers, seqs, heads, device=gen_device)
+        self.trace = trace if trace is not None else decoder.controller_trace(
+            w, steps, device=gen_device, clips=clips)
+        self.ref = decoder.ReferenceRun(w, self.trace, layers, seqs, heads, device=gen_device,
+                                        clips=clips)
         self.ref.prefill()
         self.inp = runner.Inputs(w, 0, steps)
         self.out = [torch.empty(w.batch, w.num_q_heads, w.head_dim, dtype=torch.float16,

@@ -65,3 +65,41 @@ def test_create_rejects_bad_config_without_gpu(lib):
     kb = (ctypes.c_uint8 * 1)(4)
     assert lib.ekv_create(ctypes.byref(cfg), kb, kb, ctypes.byref(h)) == 1   # EINVAL
     assert lib.ekv_create(None, kb, kb, ctypes.byref(h)) == 1
+
+
+def test_autok_host_allocator_matches_oracle(lib):
+    """AutoK runs on the host: the library's order and count equal the oracle's."""
+    import numpy as np
+    from mixed_precision_quantized_gb300 import ekv
+    from oracle import artifacts
+    rng = np.random.default_rng(17)
+    for _ in range(300):
+        L = int(rng.integers(0, 40))
+        s = rng.random(L) ** 3
+        s[rng.random(L) < 0.2] = 0.0
+        s[rng.random(L) < 0.2] = s[0] if L else 0.0          # equal values: order by layer
+        frac = float(rng.choice([0.0, 0.3, 0.5, 0.9, 0.99, 1.0, rng.random()]))
+        k, order = ekv.autok(s.tolist(), frac)
+        assert order == artifacts.sensitivity_order(s)
+        assert k == artifacts.autok(s, frac)
+    for bad_s, bad_f in (([1.0, -1.0], 0.5), ([float("nan")], 0.5), ([float("inf")], 0.5),
+                         ([1.0], 1.01), ([1.0], -0.5)):
+        with pytest.raises(ekv.EkvError):
+            ekv.autok(bad_s, bad_f)
+
+
+def test_artifact_save_load_round_trip(tmp_path):
+    """The static-artifact bundle survives a save and comes back read-only."""
+    import numpy as np
+    from mixed_precision_quantized_gb300 import artifacts as product
+    a = product.Artifact([4, 8, 4], [4, 8, 16], np.arange(3 * 2 * 64, dtype=np.float32).reshape(3, 2, 64) + 1,
+                         np.array([[1, np.inf], [2, 3], [4, 5]], np.float32), [1.0, 0.99, 0.9],
+                         [1.0, 1.0, 0.99], [0.1, 0.3, 0.2], 0.5, 4, 8)
+    p = tmp_path / "a.npz"
+    a.save(p)
+    b = product.Artifact.load(p)
+    assert (b.k_bits, b.v_bits, b.k_percentile, b.v_percentile, b.sensitivity, b.frac, b.low,
+            b.high) == (a.k_bits, a.v_bits, a.k_percentile, a.v_percentile, a.sensitivity,
+                        a.frac, a.low, a.high)
+    assert np.array_equal(b.k_clip, a.k_clip) and np.array_equal(b.v_clip, a.v_clip)
+    assert not b.v_clip.flags.writeable
