@@ -68,6 +68,11 @@ def parse():
                         "pages fit in L2 is still read from HBM")
     p.add_argument("--no-overlap-check", action="store_true",
                    help="skip timing the fused step without the overlap of consecutive layers")
+    p.add_argument("--static", action="store_true",
+                   help="static-artifact mode: calibrate thresholds and per-layer K bits on "
+                        "the workload's first --calib-tokens prefill tokens, load them, and "
+                        "time the same step with the canary off")
+    p.add_argument("--calib-tokens", type=int, default=8192)
     p.add_argument("--separate", action="store_true",
                    help="append and attention as two launches per layer (default: one fused launch)")
     return p.parse_args()
@@ -237,6 +242,41 @@ def main():
     if n_steps_total > w.steps:
         raise SystemExit(f"workload holds {w.steps} decode steps; asked for {n_steps_total}")
 
+    static = None
+    if a.static:
+        from mixed_precision_quantized_gb300 import artifacts
+        wc = w.scaled(prefill=[min(t, a.calib_tokens) for t in w.prefill])
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        art, _ = artifacts.calibrate(wc, device=dev)
+        torch.cuda.synchronize()
+        cal_s = time.perf_counter() - t0
+        # the percentile select on one layer's full prefill keys and values
+        kf, vf = w.prefill_kv(0, list(range(w.batch)), device=dev)
+        kf, vf = kf.flatten(0, 1).contiguous(), vf.flatten(0, 1).contiguous()
+        sel = {}
+        for name, fn, x in (("k", ekv.k_thresholds, kf), ("v", ekv.v_thresholds, vf)):
+            fn(x, 0.999)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(5):
+                fn(x, 0.999)
+            e1.record()
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / 5
+            sel[name] = {"us": us, "bytes_read": 2 * x.numel() * 2,
+                         "gbs": 2 * x.numel() * 2 / (us * 1e-6) / 1e9}
+        del kf, vf
+        bits = {str(b): art.k_bits.count(b) for b in sorted(set(art.k_bits))}
+        static = {"calibration_s": cal_s, "calibration_tokens_per_seq": wc.prefill[0],
+                  "k_bits_layers": bits, "frac": art.frac, "low": art.low, "high": art.high,
+                  "k_percentiles": sorted(set(art.k_percentile)),
+                  "v_percentiles": sorted(set(art.v_percentile)),
+                  "percentile_select": {**sel, "note": "two passes over the data (radix "
+                                        "select): bytes_read counts both; one layer's "
+                                        "full prefill"}}
+        w = art.workload(w)
+
     NR = max(1, a.rotate)
     if K % NR:
         raise SystemExit("--steps must be a multiple of --rotate")
@@ -245,6 +285,8 @@ def main():
     t0 = time.perf_counter()
     for _ in range(NR):
         caches.append(ekv.cache_for(w, device=dev))
+        if static is not None:
+            art.apply(caches[-1])
         runner.prefill(caches[-1], w, slots, device=dev)
         caches[-1].sync()
     prefill_s = (time.perf_counter() - t0) / NR
@@ -503,8 +545,10 @@ def main():
         "config": {"workload": f"{w.name}: {w.num_layers} layers, batch {B}, "
                                f"{w.num_q_heads} q / {w.num_kv_heads} kv heads, d {w.head_dim}, "
                                f"{w.prefill[0] if len(set(w.prefill)) == 1 else 'ragged'} cached "
-                               f"tokens, K tier by canary every {w.canary_period} steps "
-                               f"(tau {w.tau}), V INT{w.v_bits[0]}",
+                               + (f"tokens, K tier by canary every {w.canary_period} steps "
+                                  f"(tau {w.tau}), " if static is None else
+                                  "tokens, K bits per layer from the static artifact, ")
+                               + f"V INT{w.v_bits[0]}",
                    "l2": (f"inputs larger than L2: {step_bytes / 1e9:.2f} GB of pages read per step"
                           if NR == 1 else
                           f"steps rotate over {NR} caches of {step_bytes / 1e9:.3f} GB of pages "
@@ -512,7 +556,10 @@ def main():
                    "parallelism": f"replicas x{world} (one sequence set per GPU)",
                    "graph": "CUDA graph of the timed steps", "canary_fires_in_timed": fired_A,
                    "step": ("one fused append + attention launch per layer" if fused
-                            else "append and attention launches per layer")},
+                            else "append and attention launches per layer")
+                           + ("; static artifact: calibrated per-layer K bits and clipping "
+                              "thresholds loaded, canary off" if static else "")},
+        "static": static,
         "attn_hbm_gbs": achieved,
         "attn_frac_of_8tbs": achieved / NOMINAL_HBM_GBS if achieved else None,
         "step_hbm_gbs": step_bytes / (tA / K) / 1e9,

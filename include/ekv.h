@@ -265,6 +265,8 @@ EKV_API int ekv_get_clip(ekv_cache* cache, int32_t layer, float* k_clip, float* 
  *           x[r * row_stride + g * group_stride + i], r < n_rows, i < group_width
  *           (strides in elements; every addressed element must lie in the buffer)
  *   out     dev float[n_groups], 4-byte aligned
+ *   scratch dev, 4-byte aligned, at least ekv_abs_percentile_scratch_bytes
+ *           (n_groups) bytes (caller-owned; overwritten; one call at a time)
  * With the group's n = n_rows * group_width magnitudes sorted ascending, out[g]
  * is the one of 1-based rank max(1, ceil(q * n)) (q * n in fp64), so it is one
  * of the group's own values.  K thresholds of [T][Hkv][d] keys: n_rows = T,
@@ -273,7 +275,10 @@ EKV_API int ekv_get_clip(ekv_cache* cache, int32_t layer, float* k_clip, float* 
  * Needs 0 <= q <= 1, n < 2^32 and finite inputs; else EKV_EINVAL (nothing enqueued). */
 EKV_API int ekv_abs_percentile(const void* x, int64_t n_rows, int64_t row_stride,
                                int32_t n_groups, int64_t group_stride, int32_t group_width,
-                               double q, float* out, void* stream);
+                               double q, float* out, void* scratch, int64_t scratch_bytes,
+                               void* stream);
+/* Scratch bytes ekv_abs_percentile needs for n_groups groups (host only). */
+EKV_API int ekv_abs_percentile_scratch_bytes(int32_t n_groups, int64_t* out);
 
 /* AutoK: the smallest number k of layers whose sensitivities, taken largest
  * first (equal values: lower index first), sum in fp64 to >= frac times the

@@ -14,7 +14,9 @@
 // runs on integer keys in two passes: a 256-bin histogram of the key's high 8
 // bits finds the bin that holds rank r, a 128-bin histogram of the low 7 bits
 // of the keys in that bin finds the key.  Exact: the result is one of the
-// group's own values.
+// group's own values.  Each pass splits the rows over about four waves of
+// CTAs; a CTA counts in shared memory and adds its counts to a global
+// histogram (caller scratch), and one thread per group then walks the bins.
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
@@ -28,125 +30,151 @@ namespace {
 constexpr int SEL_THREADS = 256;
 constexpr int SEL_WARPS = SEL_THREADS / 32;
 constexpr int SEL_TILE = 32;   // groups per CTA when each row holds one element of a group
-constexpr int SEL_BINS = 256;  // first pass; the second uses 128
+constexpr int SEL_BINS = 256;  // first pass (key bits 14..7); the second uses 128 (bits 6..0)
+constexpr int SEL_UNROLL = 8;  // rows in flight per warp
 
 __device__ __forceinline__ uint32_t mag_key(__half x) { return __half_as_ushort(x) & 0x7fffu; }
 
-// Smallest bin whose inclusive prefix count reaches r; returns it and the rank
-// left inside it.  Sequential over the bins (one thread per group).
-__device__ __forceinline__ int find_bin(const uint32_t* h, int nbins, uint32_t r, uint32_t* rem) {
-  uint32_t acc = 0;
-  for (int b = 0; b < nbins; ++b) {
-    if (acc + h[b] >= r) {
-      *rem = r - acc;
-      return b;
-    }
-    acc += h[b];
-  }
-  *rem = 1;  // not reached when r <= n
-  return nbins - 1;
-}
-
-// Column mode (group_width == 1): CTA = 32 consecutive groups; warp w reads
-// rows w, w+8, ...; lane i owns group g0+i, so a warp reads 32 neighbouring
-// elements of one row (64 contiguous bytes when group_stride == 1).  Each lane
-// writes only its own group's histogram row: no two lanes of a warp collide.
+// Histogram of one pass over one row chunk, added to the global histogram
+// G[group][bins].  Pass 0 counts key >> 7; pass 1 counts key & 127 of the keys
+// whose key >> 7 equals the group's first-pass bin b1[group].
+//
+// COLS (group_width == 1): CTA = 32 consecutive groups x one row chunk; warp w
+// takes rows w, w+8, ...; lane i owns group g0+i, so a warp reads 32
+// neighbouring elements of one row (64 contiguous bytes when group_stride == 1)
+// and each lane writes only its own group's histogram row.
+// Segments (group_width > 1): CTA = one group x one row chunk; lanes read along
+// the segment, warps take rows; per-warp histograms keep shared-memory atomics
+// off one hot row.
+template <bool COLS>
 __global__ void __launch_bounds__(SEL_THREADS)
-select_columns_kernel(const __half* __restrict__ x, int64_t n_rows, int64_t row_stride,
-                      int n_groups, int64_t group_stride, uint32_t rank, float* __restrict__ out) {
-  __shared__ uint32_t hist[SEL_TILE][SEL_BINS + 1];  // padded: lanes on one bin hit 32 banks
-  __shared__ int s_b1[SEL_TILE];
-  __shared__ uint32_t s_rem[SEL_TILE];
+select_hist_kernel(const __half* __restrict__ x, int64_t n_rows, int64_t row_stride,
+                   int n_groups, int64_t group_stride, int width, int64_t rows_per_cta, int pass,
+                   const int32_t* __restrict__ b1, uint32_t* __restrict__ G) {
+  constexpr int NH = COLS ? SEL_TILE : SEL_WARPS;
+  __shared__ uint32_t hist[NH][SEL_BINS + 1];  // padded: 32 lanes on one bin hit 32 banks
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = blockIdx.x * SEL_TILE + lane;
-  const bool live = g < n_groups;
-  const __half* col = x + (live ? (int64_t)g * group_stride : 0);
-
-  for (int i = tid; i < SEL_TILE * (SEL_BINS + 1); i += SEL_THREADS) (&hist[0][0])[i] = 0;
+  const int nbins = pass ? 128 : SEL_BINS;
+  const int64_t r0 = (int64_t)blockIdx.y * rows_per_cta;
+  const int64_t r1 = min(n_rows, r0 + rows_per_cta);
+  for (int i = tid; i < NH * (SEL_BINS + 1); i += SEL_THREADS) (&hist[0][0])[i] = 0;
   __syncthreads();
-  if (live)
-    for (int64_t r = warp; r < n_rows; r += SEL_WARPS)
-      atomicAdd(&hist[lane][mag_key(col[r * row_stride]) >> 7], 1u);
-  __syncthreads();
-  if (tid < SEL_TILE) s_b1[tid] = find_bin(hist[tid], SEL_BINS, rank, &s_rem[tid]);
-  __syncthreads();
-  for (int i = tid; i < SEL_TILE * (SEL_BINS + 1); i += SEL_THREADS) (&hist[0][0])[i] = 0;
-  __syncthreads();
-  if (live) {
-    const uint32_t b1 = (uint32_t)s_b1[lane];
-    for (int64_t r = warp; r < n_rows; r += SEL_WARPS) {
-      const uint32_t k = mag_key(col[r * row_stride]);
-      if ((k >> 7) == b1) atomicAdd(&hist[lane][k & 127u], 1u);
+  if (COLS) {
+    const int g = blockIdx.x * SEL_TILE + lane;
+    if (g < n_groups) {
+      const __half* col = x + (int64_t)g * group_stride;
+      const uint32_t want = pass ? (uint32_t)b1[g] : 0u;
+      uint32_t* h = hist[lane];
+      int64_t r = r0 + warp;
+      for (; r + (SEL_UNROLL - 1) * SEL_WARPS < r1; r += SEL_UNROLL * SEL_WARPS) {
+        uint32_t k[SEL_UNROLL];
+#pragma unroll
+        for (int u = 0; u < SEL_UNROLL; ++u) k[u] = mag_key(col[(r + u * SEL_WARPS) * row_stride]);
+#pragma unroll
+        for (int u = 0; u < SEL_UNROLL; ++u) {
+          if (!pass) atomicAdd(h + (k[u] >> 7), 1u);
+          else if ((k[u] >> 7) == want) atomicAdd(h + (k[u] & 127u), 1u);
+        }
+      }
+      for (; r < r1; r += SEL_WARPS) {
+        const uint32_t k = mag_key(col[r * row_stride]);
+        if (!pass) atomicAdd(h + (k >> 7), 1u);
+        else if ((k >> 7) == want) atomicAdd(h + (k & 127u), 1u);
+      }
     }
-  }
-  __syncthreads();
-  if (tid < SEL_TILE && blockIdx.x * SEL_TILE + tid < n_groups) {
-    uint32_t rem2;
-    const int b2 = find_bin(hist[tid], 128, s_rem[tid], &rem2);
-    out[blockIdx.x * SEL_TILE + tid] =
-        __half2float(__ushort_as_half((unsigned short)(((uint32_t)s_b1[tid] << 7) | b2)));
-  }
-}
-
-// Row-segment mode (group_width > 1): CTA = one group of n_rows segments of
-// group_width contiguous elements; lanes read along the segment, warps take
-// rows.  Per-warp histograms keep shared-memory atomics off one hot row.
-__global__ void __launch_bounds__(SEL_THREADS)
-select_segments_kernel(const __half* __restrict__ x, int64_t n_rows, int64_t row_stride,
-                       int64_t group_stride, int width, uint32_t rank, float* __restrict__ out) {
-  __shared__ uint32_t hist[SEL_WARPS][SEL_BINS];
-  __shared__ uint32_t tot[SEL_BINS];
-  __shared__ int s_b1;
-  __shared__ uint32_t s_rem;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const __half* base = x + (int64_t)blockIdx.x * group_stride;
-
-  for (int pass = 0; pass < 2; ++pass) {
-    for (int i = tid; i < SEL_WARPS * SEL_BINS; i += SEL_THREADS) (&hist[0][0])[i] = 0;
     __syncthreads();
-    const uint32_t b1 = pass ? (uint32_t)s_b1 : 0u;
-    for (int64_t r = warp; r < n_rows; r += SEL_WARPS) {
+    for (int i = tid; i < SEL_TILE * nbins; i += SEL_THREADS) {
+      const int gi = i / nbins, b = i % nbins, g = blockIdx.x * SEL_TILE + gi;
+      const uint32_t c = hist[gi][b];
+      if (c && g < n_groups) atomicAdd(G + (size_t)g * SEL_BINS + b, c);
+    }
+  } else {
+    const int g = blockIdx.x;
+    const __half* base = x + (int64_t)g * group_stride;
+    const uint32_t want = pass ? (uint32_t)b1[g] : 0u;
+    uint32_t* h = hist[warp];
+    for (int64_t r = r0 + warp; r < r1; r += SEL_WARPS) {
       const __half* row = base + r * row_stride;
       for (int i = lane; i < width; i += 32) {
         const uint32_t k = mag_key(row[i]);
-        if (pass == 0) atomicAdd(&hist[warp][k >> 7], 1u);
-        else if ((k >> 7) == b1) atomicAdd(&hist[warp][k & 127u], 1u);
+        if (!pass) atomicAdd(h + (k >> 7), 1u);
+        else if ((k >> 7) == want) atomicAdd(h + (k & 127u), 1u);
       }
     }
     __syncthreads();
-    for (int b = tid; b < SEL_BINS; b += SEL_THREADS) {
-      uint32_t s = 0;
+    for (int b = tid; b < nbins; b += SEL_THREADS) {
+      uint32_t c = 0;
 #pragma unroll
-      for (int w = 0; w < SEL_WARPS; ++w) s += hist[w][b];
-      tot[b] = s;
+      for (int w = 0; w < SEL_WARPS; ++w) c += hist[w][b];
+      if (c) atomicAdd(G + (size_t)g * SEL_BINS + b, c);
     }
-    __syncthreads();
-    if (tid == 0) {
-      if (pass == 0) {
-        s_b1 = find_bin(tot, SEL_BINS, rank, &s_rem);
-      } else {
-        uint32_t rem2;
-        const int b2 = find_bin(tot, 128, s_rem, &rem2);
-        out[blockIdx.x] =
-            __half2float(__ushort_as_half((unsigned short)(((uint32_t)s_b1 << 7) | b2)));
-      }
+  }
+}
+
+// One thread per group: the smallest bin whose inclusive prefix count reaches
+// the rank.  Pass 0 keeps that bin and the rank left inside it (and clears the
+// group's histogram for pass 1); pass 1 assembles the key and writes the value.
+__global__ void select_pick_kernel(uint32_t* __restrict__ G, int n_groups, int pass,
+                                   uint32_t rank, int32_t* __restrict__ b1,
+                                   uint32_t* __restrict__ rem, float* __restrict__ out) {
+  const int g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= n_groups) return;
+  uint32_t* h = G + (size_t)g * SEL_BINS;
+  const int nbins = pass ? 128 : SEL_BINS;
+  const uint32_t r = pass ? rem[g] : rank;
+  uint32_t acc = 0;
+  int bin = nbins - 1;
+  uint32_t left = 1;
+  for (int b = 0; b < nbins; ++b) {
+    if (acc + h[b] >= r) {
+      bin = b;
+      left = r - acc;
+      break;
     }
-    __syncthreads();
+    acc += h[b];
+  }
+  if (pass == 0) {
+    b1[g] = bin;
+    rem[g] = left;
+    for (int b = 0; b < SEL_BINS; ++b) h[b] = 0;
+  } else {
+    out[g] = __half2float(__ushort_as_half((unsigned short)(((uint32_t)b1[g] << 7) | bin)));
   }
 }
 
 }  // namespace
 
+size_t abs_percentile_scratch_bytes(int n_groups) {
+  return (size_t)n_groups * (SEL_BINS + 2) * 4;
+}
+
 cudaError_t launch_abs_percentile(const __half* x, int64_t n_rows, int64_t row_stride,
                                   int n_groups, int64_t group_stride, int width, uint32_t rank,
-                                  float* out, cudaStream_t s) {
-  if (width == 1)
-    select_columns_kernel<<<(n_groups + SEL_TILE - 1) / SEL_TILE, SEL_THREADS, 0, s>>>(
-        x, n_rows, row_stride, n_groups, group_stride, rank, out);
-  else
-    select_segments_kernel<<<n_groups, SEL_THREADS, 0, s>>>(x, n_rows, row_stride, group_stride,
-                                                            width, rank, out);
-  return cudaGetLastError();
+                                  float* out, void* scratch, int num_sm, cudaStream_t s) {
+  uint32_t* G = static_cast<uint32_t*>(scratch);
+  int32_t* b1 = reinterpret_cast<int32_t*>(G + (size_t)n_groups * SEL_BINS);
+  uint32_t* rem = reinterpret_cast<uint32_t*>(b1 + n_groups);
+  const bool cols = width == 1;
+  const int64_t units = cols ? (n_groups + SEL_TILE - 1) / SEL_TILE : n_groups;
+  // about four waves of CTAs, at least 64 rows each (a chunk's histogram flush
+  // costs about as much as reading 64 rows)
+  const int64_t want = std::max<int64_t>(1, (int64_t)4 * num_sm / units);
+  const int64_t chunks = std::max<int64_t>(1, std::min<int64_t>(
+      {want, (n_rows + 63) / 64, 65535}));
+  const int64_t per = (n_rows + chunks - 1) / chunks;
+  const dim3 grid((unsigned)units, (unsigned)((n_rows + per - 1) / per));
+  cudaError_t e = cudaMemsetAsync(G, 0, (size_t)n_groups * SEL_BINS * 4, s);
+  for (int pass = 0; pass < 2 && e == cudaSuccess; ++pass) {
+    if (cols)
+      select_hist_kernel<true><<<grid, SEL_THREADS, 0, s>>>(x, n_rows, row_stride, n_groups,
+                                                            group_stride, width, per, pass, b1, G);
+    else
+      select_hist_kernel<false><<<grid, SEL_THREADS, 0, s>>>(x, n_rows, row_stride, n_groups,
+                                                             group_stride, width, per, pass, b1, G);
+    select_pick_kernel<<<(n_groups + 127) / 128, 128, 0, s>>>(G, n_groups, pass, rank, b1, rem, out);
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 }  // namespace ekv
@@ -155,20 +183,32 @@ using namespace ekv;
 
 extern "C" {
 
+int ekv_abs_percentile_scratch_bytes(int32_t n_groups, int64_t* out) {
+  if (n_groups < 1 || !out) return EKV_EINVAL;
+  *out = (int64_t)abs_percentile_scratch_bytes(n_groups);
+  return EKV_OK;
+}
+
 int ekv_abs_percentile(const void* x, int64_t n_rows, int64_t row_stride, int32_t n_groups,
                        int64_t group_stride, int32_t group_width, double q, float* out,
-                       void* stream) {
-  if (!x || !out || n_rows < 1 || n_groups < 1 || group_width < 1 || row_stride < 0 ||
-      group_stride < 0 || !(q >= 0.0 && q <= 1.0))
+                       void* scratch, int64_t scratch_bytes, void* stream) {
+  if (!x || !out || !scratch || n_rows < 1 || n_groups < 1 || group_width < 1 ||
+      row_stride < 0 || group_stride < 0 || !(q >= 0.0 && q <= 1.0))
     return EKV_EINVAL;
   const int64_t n = n_rows * (int64_t)group_width;
   if (n_rows > (int64_t)1 << 31 || n >= (int64_t)1 << 32) return EKV_EINVAL;  // uint32 counts
-  if ((reinterpret_cast<uintptr_t>(x) & 1) || (reinterpret_cast<uintptr_t>(out) & 3))
+  if ((reinterpret_cast<uintptr_t>(x) & 1) || (reinterpret_cast<uintptr_t>(out) & 3) ||
+      (reinterpret_cast<uintptr_t>(scratch) & 3) ||
+      scratch_bytes < (int64_t)abs_percentile_scratch_bytes(n_groups))
     return EKV_EINVAL;
   int64_t r = (int64_t)std::ceil(q * (double)n);
   r = std::min<int64_t>(std::max<int64_t>(r, 1), n);
+  int dev = 0, num_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&num_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return EKV_ECUDA;
   return launch_abs_percentile(static_cast<const __half*>(x), n_rows, row_stride, n_groups,
-                               group_stride, group_width, (uint32_t)r, out,
+                               group_stride, group_width, (uint32_t)r, out, scratch, num_sm,
                                static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? EKV_OK
              : EKV_ECUDA;

@@ -75,7 +75,9 @@ _SIGS = {
     "ekv_set_clip": (ctypes.c_int, [_P, _I32, _P, _P, _P]),
     "ekv_get_clip": (ctypes.c_int, [_P, _I32, _P, _P, _P]),
     "ekv_abs_percentile": (ctypes.c_int, [_P, ctypes.c_int64, ctypes.c_int64, _I32,
-                                          ctypes.c_int64, _I32, ctypes.c_double, _P, _P]),
+                                          ctypes.c_int64, _I32, ctypes.c_double, _P, _P,
+                                          ctypes.c_int64, _P]),
+    "ekv_abs_percentile_scratch_bytes": (ctypes.c_int, [_I32, _P]),
     "ekv_autok": (ctypes.c_int, [_P, _I32, ctypes.c_double, _P, _P]),
 }
 EXPORTS = tuple(_SIGS)
@@ -326,9 +328,14 @@ def abs_percentile(x: torch.Tensor, q: float, n_rows: int, row_stride: int, n_gr
         raise TypeError("x must be a CUDA fp16 tensor")
     if out is None:
         out = torch.empty(n_groups, dtype=torch.float32, device=x.device)
+    nb = ctypes.c_int64(0)
+    if n_groups >= 1:
+        _check(lib().ekv_abs_percentile_scratch_bytes(n_groups, ctypes.byref(nb)),
+               "ekv_abs_percentile_scratch_bytes")
+    scratch = torch.empty(max(4, nb.value) // 4, dtype=torch.int32, device=x.device)
     _check(lib().ekv_abs_percentile(_ptr(x), n_rows, row_stride, n_groups, group_stride,
-                                    group_width, float(q), _ptr(out), _stream(stream)),
-           "ekv_abs_percentile")
+                                    group_width, float(q), _ptr(out), _ptr(scratch), nb.value,
+                                    _stream(stream)), "ekv_abs_percentile")
     return out
 
 
