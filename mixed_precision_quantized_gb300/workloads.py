@@ -46,6 +46,7 @@ class Workload:
     outlier_fixed: tuple | None = None
     layer_slope: float = 0.0
     seed: int = 0
+    asym: bool = False           # KIVI-style asymmetric quantizer (K, V and canary)
 
     @property
     def group(self) -> int:

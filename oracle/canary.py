@@ -31,16 +31,21 @@ GROUP = 16
 RING = 64
 
 
-def window_dequant(w16: np.ndarray, b: int, clip=None) -> np.ndarray:
+def window_dequant(w16: np.ndarray, b: int, clip=None, asym: bool = False) -> np.ndarray:
     """quant_b then dequant of a window [n, d] fp16, per channel over 16-row
-    groups (clip: the head's per-channel thresholds [d], or None)."""
+    groups (clip: the head's per-channel thresholds [d], or None; asym: the
+    KIVI-style asymmetric quantizer the page names for quant_b)."""
     w16 = np.asarray(w16, dtype=np.float16)
     n = w16.shape[0]
     out = np.zeros(w16.shape, dtype=np.float32)
     for g0 in range(0, n, GROUP):
         grp = w16[g0:g0 + GROUP]
-        q, s = quant.quantize(grp, b, axis=0, clip=clip)
-        out[g0:g0 + GROUP] = quant.dequantize(q, s, axis=0)
+        if asym:
+            u, s, z = quant.quantize_asym(grp, b, axis=0)
+            out[g0:g0 + GROUP] = quant.dequantize_asym(u, s, z, axis=0)
+        else:
+            q, s = quant.quantize(grp, b, axis=0, clip=clip)
+            out[g0:g0 + GROUP] = quant.dequantize(q, s, axis=0)
     return out
 
 
@@ -50,19 +55,20 @@ def _log_softmax(z: np.ndarray) -> np.ndarray:
 
 
 def kl_per_query(q16: np.ndarray, w16: np.ndarray, b: int, scale: float | None = None,
-                 clip=None) -> np.ndarray:
+                 clip=None, asym: bool = False) -> np.ndarray:
     """KL(p || p_hat_b) for each query row of q16 [G, d] against window w16 [n, d]."""
     q = np.asarray(q16).astype(np.float64)
     d = q.shape[-1]
     sigma = 1.0 / np.sqrt(d) if scale is None else float(scale)
     w = np.asarray(w16, dtype=np.float16).astype(np.float64)
-    wq = window_dequant(w16, b, clip).astype(np.float64)
+    wq = window_dequant(w16, b, clip, asym).astype(np.float64)
     lp = _log_softmax(sigma * (q @ w.T))
     lph = _log_softmax(sigma * (q @ wq.T))
     return (np.exp(lp) * (lp - lph)).sum(axis=-1)
 
 
-def layer_delta(Q16: np.ndarray, windows, scale: float | None = None, clip=None) -> np.ndarray:
+def layer_delta(Q16: np.ndarray, windows, scale: float | None = None, clip=None,
+                asym: bool = False) -> np.ndarray:
     """delta[b] for one layer: Q16 [B, Hq, d], windows[s] = [Hkv, n_s, d] -> fp64 [3].
 
     clip: the layer's K thresholds [Hkv, d] (the cache's quantizer), or None.
@@ -78,5 +84,5 @@ def layer_delta(Q16: np.ndarray, windows, scale: float | None = None, clip=None)
         for g in range(Hkv):
             for i, b in enumerate(BITS):
                 tot[i] += kl_per_query(Q16[s, g * G:(g + 1) * G], windows[s][g], b, scale,
-                                       None if clip is None else clip[g]).sum()
+                                       None if clip is None else clip[g], asym).sum()
     return tot / (B * Hq)

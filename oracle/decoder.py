@@ -41,8 +41,10 @@ class SeqState:
     change once written).
     """
 
-    def __init__(self, n_heads: int, d: int, vbits: int, kclip=None, vclip=None):
+    def __init__(self, n_heads: int, d: int, vbits: int, kclip=None, vclip=None,
+                 asym: bool = False):
         self.H, self.d = n_heads, d
+        self.asym = asym           # KIVI-style asymmetric quantizer for K and V
         self.kclip = kclip         # [H, d] fp32 K thresholds or None
         self.vclip = vclip         # [H] fp32 V thresholds or None
         self._k = np.zeros((0, n_heads, d), dtype=np.float16)
@@ -100,6 +102,9 @@ class SeqState:
             kb = self.kbits[j]
             if kb == 16:
                 self._kh[lo:hi] = self._k[lo:hi].astype(np.float32)
+            elif self.asym:
+                u, s, z = quant.quantize_asym(self._k[lo:hi], kb, axis=0)
+                self._kh[lo:hi] = quant.dequantize_asym(u, s, z, axis=0)
             else:
                 q, s = quant.quantize(self._k[lo:hi], kb, axis=0, clip=self.kclip)
                 self._kh[lo:hi] = quant.dequantize(q, s, axis=0)
@@ -114,6 +119,9 @@ class SeqState:
         if T > lo:
             if self.vbits == 16:
                 self._vh[lo:T] = self._v[lo:T].astype(np.float32)
+            elif self.asym:
+                u, s, z = quant.quantize_asym(self._v[lo:T], self.vbits, axis=2)
+                self._vh[lo:T] = quant.dequantize_asym(u, s, z, axis=2)
             else:
                 q, s = quant.quantize(self._v[lo:T], self.vbits, axis=2, clip=self.vclip)
                 self._vh[lo:T] = quant.dequantize(q, s, axis=2)
@@ -132,9 +140,10 @@ class SeqState:
         exp = {}
         if hi - lo == BLOCK:
             exp.update(pages.sealed_k_bytes(kb, self._k[lo:hi, h],
-                                            None if self.kclip is None else self.kclip[h]))
+                                            None if self.kclip is None else self.kclip[h],
+                                            self.asym))
         exp.update(pages.v_rows_bytes(self.vbits, self._v[lo:hi, h],
-                                      None if self.vclip is None else self.vclip[h]))
+                                      None if self.vclip is None else self.vclip[h], self.asym))
         return exp
 
 
@@ -179,7 +188,8 @@ def controller_trace(w, n_steps: int, device="cpu", clips=None) -> Trace:
         for l in range(w.num_layers):
             Q = w.step_q(l, t, 1, device=device)[:, 0].cpu().numpy()
             kc = None if not clips or l not in clips else clips[l][0]
-            deltas[l] = canary.layer_delta(Q, layer_windows(w, l, t, device), clip=kc)
+            deltas[l] = canary.layer_delta(Q, layer_windows(w, l, t, device), clip=kc,
+                                           asym=getattr(w, "asym", False))
         tr.delta[t] = deltas
         ctl.update(deltas.astype(np.float32))
         tr.ema[t] = np.array(ctl.ema, dtype=np.float32)
@@ -207,7 +217,7 @@ class ReferenceRun:
         sel = lambda l, i: (None if l not in clips or clips[l][i] is None
                             else np.asarray(clips[l][i], dtype=np.float32)[self.heads])
         self.state = {(l, s): SeqState(len(self.heads), w.head_dim, w.v_bits[l],
-                                       sel(l, 0), sel(l, 1))
+                                       sel(l, 0), sel(l, 1), getattr(w, "asym", False))
                       for l in self.layers for s in self.seqs}
         self.steps_done = 0
 

@@ -16,6 +16,11 @@ Layout (our storage reading; the pages only say "packed low-bit storage"):
             vb = 16 : raw fp16 [16][d]
     page  = K part || V part            (little-endian fp16)
 
+A cache built with the KIVI-style asymmetric quantizer stores unsigned codes u
+and adds each group's fp16 zero point right after the scales: K zero points
+[d] (same order as the K scales) after the K scales, V zero points [16] after
+the V scales.  16-bit parts are unchanged.
+
 The K scales of 2- and 4-bit pages are stored in "pair order": within each
 group of n = 32/kb channels (the channels of one 32-bit code word), scale
 position p holds channel p // 2 + (p % 2) * n / 2, i.e. 0, n/2, 1, n/2+1, ...
@@ -31,19 +36,19 @@ from . import quant
 BLOCK = 16
 
 
-def k_part_bytes(kb: int, d: int) -> int:
-    return BLOCK * d * 2 if kb == 16 else BLOCK * d * kb // 8 + 2 * d
+def k_part_bytes(kb: int, d: int, asym: bool = False) -> int:
+    return BLOCK * d * 2 if kb == 16 else BLOCK * d * kb // 8 + 2 * d * (2 if asym else 1)
 
 
-def v_part_bytes(vb: int, d: int) -> int:
-    return BLOCK * d * 2 if vb == 16 else BLOCK * d * vb // 8 + 2 * BLOCK
+def v_part_bytes(vb: int, d: int, asym: bool = False) -> int:
+    return BLOCK * d * 2 if vb == 16 else BLOCK * d * vb // 8 + 2 * BLOCK * (2 if asym else 1)
 
 
-def page_bytes(kb: int, vb: int, d: int) -> int:
-    return k_part_bytes(kb, d) + v_part_bytes(vb, d)
+def page_bytes(kb: int, vb: int, d: int, asym: bool = False) -> int:
+    return k_part_bytes(kb, d, asym) + v_part_bytes(vb, d, asym)
 
 
-def regions(kb: int, vb: int, d: int) -> dict:
+def regions(kb: int, vb: int, d: int, asym: bool = False) -> dict:
     """name -> (offset, row_bytes, rows) of each region of the page."""
     r = {}
     if kb == 16:
@@ -51,12 +56,16 @@ def regions(kb: int, vb: int, d: int) -> dict:
     else:
         r["k_codes"] = (0, d * kb // 8, BLOCK)
         r["k_scales"] = (BLOCK * d * kb // 8, 2 * d, 1)
-    o = k_part_bytes(kb, d)
+        if asym:
+            r["k_zeros"] = (BLOCK * d * kb // 8 + 2 * d, 2 * d, 1)
+    o = k_part_bytes(kb, d, asym)
     if vb == 16:
         r["v_raw"] = (o, 2 * d, BLOCK)
     else:
         r["v_codes"] = (o, d * vb // 8, BLOCK)
         r["v_scales"] = (o + BLOCK * d * vb // 8, 2, BLOCK)
+        if asym:
+            r["v_zeros"] = (o + BLOCK * d * vb // 8 + 2 * BLOCK, 2, BLOCK)
     return r
 
 
@@ -69,24 +78,39 @@ def scale_order(kb: int, d: int) -> np.ndarray:
     return (p // n) * n + (p % n) // 2 + (p % 2) * (n // 2)
 
 
-def sealed_k_bytes(kb: int, k16: np.ndarray, clip=None) -> dict:
+def sealed_k_bytes(kb: int, k16: np.ndarray, clip=None, asym: bool = False) -> dict:
     """Expected bytes of a full page's K part from its 16 raw fp16 rows [16, d]
-    (clip: per-channel thresholds [d] or None)."""
+    (clip: per-channel thresholds [d] or None; asym: the asymmetric quantizer)."""
     k16 = np.asarray(k16, dtype=np.float16)
     assert k16.shape[0] == BLOCK
     if kb == 16:
         return {"k_raw": k16.view(np.uint8).reshape(BLOCK, -1)}
+    if asym:
+        if clip is not None:
+            raise ValueError("clipping thresholds apply to the symmetric quantizer only")
+        u, s, z = quant.quantize_asym(k16, kb, axis=0)
+        order = scale_order(kb, k16.shape[1])
+        return {"k_codes": quant.pack_unsigned(u, kb),
+                "k_scales": s[order].astype(np.float16).view(np.uint8)[None, :],
+                "k_zeros": z[order].astype(np.float16).view(np.uint8)[None, :]}
     q, s = quant.quantize(k16, kb, axis=0, clip=clip)   # one group per channel
     s = s[scale_order(kb, k16.shape[1])]
     return {"k_codes": quant.pack(q, kb), "k_scales": s.astype(np.float16).view(np.uint8)[None, :]}
 
 
-def v_rows_bytes(vb: int, v16: np.ndarray, clip=None) -> dict:
+def v_rows_bytes(vb: int, v16: np.ndarray, clip=None, asym: bool = False) -> dict:
     """Expected bytes of V rows [n, d] (rows 0..n-1 of the page; clip: the
-    head's threshold or None)."""
+    head's threshold or None; asym: the asymmetric quantizer)."""
     v16 = np.asarray(v16, dtype=np.float16)
     if vb == 16:
         return {"v_raw": v16.view(np.uint8).reshape(v16.shape[0], -1)}
+    if asym:
+        if clip is not None:
+            raise ValueError("clipping thresholds apply to the symmetric quantizer only")
+        u, s, z = quant.quantize_asym(v16, vb, axis=1)
+        return {"v_codes": quant.pack_unsigned(u, vb),
+                "v_scales": s.astype(np.float16).view(np.uint8).reshape(-1, 2),
+                "v_zeros": z.astype(np.float16).view(np.uint8).reshape(-1, 2)}
     q, s = quant.quantize(v16, vb, axis=1, clip=clip)   # one group per token
     return {"v_codes": quant.pack(q, vb),
             "v_scales": s.astype(np.float16).view(np.uint8).reshape(-1, 2)}

@@ -74,6 +74,57 @@ def dequantize(q: np.ndarray, s16: np.ndarray, axis: int) -> np.ndarray:
     return (q.astype(F32) * s).astype(F32)
 
 
+def levels(b: int) -> int:
+    if b not in (2, 4, 8):
+        raise ValueError(f"no integer quantizer for {b} bits")
+    return (1 << b) - 1
+
+
+def quantize_asym(x16: np.ndarray, b: int, axis: int):
+    """KIVI-style asymmetric b-bit quantization of fp16 `x16` in groups along
+    `axis` -> (u int16 in [0, 2^b - 1], s fp16, z fp16), `axis` removed.
+
+    Follows "EchoKV: watching a language model decide its own precision",
+    "Show the math" (quant_b is KIVI-style asymmetric per-group quantization,
+    whose per-group scale is a function of the group's max and min, "Bidirectional
+    adjustment"), and the page's per-token KIVI INT2/4/8 cache storage
+    ("Upstreaming into vLLM").  Reading (the page gives no formula):
+
+        lo, hi = min x_i, max x_i              (exact on fp16 values)
+        s  = fp16_rne( fp32(fp32(hi - lo) / fp32(2^b - 1)) )   the stored scale
+        z  = lo                                the stored zero point (fp16, exact)
+        u_i = clamp( rne( fp32(fp32(x_i - z) / fp32(s)) ), 0, 2^b - 1 ),  u = 0 if s == 0
+        xhat = fp32( fp32(u) * fp32(s) + fp32(z) )   (the product is exact)
+    """
+    x16 = np.asarray(x16)
+    if x16.dtype != F16:
+        raise TypeError("quantizer input must be fp16")
+    x = x16.astype(F32)
+    lv = F32(levels(b))
+    lo = np.min(x, axis=axis, keepdims=True)
+    hi = np.max(x, axis=axis, keepdims=True)
+    s16 = ((hi - lo).astype(F32) / lv).astype(F32).astype(F16)
+    sf = s16.astype(F32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = ((x - lo).astype(F32) / sf).astype(F32)
+    u = np.clip(np.rint(r), F32(0), lv)
+    u = np.where(sf == 0, F32(0), u)
+    return (u.astype(np.int16), np.squeeze(s16, axis=axis),
+            np.squeeze(lo.astype(F16), axis=axis))
+
+
+def dequantize_asym(u: np.ndarray, s16: np.ndarray, z16: np.ndarray, axis: int) -> np.ndarray:
+    """xhat = fp32(u) * fp32(s) + fp32(z), `s16` and `z16` broadcast along `axis`."""
+    s = np.expand_dims(np.asarray(s16, dtype=F16).astype(F32), axis)
+    z = np.expand_dims(np.asarray(z16, dtype=F16).astype(F32), axis)
+    return ((u.astype(F32) * s).astype(F32) + z).astype(F32)
+
+
+def pack_unsigned(u: np.ndarray, b: int) -> np.ndarray:
+    """Pack unsigned codes u in [0, 2^b - 1] (stored as they are, LSB first)."""
+    return pack(np.asarray(u, dtype=np.int64) - (1 << (b - 1)), b)
+
+
 def pack(q: np.ndarray, b: int) -> np.ndarray:
     """Pack int codes along the last axis, offset binary, LSB first -> uint8."""
     q = np.asarray(q, dtype=np.int64)
