@@ -73,6 +73,8 @@ def parse():
                         "the workload's first --calib-tokens prefill tokens, load them, and "
                         "time the same step with the canary off")
     p.add_argument("--calib-tokens", type=int, default=8192)
+    p.add_argument("--asym", action="store_true",
+                   help="KIVI-style asymmetric quantizer for the pages and the canary")
     p.add_argument("--separate", action="store_true",
                    help="append and attention as two launches per layer (default: one fused launch)")
     return p.parse_args()
@@ -81,7 +83,7 @@ def parse():
 def attn_source_sha() -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in ("ekv_attn.cu", "ekv_internal.h", "ekv_quant.cuh"):
+    for f in ("ekv_attn.cu", "ekv_attn_body.cuh", "ekv_internal.h", "ekv_quant.cuh"):
         with open(os.path.join(ROOT, "mixed_precision_quantized_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -160,10 +162,10 @@ def attn_bytes_per_layer(cache, w, layer: int) -> float:
                 fmt = (e >> 28) & 15
                 kb = 2 << (fmt >> 2)
                 if nopen and j == len(bt) - 1:
-                    vrow = d * 2 if vb == 16 else d * vb // 8 + 2
+                    vrow = d * 2 if vb == 16 else d * vb // 8 + (4 if w.asym else 2)
                     total += nopen * (2 * d + vrow)       # open rows: fp16 K + V row
                 else:
-                    total += ekv.page_bytes(kb, vb, d)
+                    total += ekv.page_bytes(kb, vb, d, w.asym)
                 total += 4                                  # page-table entry
         total += 2 * Hq * d * 2                             # Q in, O out
     return total
@@ -213,6 +215,10 @@ def main():
     w = replicas.shard(workloads.by_name(a.workload), rank)
     if a.layers:
         w = w.scaled(num_layers=a.layers)
+    if a.asym:
+        if a.static:
+            raise SystemExit("the static artifact's thresholds cap the symmetric quantizer")
+        w = w.scaled(asym=True)
 
     if a.impl == "reference":
         if rank != 0:
@@ -548,7 +554,8 @@ def main():
                                + (f"tokens, K tier by canary every {w.canary_period} steps "
                                   f"(tau {w.tau}), " if static is None else
                                   "tokens, K bits per layer from the static artifact, ")
-                               + f"V INT{w.v_bits[0]}",
+                               + f"V INT{w.v_bits[0]}"
+                               + (", KIVI-style asymmetric quantizer" if w.asym else ""),
                    "l2": (f"inputs larger than L2: {step_bytes / 1e9:.2f} GB of pages read per step"
                           if NR == 1 else
                           f"steps rotate over {NR} caches of {step_bytes / 1e9:.3f} GB of pages "
@@ -570,6 +577,7 @@ def main():
                      "frac": achieved / peak if achieved else None,
                      "traffic": (TRAFFIC_BYTES if attn_source_sha() == TRAFFIC_SOURCE_SHA
                                  and w.name == "llama70b_128k" and not a.layers and fused
+                                 and not a.asym and not a.static
                                  else None),
                      "traffic_unit": "bytes per launch",
                      "kernel": ("decode_attn_kernel (fused append + attention)" if fused

@@ -94,6 +94,17 @@ typedef struct ekv_config {
                               needs ema_b < budget * (1 - hysteresis)                */
   int32_t vote;            /* >= 2: a tier changes only after that many consecutive
                               firings picked the same new tier                      */
+  /* Quantizer of every page and of the canary: EKV_QUANT_SYMMETRIC (0, the
+   * default) or EKV_QUANT_ASYMMETRIC (1, KIVI-style: "EchoKV: watching a
+   * language model decide its own precision", "Show the math" names it for the
+   * canary and "Upstreaming into vLLM" for the cache).  Per group (K: a
+   * channel over a block's 16 tokens, V: a token's d channels; the canary: a
+   * channel over a 16-row group of the ring): lo, hi = min, max;
+   * s = fp16_rne((hi - lo) / (2^b - 1)) (fp32 subtraction and division);
+   * z = lo; u = clamp(rne((x - z) / s), 0, 2^b - 1) (0 if s = 0); the value
+   * read back is u * s + z.  Codes are stored unsigned; each quantized part
+   * adds one fp16 zero point per group after its scales. */
+  int32_t quantizer;
   /* Device allocator.  NULL -> cudaMalloc/cudaFree.  Called only inside
    * ekv_create/ekv_destroy; must return 16-byte aligned memory (else
    * ekv_create fails with EKV_ENOMEM). */
@@ -101,6 +112,9 @@ typedef struct ekv_config {
   void (*dev_free)(void* ptr, void* ctx);
   void* alloc_ctx;
 } ekv_config;
+
+#define EKV_QUANT_SYMMETRIC 0
+#define EKV_QUANT_ASYMMETRIC 1
 
 /* Human-readable name of a status code (static string, never NULL). */
 EKV_API const char* ekv_status_string(int status);
@@ -114,6 +128,11 @@ EKV_API const char* ekv_status_string(int status);
  * Codes are offset binary (q + 2^(b-1)), packed along channels, least
  * significant bits first: channel c sits in byte c*b/8 at bit (c*b)%8. */
 EKV_API int32_t ekv_page_bytes(int32_t k_bits, int32_t v_bits, int32_t head_dim);
+/* The same for a quantizer (EKV_QUANT_*): the asymmetric one adds a zero-point
+ * row after each quantized part's scales (K: [d] fp16, same order as the K
+ * scales; V: [16] fp16).  -1 for an invalid argument. */
+EKV_API int32_t ekv_page_bytes_q(int32_t k_bits, int32_t v_bits, int32_t head_dim,
+                                 int32_t quantizer);
 
 /* Create a cache.  k_bits_init[num_layers] (host): each layer's starting K tier
  * (2, 4, 8 or 16).  v_bits[num_layers] (host): each layer's fixed V width.
@@ -252,7 +271,7 @@ EKV_API int ekv_set_tiers(ekv_cache* cache, const uint8_t* tiers, void* stream);
  * to +-qmax, so values beyond c take the end codes).  The canary quantizes the
  * ring with the same K thresholds.  NULL = no clipping (+inf) for that part;
  * every threshold must be > 0 (+inf allowed), else EKV_EINVAL and nothing
- * changes.  New thresholds govern pages sealed and V rows written afterwards;
+ * changes.  A handle with the asymmetric quantizer returns EKV_EUNSUPPORTED.  New thresholds govern pages sealed and V rows written afterwards;
  * pages already written keep their bytes.  A new handle has no clipping. */
 EKV_API int ekv_set_clip(ekv_cache* cache, int32_t layer, const float* k_clip,
                          const float* v_clip, void* stream);

@@ -80,13 +80,19 @@ append_kernel(DevState st, int layer, const int32_t* __restrict__ slots, int n_n
       const int fmt = entry_fmt(e);
       const int kb = bits_of_code(fmt >> 2), vb = bits_of_code(fmt & 3);
       uint8_t* page = st.pool_base[fmt] + (size_t)entry_idx(e) * st.pool_page_bytes[fmt];
-      uint8_t* vpart = page + k_part_bytes(kb, D);
+      uint8_t* vpart = page + k_part_bytes(kb, D, st.asym);
       const size_t lh = (size_t)layer * st.Hkv + h;
       const float vc = st.vclip[lh];
-      for (int p = lo + warp; p < hi; p += NWARP)
-        quant_v_row<D>(vin + (size_t)(p - told) * in_row, vpart, p - j * BLOCK, vb, lane, vc);
+      for (int p = lo + warp; p < hi; p += NWARP) {
+        const __half* src = vin + (size_t)(p - told) * in_row;
+        if (st.asym) quant_v_row<D, true>(src, vpart, p - j * BLOCK, vb, lane, vc);
+        else quant_v_row<D, false>(src, vpart, p - j * BLOCK, vb, lane, vc);
+      }
       if (hi == j * BLOCK + BLOCK) {
-        if (tid < CH) seal_k<D>(stg, kin, in_row, j, told, kb, page, tid, st.kclip + lh * D);
+        if (tid < CH) {
+          if (st.asym) seal_k<D, true>(stg, kin, in_row, j, told, kb, page, tid, st.kclip + lh * D);
+          else seal_k<D, false>(stg, kin, in_row, j, told, kb, page, tid, st.kclip + lh * D);
+        }
       } else {
         for (int i = tid; i < (hi - lo) * CH; i += APPEND_THREADS) {
           const int p = lo + i / CH, cc = i % CH;

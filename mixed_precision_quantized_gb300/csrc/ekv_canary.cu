@@ -76,6 +76,24 @@ canary_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   for (int i = tid; i < ngr * D; i += CANARY_THREADS) {
     const int gi = i / D, c = i % D;
     const int r0 = gi * 16, r1 = min(r0 + 16, n);
+    if (st.asym) {  // KIVI-style: min/max scale, zero point lo, unsigned codes
+      float lo = CUDART_INF_F, hi = -CUDART_INF_F;
+      for (int r = r0; r < r1; ++r) {
+        lo = fminf(lo, W[r * P + c]);
+        hi = fmaxf(hi, W[r * P + c]);
+      }
+#pragma unroll
+      for (int bi = 0; bi < NBITS; ++bi) {
+        const int L = (1 << (2 << bi)) - 1;
+        const float sf = __half2float(__float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), (float)L)));
+        for (int r = r0; r < r1; ++r) {
+          const float x = W[r * P + c];
+          const int u = sf == 0.f ? 0 : min(max(__float2int_rn(__fdiv_rn(__fsub_rn(x, lo), sf)), 0), L);
+          WQ[(bi * RING + r) * P + c] = __fadd_rn(__fmul_rn((float)u, sf), lo);
+        }
+      }
+      continue;
+    }
     float m = 0.f;
     for (int r = r0; r < r1; ++r) m = fmaxf(m, fabsf(W[r * P + c]));
     m = fminf(m, st.kclip[((size_t)layer * st.Hkv + h) * D + c]);  // the cache's own quantizer

@@ -91,8 +91,14 @@ const char* ekv_status_string(int status) {
 }
 
 int32_t ekv_page_bytes(int32_t k_bits, int32_t v_bits, int32_t head_dim) {
-  if (!valid_bits(k_bits) || !valid_bits(v_bits) || (head_dim != 64 && head_dim != 128)) return -1;
-  return page_bytes(k_bits, v_bits, head_dim);
+  return ekv_page_bytes_q(k_bits, v_bits, head_dim, EKV_QUANT_SYMMETRIC);
+}
+
+int32_t ekv_page_bytes_q(int32_t k_bits, int32_t v_bits, int32_t head_dim, int32_t quantizer) {
+  if (!valid_bits(k_bits) || !valid_bits(v_bits) || (head_dim != 64 && head_dim != 128) ||
+      (quantizer != EKV_QUANT_SYMMETRIC && quantizer != EKV_QUANT_ASYMMETRIC))
+    return -1;
+  return page_bytes(k_bits, v_bits, head_dim, quantizer == EKV_QUANT_ASYMMETRIC);
 }
 
 int ekv_create(const ekv_config* cfg, const uint8_t* k_bits_init, const uint8_t* v_bits,
@@ -109,6 +115,8 @@ int ekv_create(const ekv_config* cfg, const uint8_t* k_bits_init, const uint8_t*
   if ((k.dev_alloc == nullptr) != (k.dev_free == nullptr)) return EKV_EINVAL;
   if (!(k.ema_alpha >= 0.f && k.ema_alpha <= 1.f)) return EKV_EINVAL;
   if (k.tau_ctx0 < 0 || !(k.hysteresis >= 0.f && k.hysteresis < 1.f) || k.vote < 0)
+    return EKV_EINVAL;
+  if (k.quantizer != EKV_QUANT_SYMMETRIC && k.quantizer != EKV_QUANT_ASYMMETRIC)
     return EKV_EINVAL;
   for (int l = 0; l < k.num_layers; ++l)
     if (!valid_bits(k_bits_init[l]) || !valid_bits(v_bits[l])) return EKV_EINVAL;
@@ -134,6 +142,7 @@ int ekv_create(const ekv_config* cfg, const uint8_t* k_bits_init, const uint8_t*
   st.tau_ctx0 = k.tau_ctx0;
   st.hyst = k.hysteresis;
   st.vote = k.vote < 1 ? 1 : k.vote;
+  st.asym = k.quantizer == EKV_QUANT_ASYMMETRIC;
   c->vbits.assign(v_bits, v_bits + k.num_layers);
 
   int dev = 0;
@@ -153,7 +162,7 @@ int ekv_create(const ekv_config* cfg, const uint8_t* k_bits_init, const uint8_t*
   };
   for (int f = 0; f < NFMT; ++f) {
     const int kb = bits_of_code(f >> 2), vb = bits_of_code(f & 3);
-    st.pool_page_bytes[f] = page_bytes(kb, vb, st.D);
+    st.pool_page_bytes[f] = page_bytes(kb, vb, st.D, st.asym);
     st.pool_cap[f] = (int32_t)k.pool_pages[f];
     if (k.pool_pages[f] > 0) {
       st.pool_base[f] = (uint8_t*)A((size_t)k.pool_pages[f] * st.pool_page_bytes[f]);
@@ -328,6 +337,7 @@ int ekv_set_tiers(ekv_cache* c, const uint8_t* tiers, void* stream) {
 int ekv_set_clip(ekv_cache* c, int32_t layer, const float* k_clip, const float* v_clip,
                  void* stream) {
   if (!c || layer < 0 || layer >= c->st.L) return EKV_EINVAL;
+  if (c->st.asym) return EKV_EUNSUPPORTED;  // thresholds cap the symmetric quantizer's absmax
   const int H = c->st.Hkv, D = c->st.D;
   std::vector<float> kc((size_t)H * D, INFINITY), vc(H, INFINITY);
   auto take = [](const float* src, std::vector<float>& dst) {
@@ -420,7 +430,7 @@ int ekv_read_pages(ekv_cache* c, int32_t layer, int32_t seq_slot, int32_t kv_hea
       first_block + n_blocks > c->st.maxblk || (dst_stride & 15) || ((uintptr_t)dst & 15))
     return EKV_EINVAL;
   const int vb = c->vbits[layer];
-  if ((int64_t)dst_stride < page_bytes(16, vb, c->st.D)) return EKV_EINVAL;
+  if ((int64_t)dst_stride < page_bytes(16, vb, c->st.D, c->st.asym)) return EKV_EINVAL;
   if (n_blocks == 0) return EKV_OK;
   return cuda_status(launch_read_pages(c->st, layer, seq_slot, kv_head, first_block, n_blocks,
                                        static_cast<uint8_t*>(dst), dst_stride, as_stream(stream)));

@@ -23,14 +23,16 @@ __host__ __device__ inline int bits_of_code(int code) { return 2 << code; }
 __host__ __device__ inline int code_of_bits(int b) {
   return b == 2 ? 0 : b == 4 ? 1 : b == 8 ? 2 : b == 16 ? 3 : -1;
 }
-__host__ __device__ constexpr int k_part_bytes(int kb, int d) {
-  return kb == 16 ? BLOCK * d * 2 : BLOCK * d * kb / 8 + 2 * d;
+// Page parts.  Quantized parts hold codes, then one fp16 scale per group, then
+// (asymmetric quantizer only) one fp16 zero point per group.
+__host__ __device__ constexpr int k_part_bytes(int kb, int d, bool asym = false) {
+  return kb == 16 ? BLOCK * d * 2 : BLOCK * d * kb / 8 + 2 * d * (asym ? 2 : 1);
 }
-__host__ __device__ constexpr int v_part_bytes(int vb, int d) {
-  return vb == 16 ? BLOCK * d * 2 : BLOCK * d * vb / 8 + 2 * BLOCK;
+__host__ __device__ constexpr int v_part_bytes(int vb, int d, bool asym = false) {
+  return vb == 16 ? BLOCK * d * 2 : BLOCK * d * vb / 8 + 2 * BLOCK * (asym ? 2 : 1);
 }
-__host__ __device__ constexpr int page_bytes(int kb, int vb, int d) {
-  return k_part_bytes(kb, d) + v_part_bytes(vb, d);
+__host__ __device__ constexpr int page_bytes(int kb, int vb, int d, bool asym = false) {
+  return k_part_bytes(kb, d, asym) + v_part_bytes(vb, d, asym);
 }
 
 // Page entry: (format << 28) | index, -1 = none.  Formats >= 8 make the int32
@@ -47,6 +49,7 @@ struct DevState {
   int tau_ctx0;      // > 0: budget scales with sqrt(mean length / tau_ctx0)
   float hyst;        // demotion margin
   int vote;          // consecutive firings a new tier needs (>= 1)
+  int asym;          // 1: KIVI-style asymmetric quantizer (pages and canary)
   uint8_t* pool_base[NFMT];
   int32_t pool_page_bytes[NFMT];
   int32_t pool_cap[NFMT];
@@ -89,6 +92,8 @@ __host__ __device__ inline size_t lsh_index(const DevState& st, int l, int s, in
 cudaError_t launch_append(const DevState& st, int layer, int n_seqs, const int32_t* slots,
                           int n_new, const __half* k, const __half* v, cudaStream_t s);
 cudaError_t attn_init();   // once per process, before any launch
+cudaError_t attn_init_sym();
+cudaError_t attn_init_asym();
 int attn_ctas_per_sm(int vb);  // resident decode-attention CTAs per SM for V width vb
 // With knew/vnew set ([n_seqs][Hkv][d] fp16 each) the launch first appends that
 // one token to every sequence (the fused decode step), then attends over it too;
@@ -98,6 +103,15 @@ cudaError_t launch_decode_attn(const DevState& st, int layer, int n_seqs, const 
                                const __half* q, __half* o, int splits, int vb, cudaStream_t s,
                                const __half* knew = nullptr, const __half* vnew = nullptr,
                                bool overlap = false);
+// The two page variants behind launch_decode_attn (st.asym picks one).
+cudaError_t launch_decode_attn_sym(const DevState& st, int layer, int n_seqs,
+                                   const int32_t* slots, const __half* q, __half* o, int splits,
+                                   int vb, cudaStream_t s, const __half* knew,
+                                   const __half* vnew, bool overlap);
+cudaError_t launch_decode_attn_asym(const DevState& st, int layer, int n_seqs,
+                                    const int32_t* slots, const __half* q, __half* o, int splits,
+                                    int vb, cudaStream_t s, const __half* knew,
+                                    const __half* vnew, bool overlap);
 cudaError_t canary_init();  // once per process, before any launch
 cudaError_t launch_canary(const DevState& st, int layer, int n_seqs, const int32_t* slots,
                           const __half* q, float* delta_out, cudaStream_t s);

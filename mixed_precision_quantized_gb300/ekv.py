@@ -39,6 +39,7 @@ class EkvConfig(ctypes.Structure):
         ("tau_ctx0", ctypes.c_int32),
         ("hysteresis", ctypes.c_float),
         ("vote", ctypes.c_int32),
+        ("quantizer", ctypes.c_int32),
         ("dev_alloc", ctypes.c_void_p),
         ("dev_free", ctypes.c_void_p),
         ("alloc_ctx", ctypes.c_void_p),
@@ -53,6 +54,7 @@ _I32 = ctypes.c_int32
 _SIGS = {
     "ekv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "ekv_page_bytes": (_I32, [_I32, _I32, _I32]),
+    "ekv_page_bytes_q": (_I32, [_I32, _I32, _I32, _I32]),
     "ekv_create": (ctypes.c_int, [ctypes.POINTER(EkvConfig), _P, _P, ctypes.POINTER(_P)]),
     "ekv_destroy": (ctypes.c_int, [_P]),
     "ekv_seq_reset": (ctypes.c_int, [_P, _I32, _P]),
@@ -113,8 +115,12 @@ def _check(rc: int, what: str):
         raise EkvError(rc, what)
 
 
-def page_bytes(k_bits: int, v_bits: int, head_dim: int) -> int:
-    return lib().ekv_page_bytes(k_bits, v_bits, head_dim)
+QUANT_SYMMETRIC, QUANT_ASYMMETRIC = 0, 1
+
+
+def page_bytes(k_bits: int, v_bits: int, head_dim: int, asym: bool = False) -> int:
+    return lib().ekv_page_bytes_q(k_bits, v_bits, head_dim,
+                                  QUANT_ASYMMETRIC if asym else QUANT_SYMMETRIC)
 
 
 def _ptr(t: torch.Tensor | None):
@@ -133,7 +139,7 @@ class Cache:
                  head_dim: int, max_seq_len: int, pool_pages: dict, k_bits_init, v_bits,
                  alpha: float = 0.25, tau: float = 0.05, softmax_scale: float = 0.0,
                  device=None, torch_alloc: bool = True, tau_ctx0: int = 0,
-                 hysteresis: float = 0.0, vote: int = 1):
+                 hysteresis: float = 0.0, vote: int = 1, asym: bool = False):
         L = lib()
         self.device = torch.device("cuda" if device is None else device)
         self.num_layers, self.max_seqs = num_layers, max_seqs
@@ -147,6 +153,8 @@ class Cache:
             cfg.pool_pages[fmt_index(kb, vb)] = int(n)
         cfg.softmax_scale, cfg.ema_alpha, cfg.tau = softmax_scale, alpha, tau
         cfg.tau_ctx0, cfg.hysteresis, cfg.vote = int(tau_ctx0), float(hysteresis), int(vote)
+        cfg.quantizer = QUANT_ASYMMETRIC if asym else QUANT_SYMMETRIC
+        self.asym = bool(asym)
         self._keep = []
         if torch_alloc:
             dev = self.device.index if self.device.index is not None else torch.cuda.current_device()
@@ -291,7 +299,7 @@ class Cache:
 
     def read_pages(self, layer: int, slot: int, kv_head: int, first: int, n: int,
                    stream=None) -> torch.Tensor:
-        stride = page_bytes(16, 16, self.head_dim)
+        stride = page_bytes(16, 16, self.head_dim, self.asym)
         dst = torch.zeros(max(1, n), stride, dtype=torch.uint8, device=self.device)
         _check(lib().ekv_read_pages(self._h, layer, slot, kv_head, first, n, _ptr(dst), stride,
                                     _stream(stream)), "ekv_read_pages")
@@ -368,4 +376,5 @@ def cache_for(w, device=None, max_seqs: int | None = None, torch_alloc: bool = T
     """A cache sized for a `workloads.Workload`."""
     return Cache(w.num_layers, max_seqs or w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim,
                  w.max_seq_len, w.pool_pages(), w.k_bits_init, w.v_bits, alpha=w.alpha,
-                 tau=w.tau, device=device, torch_alloc=torch_alloc)
+                 tau=w.tau, device=device, torch_alloc=torch_alloc,
+                 asym=getattr(w, "asym", False))

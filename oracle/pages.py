@@ -116,9 +116,10 @@ def v_rows_bytes(vb: int, v16: np.ndarray, clip=None, asym: bool = False) -> dic
             "v_scales": s.astype(np.float16).view(np.uint8).reshape(-1, 2)}
 
 
-def extract(page: np.ndarray, kb: int, vb: int, d: int, name: str, rows: int | None = None):
+def extract(page: np.ndarray, kb: int, vb: int, d: int, name: str, rows: int | None = None,
+            asym: bool = False):
     """Slice region `name` out of raw page bytes as [rows, row_bytes] uint8."""
-    off, rb, n = regions(kb, vb, d)[name]
+    off, rb, n = regions(kb, vb, d, asym)[name]
     if rows is None:
         rows = n
     return np.asarray(page, dtype=np.uint8)[off:off + rb * n].reshape(n, rb)[:rows]

@@ -63,7 +63,7 @@ def check_pages(cache: ekv.Cache, ref: decoder.ReferenceRun, l: int, s: int, hea
             rows = min(16, st.T - 16 * j)
             for name, want in exp.items():
                 got = pages.extract(raw[j], kb, vb, w.head_dim, name,
-                                    rows=want.shape[0])
+                                    rows=want.shape[0], asym=getattr(w, "asym", False))
                 assert np.array_equal(got, want), (
                     f"layer {l} seq {s} head {h} block {j} ({kb},{vb}) region {name} "
                     f"rows {rows}: {np.argwhere(got != want)[:5].tolist()}")
@@ -82,7 +82,8 @@ class Run:
         else:
             self.cache = ekv.Cache(w.num_layers, w.batch, w.num_q_heads, w.num_kv_heads,
                                    w.head_dim, w.max_seq_len, pool_pages, w.k_bits_init,
-                                   w.v_bits, alpha=w.alpha, tau=w.tau)
+                                   w.v_bits, alpha=w.alpha, tau=w.tau,
+                                   asym=getattr(w, "asym", False))
         for l, (kc, vc) in (clips or {}).items():
             self.cache.set_clip(l, kc, vc)
         self.slots = torch.arange(w.batch, dtype=torch.int32, device="cuda")

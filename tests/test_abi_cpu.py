@@ -48,6 +48,12 @@ def test_page_bytes_matches_oracle_layout(lib):
                 assert lib.ekv_page_bytes(kb, vb, d) == pages.page_bytes(kb, vb, d)
     assert lib.ekv_page_bytes(3, 4, 128) == -1
     assert lib.ekv_page_bytes(4, 4, 96) == -1
+    for kb in (2, 4, 8, 16):
+        for vb in (2, 4, 8, 16):
+            for d in (64, 128):
+                assert lib.ekv_page_bytes_q(kb, vb, d, 1) == pages.page_bytes(kb, vb, d, asym=True)
+                assert lib.ekv_page_bytes_q(kb, vb, d, 0) == pages.page_bytes(kb, vb, d)
+    assert lib.ekv_page_bytes_q(4, 4, 128, 2) == -1
 
 
 def test_status_strings(lib):
