@@ -19,8 +19,8 @@ sides, max over ranks):
      bracketed by timing events inside the graph         -> roofline (attention)
   E  the next K steps with a pinned-host -> device copy of the step's inputs
      and a device -> pinned-host copy of every layer's output per step -> e2e
-The canary cost is timed separately (all layers' canary + one controller
-update, replayed as a graph) -> canary_us_per_firing.
+The canary cost is timed separately (every layer's canary in one launch + one
+controller update, replayed as a graph) -> canary_us_per_firing.
 
 `--impl reference` times the CPU oracle on the same workload on a bounded
 sample (a few layers of one decode step), on rank 0 only.
@@ -315,8 +315,8 @@ def main():
         combine = functools.partial(replicas.combine_readings, R, n_queries=nq,
                                     total=replicas.total_queries(R, nq, dev))
 
-    def canary(c, l, q):
-        c.canary_kl(l, slots, q, None if delta_buf is None else delta_buf[l])
+    def canary(c, q_layers):  # every layer's canary in one launch; q_layers [L, B, Hq, d]
+        c.canary_kl_layers(0, slots, q_layers, delta_buf)
 
     def fire_end(c, freeze=False):
         if combine is None:
@@ -346,7 +346,7 @@ def main():
                                              delta_out=delta_buf, fused=fused, combine=combine)
                           for i in range(W, W + K)])
     per_layer = 1 if fused else 2
-    launches = sum(per_layer * L + ((L + 1) if w.fires(i) else 0) for i in range(W, W + K))
+    launches = sum(per_layer * L + (2 if w.fires(i) else 0) for i in range(W, W + K))
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     clk = Clocks(local).__enter__()
@@ -409,9 +409,8 @@ def main():
                     c.decode_attn(l, slots, q, outs[l])
                 if external_ok:
                     pairs[n * L + l][1].record(stream)
-                if w.fires(i):
-                    canary(c, l, q)
             if w.fires(i):
+                canary(c, inp.step_q(i))
                 fire_end(c)
 
     gB = capture(steps_with_events)
@@ -428,11 +427,10 @@ def main():
     attn_avg_s = (sum(attn_ms) / len(attn_ms) / 1e3) if attn_ms else None
 
     # ---- canary: all layers + one controller update ----------------------------
-    q_last = [inp.layer(l, W + 2 * K - 1)[0] for l in range(L)]
+    q_last = inp.step_q(W + 2 * K - 1)
 
     def firing():
-        for l in range(L):
-            canary(cache, l, q_last[l])
+        canary(cache, q_last)
         fire_end(cache, freeze=True)
 
     gC = capture(firing)
@@ -486,7 +484,8 @@ def main():
         del per_step, inpE
         nq, nkv = B * w.num_q_heads * w.head_dim, B * w.num_kv_heads * w.head_dim
         dbuf = torch.empty(host_in.shape[1], dtype=torch.float16, device=dev)
-        qd = [dbuf[l * nq:(l + 1) * nq].view(B, w.num_q_heads, w.head_dim) for l in range(L)]
+        qd_all = dbuf[:L * nq].view(L, B, w.num_q_heads, w.head_dim)
+        qd = [qd_all[l] for l in range(L)]
         kd = [dbuf[L * nq + l * nkv:L * nq + (l + 1) * nkv].view(B, 1, w.num_kv_heads, w.head_dim)
               for l in range(L)]
         vd = [dbuf[L * (nq + nkv) + l * nkv:L * (nq + nkv) + (l + 1) * nkv]
@@ -501,13 +500,12 @@ def main():
                 for l in range(L):
                     if fused:
                         c.append_decode_attn(l, slots, kd[l], vd[l], qd[l], outs[l],
-                                             after_other_layer=l > 0 and not w.fires(i))
+                                             after_other_layer=l > 0)
                     else:
                         c.append(l, slots, kd[l], vd[l])
                         c.decode_attn(l, slots, qd[l], outs[l])
-                    if w.fires(i):
-                        canary(c, l, qd[l])
                 if w.fires(i):
+                    canary(c, qd_all)
                     fire_end(c)
                 host_out[n].copy_(out, non_blocking=True)
 

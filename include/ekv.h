@@ -237,6 +237,17 @@ EKV_API int ekv_decode_attn_noalloc(ekv_cache* cache, int32_t layer, int32_t n_s
 EKV_API int ekv_canary_kl(ekv_cache* cache, int32_t layer, int32_t n_seqs, const int32_t* seq_slots,
                   const void* q, float* delta_out, void* stream);
 
+/* The canary of layers first_layer .. first_layer+n_layers-1 in one launch, with
+ * the same readings as n_layers calls of ekv_canary_kl.  Layer first_layer+i
+ * reads its queries [n_seqs][Hq][d] at q + i * q_layer_stride (fp16 elements,
+ * >= n_seqs*Hq*d when n_layers > 1) and, if delta_out (dev float[n_layers][3])
+ * is not NULL, writes its readings to delta_out[i].  A decode step that fires
+ * the canary calls it once, after every layer's append (a layer's ring and
+ * queries are final then): one launch instead of one per layer. */
+EKV_API int ekv_canary_kl_layers(ekv_cache* cache, int32_t first_layer, int32_t n_layers,
+                                 int32_t n_seqs, const int32_t* seq_slots, const void* q,
+                                 int64_t q_layer_stride, float* delta_out, void* stream);
+
 /* Controller update for every layer whose layer_mask entry is nonzero
  * (layer_mask dev uint8[num_layers], NULL = all layers):
  *   ema = first reading ? delta : (1-alpha)*ema + alpha*delta   (fp32, unfused)

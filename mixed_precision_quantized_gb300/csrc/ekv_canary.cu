@@ -9,11 +9,15 @@
 // in FP16? — No."); quant_b is the cache's symmetric quantizer applied per
 // channel over consecutive 16-row groups of W starting at the oldest row.
 //
-// One CTA per (sequence, KV head) holds W, its three quantize-dequantize
+// One CTA per (layer, sequence, KV head) holds W, its three quantize-dequantize
 // copies and the group's queries in shared memory, computes the four logit
 // sets, the log-softmaxes and the three KL sums of its G query heads, and
-// writes one partial per reading.  The last CTA (atomic ticket, no waiting)
-// adds the partials in a fixed order and stores the layer's mean readings.
+// writes one partial per reading.  The last CTA of a layer (atomic ticket, no
+// waiting) adds the layer's partials in a fixed order and stores its mean
+// readings.  One launch may cover several layers (a firing step's canary runs
+// once, after every layer's append, over all of them: a layer's ring and
+// queries are final then), so a launch fills the GPU instead of Hkv * n_seqs
+// CTAs.
 //
 // Controller ("Show the math", EMA and pick; "Bidirectional adjustment"):
 //   ema = first reading ? delta : (1-alpha) ema + alpha delta   (fp32, unfused)
@@ -42,8 +46,9 @@ __host__ __device__ constexpr size_t canary_smem_bytes() {
 
 template <int D>
 __global__ void __launch_bounds__(CANARY_THREADS)
-canary_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
-              const __half* __restrict__ q, float* __restrict__ delta_out, int n_seqs) {
+canary_kernel(DevState st, int layer0, const int32_t* __restrict__ slots,
+              const __half* __restrict__ qs, size_t q_layer_stride,
+              float* __restrict__ delta_out, int n_seqs) {
   constexpr int P = D + 1;  // padded row
   extern __shared__ float sm[];
   float* W = sm;                             // [64][P]   fp16 window as fp32
@@ -54,6 +59,8 @@ canary_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   __shared__ int s_last;
 
   const int h = blockIdx.x, z = blockIdx.y;
+  const int layer = layer0 + blockIdx.z;
+  const __half* q = qs + blockIdx.z * q_layer_stride;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = st.G;
   const int slot = slots[z];
@@ -162,10 +169,11 @@ canary_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   __syncthreads();
 
   const int cta = z * st.Hkv + h;
+  float* part = st.canary_part + (size_t)layer * st.S * st.Hkv * NBITS;
   if (tid < NBITS) {
     float s = 0.f;
     for (int hd = 0; hd < G; ++hd) s += n > 0 ? s_kl[tid][hd] : 0.f;
-    st.canary_part[(size_t)cta * NBITS + tid] = s;
+    part[(size_t)cta * NBITS + tid] = s;
   }
   __threadfence();
   __syncthreads();
@@ -180,10 +188,10 @@ canary_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   __threadfence();
   if (tid < NBITS) {
     float s = 0.f;
-    for (int i = 0; i < n_seqs * st.Hkv; ++i) s += __ldcg(st.canary_part + (size_t)i * NBITS + tid);
+    for (int i = 0; i < n_seqs * st.Hkv; ++i) s += __ldcg(part + (size_t)i * NBITS + tid);
     const float dl = s / (float)(n_seqs * st.Hq);
     st.delta[layer * NBITS + tid] = dl;
-    if (delta_out) delta_out[tid] = dl;
+    if (delta_out) delta_out[blockIdx.z * NBITS + tid] = dl;
   }
 }
 
@@ -256,15 +264,16 @@ cudaError_t canary_init() {
   return e;
 }
 
-cudaError_t launch_canary(const DevState& st, int layer, int n_seqs, const int32_t* slots,
-                          const __half* q, float* delta_out, cudaStream_t s) {
-  dim3 grid(st.Hkv, n_seqs);
+cudaError_t launch_canary(const DevState& st, int layer0, int n_layers, int n_seqs,
+                          const int32_t* slots, const __half* q, size_t q_layer_stride,
+                          float* delta_out, cudaStream_t s) {
+  dim3 grid(st.Hkv, n_seqs, n_layers);
   if (st.D == 64)
-    canary_kernel<64><<<grid, CANARY_THREADS, canary_smem_bytes<64>(), s>>>(st, layer, slots, q,
-                                                                           delta_out, n_seqs);
+    canary_kernel<64><<<grid, CANARY_THREADS, canary_smem_bytes<64>(), s>>>(
+        st, layer0, slots, q, q_layer_stride, delta_out, n_seqs);
   else
-    canary_kernel<128><<<grid, CANARY_THREADS, canary_smem_bytes<128>(), s>>>(st, layer, slots, q,
-                                                                             delta_out, n_seqs);
+    canary_kernel<128><<<grid, CANARY_THREADS, canary_smem_bytes<128>(), s>>>(
+        st, layer0, slots, q, q_layer_stride, delta_out, n_seqs);
   return cudaGetLastError();
 }
 

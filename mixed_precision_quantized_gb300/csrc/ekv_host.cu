@@ -195,7 +195,7 @@ int ekv_create(const ekv_config* cfg, const uint8_t* k_bits_init, const uint8_t*
   st.attn_acc = (float*)A((size_t)parts * MAX_G * D * 4);
   st.attn_ml = (float*)A((size_t)parts * MAX_G * 2 * 4);
   st.attn_ticket = (int32_t*)A(S * H * ATTN_TICKETS * 4);
-  st.canary_part = (float*)A(S * H * 3 * 4);
+  st.canary_part = (float*)A(L * S * H * 3 * 4);
   st.canary_ticket = (int32_t*)A(L * 4);
   if (!ok) {
     free_all(c);
@@ -311,7 +311,21 @@ int ekv_canary_kl(ekv_cache* c, int32_t layer, int32_t n_seqs, const int32_t* se
                   const void* q, float* delta_out, void* stream) {
   if (!c || layer < 0 || layer >= c->st.L || n_seqs <= 0 || n_seqs > c->st.S) return EKV_EINVAL;
   if (!seq_slots || !q) return EKV_EINVAL;
-  return cuda_status(launch_canary(c->st, layer, n_seqs, seq_slots, static_cast<const __half*>(q),
+  return cuda_status(launch_canary(c->st, layer, 1, n_seqs, seq_slots,
+                                   static_cast<const __half*>(q), 0, delta_out,
+                                   as_stream(stream)));
+}
+
+int ekv_canary_kl_layers(ekv_cache* c, int32_t first_layer, int32_t n_layers, int32_t n_seqs,
+                         const int32_t* seq_slots, const void* q, int64_t q_layer_stride,
+                         float* delta_out, void* stream) {
+  if (!c || first_layer < 0 || n_layers <= 0 || first_layer + n_layers > c->st.L ||
+      n_seqs <= 0 || n_seqs > c->st.S || !seq_slots || !q || q_layer_stride < 0 ||
+      n_layers > 65535)
+    return EKV_EINVAL;
+  if (n_layers > 1 && q_layer_stride < (int64_t)n_seqs * c->st.Hq * c->st.D) return EKV_EINVAL;
+  return cuda_status(launch_canary(c->st, first_layer, n_layers, n_seqs, seq_slots,
+                                   static_cast<const __half*>(q), (size_t)q_layer_stride,
                                    delta_out, as_stream(stream)));
 }
 

@@ -75,7 +75,7 @@ struct DevState {
   float* attn_ml;           // [parts][G][2]   split partial (max, sum), log2 domain
   int32_t* attn_ticket;     // [S][Hkv][ATTN_TICKETS] merge tickets (head, then groups)
   int32_t attn_parts_cap;
-  float* canary_part;       // [S*Hkv][3]
+  float* canary_part;       // [L][S*Hkv][3]
   int32_t* canary_ticket;   // [L]
 };
 
@@ -113,8 +113,11 @@ cudaError_t launch_decode_attn_asym(const DevState& st, int layer, int n_seqs,
                                     int vb, cudaStream_t s, const __half* knew,
                                     const __half* vnew, bool overlap);
 cudaError_t canary_init();  // once per process, before any launch
-cudaError_t launch_canary(const DevState& st, int layer, int n_seqs, const int32_t* slots,
-                          const __half* q, float* delta_out, cudaStream_t s);
+// Layers layer0 .. layer0+n_layers-1 in one launch; layer layer0+i reads its
+// queries at q + i * q_layer_stride and writes delta_out[i][3] (if not null).
+cudaError_t launch_canary(const DevState& st, int layer0, int n_layers, int n_seqs,
+                          const int32_t* slots, const __half* q, size_t q_layer_stride,
+                          float* delta_out, cudaStream_t s);
 cudaError_t launch_tier_update(const DevState& st, const float* delta, const uint8_t* mask,
                                int freeze, cudaStream_t s);
 cudaError_t launch_seq_reset(const DevState& st, int slot, cudaStream_t s);

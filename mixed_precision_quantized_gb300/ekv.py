@@ -63,6 +63,8 @@ _SIGS = {
     "ekv_append_decode_attn": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P, _P, _P, _I32, _P]),
     "ekv_decode_attn_noalloc": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P, _P]),
     "ekv_canary_kl": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P, _P]),
+    "ekv_canary_kl_layers": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P, ctypes.c_int64, _P,
+                                            _P]),
     "ekv_tier_update": (ctypes.c_int, [_P, _P, _P, _I32, _P]),
     "ekv_set_tiers": (ctypes.c_int, [_P, _P, _P]),
     "ekv_get_state": (ctypes.c_int, [_P, _P, _P, _P, _P, _P]),
@@ -235,6 +237,19 @@ class Cache:
                   delta_out: torch.Tensor | None = None, stream=None):
         _check(lib().ekv_canary_kl(self._h, layer, seq_slots.numel(), _ptr(seq_slots), _ptr(q),
                                    _ptr(delta_out), _stream(stream)), "ekv_canary_kl")
+        return delta_out
+
+    def canary_kl_layers(self, first_layer: int, seq_slots: torch.Tensor, q: torch.Tensor,
+                         delta_out: torch.Tensor | None = None, stream=None):
+        """Canary of layers first_layer .. first_layer + q.shape[0] - 1 in one launch;
+        q [n_layers, n_seqs, Hq, d] (each layer's block contiguous)."""
+        n = q.shape[0]
+        if q[0].numel() and not q[0].is_contiguous():
+            raise ValueError("each layer's queries must be contiguous")
+        stride = q.stride(0) if n > 1 else 0
+        _check(lib().ekv_canary_kl_layers(self._h, first_layer, n, seq_slots.numel(),
+                                          _ptr(seq_slots), _ptr(q), stride, _ptr(delta_out),
+                                          _stream(stream)), "ekv_canary_kl_layers")
         return delta_out
 
     def tier_update(self, delta: torch.Tensor | None = None, layer_mask: torch.Tensor | None = None,

@@ -1,9 +1,11 @@
 """Issue the decode path of a workload through the C ABI.
 
 One decode step is, per layer l: append the step's K/V (ring write, V
-quantization, K staging or seal, page admission at the layer's tier), decode
-attention over the whole cache, and on a firing step the canary; after the
-last layer of a firing step, the controller updates every layer's EMA and tier.
+quantization, K staging or seal, page admission at the layer's tier) and
+decode attention over the whole cache.  On a firing step the canary of every
+layer then runs in one launch (a layer's ring and queries are final once its
+append is done, so the readings are those of a canary right after each
+layer), and the controller updates every layer's EMA and tier.
 """
 from __future__ import annotations
 
@@ -16,14 +18,24 @@ class Inputs:
     """Device-resident per-step inputs of a workload (Q, new K, new V per layer)."""
 
     def __init__(self, w: workloads.Workload, step0: int, n_steps: int, device="cuda"):
-        self.q, self.k, self.v = [], [], []
-        for l in range(w.num_layers):
+        self.k, self.v = [], []
+        L = w.num_layers
+        # Q of every layer of a step side by side, [n, L, B, Hq, d], for the
+        # canary's all-layer launch
+        self.q_all = torch.empty(n_steps, L, w.batch, w.num_q_heads, w.head_dim,
+                                 dtype=torch.float16, device=device)
+        for l in range(L):
             k, v = w.step_kv(l, step0, n_steps, device=device)     # [B, n, Hkv, d]
             q = w.step_q(l, step0, n_steps, device=device)         # [B, n, Hq, d]
             self.k.append(k.transpose(0, 1).contiguous())          # [n, B, Hkv, d]
             self.v.append(v.transpose(0, 1).contiguous())
-            self.q.append(q.transpose(0, 1).contiguous())          # [n, B, Hq, d]
+            self.q_all[:, l] = q.transpose(0, 1)
+        self.q = [self.q_all[:, l] for l in range(L)]              # [n, B, Hq, d] views
         self.step0, self.n = step0, n_steps
+
+    def step_q(self, i: int) -> torch.Tensor:
+        """Q of every layer of local step i, [L, B, Hq, d]."""
+        return self.q_all[i]
 
     def layer(self, l: int, i: int):
         """(q [B,Hq,d], k [B,1,Hkv,d], v [B,1,Hkv,d]) of local step i."""
@@ -63,15 +75,14 @@ def decode_step(cache: ekv.Cache, w: workloads.Workload, slots: torch.Tensor, in
         q, k, v = inp.layer(l, i)
         if fused:
             # the previous launch is the fused step of layer l-1 unless this is
-            # the first layer or the canary ran after each layer
+            # the first layer
             cache.append_decode_attn(l, slots, k, v, q, out[l],
-                                     after_other_layer=overlap and l > 0 and not fires)
+                                     after_other_layer=overlap and l > 0)
         else:
             cache.append(l, slots, k, v)
             cache.decode_attn(l, slots, q, out[l])
-        if fires:
-            cache.canary_kl(l, slots, q, None if delta_out is None else delta_out[l])
     if fires:
+        cache.canary_kl_layers(0, slots, inp.step_q(i), delta_out)
         if combine is not None:
             combine(delta_out)
             cache.tier_update(delta_out)

@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 import torch
 
-from mixed_precision_quantized_gb300 import build, ekv, workloads
+from mixed_precision_quantized_gb300 import build, ekv, runner, workloads
 from oracle import controller, decoder
 
 from gpu_harness import Run
@@ -246,5 +246,32 @@ def test_empty_sequence_attends_to_zero():
         o = cache.decode_attn(0, slots, q)
         cache.sync()
         assert torch.all(o == 0)
+    finally:
+        cache.close()
+
+
+def test_all_layer_canary_launch_equals_per_layer_calls():
+    """One canary launch over every layer gives each layer exactly the readings
+    of its own call (the same CTAs, the same fixed reduction order)."""
+    w = workloads.qwen14b_32k().scaled(num_layers=4, batch=2, prefill=[90, 200], steps=2,
+                                       k_bits_init=[2, 4, 8, 4], v_bits=[4, 4, 4, 4])
+    cache = ekv.cache_for(w)
+    try:
+        slots = torch.arange(w.batch, dtype=torch.int32, device="cuda")
+        runner.prefill(cache, w, slots)
+        inp = runner.Inputs(w, 0, 1)
+        one = torch.zeros(w.num_layers, 3, dtype=torch.float32, device="cuda")
+        for l in range(w.num_layers):
+            cache.canary_kl(l, slots, inp.layer(l, 0)[0], one[l])
+        allv = torch.zeros_like(one)
+        cache.canary_kl_layers(0, slots, inp.step_q(0), allv)
+        part = torch.zeros(2, 3, dtype=torch.float32, device="cuda")
+        cache.canary_kl_layers(1, slots, inp.step_q(0)[1:3], part)
+        cache.sync()
+        assert torch.equal(one, allv)
+        assert torch.equal(one[1:3], part)
+        assert torch.equal(torch.tensor(cache.state()["delta"]), one[:].cpu())
+        with pytest.raises(ekv.EkvError):
+            cache.canary_kl_layers(3, slots, inp.step_q(0)[:2], part)   # past the last layer
     finally:
         cache.close()
