@@ -31,7 +31,8 @@ constexpr int SEL_THREADS = 256;
 constexpr int SEL_WARPS = SEL_THREADS / 32;
 constexpr int SEL_TILE = 32;   // groups per CTA when each row holds one element of a group
 constexpr int SEL_BINS = 256;  // first pass (key bits 14..7); the second uses 128 (bits 6..0)
-constexpr int SEL_UNROLL = 8;  // rows in flight per warp
+constexpr int SEL_UNROLL = 16;  // rows in flight per warp (column groups)
+constexpr int SEL_RU = 4;       // rows in flight per warp (segment groups)
 
 __device__ __forceinline__ uint32_t mag_key(__half x) { return __half_as_ushort(x) & 0x7fffu; }
 
@@ -93,12 +94,20 @@ select_hist_kernel(const __half* __restrict__ x, int64_t n_rows, int64_t row_str
     const __half* base = x + (int64_t)g * group_stride;
     const uint32_t want = pass ? (uint32_t)b1[g] : 0u;
     uint32_t* h = hist[warp];
-    for (int64_t r = r0 + warp; r < r1; r += SEL_WARPS) {
-      const __half* row = base + r * row_stride;
+    for (int64_t r = r0 + warp; r < r1; r += SEL_RU * SEL_WARPS) {
       for (int i = lane; i < width; i += 32) {
-        const uint32_t k = mag_key(row[i]);
-        if (!pass) atomicAdd(h + (k >> 7), 1u);
-        else if ((k >> 7) == want) atomicAdd(h + (k & 127u), 1u);
+        uint32_t k[SEL_RU];
+#pragma unroll
+        for (int u = 0; u < SEL_RU; ++u) {
+          const int64_t ru = r + u * SEL_WARPS;
+          k[u] = ru < r1 ? mag_key(base[ru * row_stride + i]) : 0xFFFFu;  // 0xFFFF: no row
+        }
+#pragma unroll
+        for (int u = 0; u < SEL_RU; ++u) {
+          if (k[u] == 0xFFFFu) continue;
+          if (!pass) atomicAdd(h + (k[u] >> 7), 1u);
+          else if ((k[u] >> 7) == want) atomicAdd(h + (k[u] & 127u), 1u);
+        }
       }
     }
     __syncthreads();

@@ -29,7 +29,7 @@
 namespace ekv {
 namespace {
 
-constexpr int CANARY_THREADS = 256;
+constexpr int CANARY_THREADS = 1024;
 constexpr int NBITS = 3;
 
 __device__ __forceinline__ int quant_code(float x, float s, int qm) {
@@ -41,7 +41,7 @@ __device__ __forceinline__ int quant_code(float x, float s, int qm) {
 template <int D>
 __host__ __device__ constexpr size_t canary_smem_bytes() {
   return sizeof(float) * ((size_t)(1 + NBITS) * RING * (D + 1) + (size_t)MAX_G * D +
-                          (size_t)(1 + NBITS) * MAX_G * RING);
+                          (size_t)2 * (1 + NBITS) * MAX_G * RING);
 }
 
 template <int D>
@@ -54,7 +54,7 @@ canary_kernel(DevState st, int layer0, const int32_t* __restrict__ slots,
   float* W = sm;                             // [64][P]   fp16 window as fp32
   float* WQ = W + RING * P;                  // [3][64][P] quantize-dequantize copies
   float* Qs = WQ + NBITS * RING * P;         // [G][D]
-  float* Z = Qs + MAX_G * D;                 // [4][G][64] logits (sigma applied)
+  float* Z = Qs + MAX_G * D;                 // [2][4][G][64] half-sums, then logits
   __shared__ float s_kl[NBITS][MAX_G];
   __shared__ int s_last;
 
@@ -78,10 +78,10 @@ canary_kernel(DevState st, int layer0, const int32_t* __restrict__ slots,
     Qs[i] = __half2float(q[((size_t)z * st.Hq + (size_t)h * G) * D + i]);
   __syncthreads();
 
-  // quantize-dequantize: one group per (16-row group, channel)
+  // quantize-dequantize: one task per (bit width, 16-row group, channel)
   const int ngr = (n + 15) / 16;
-  for (int i = tid; i < ngr * D; i += CANARY_THREADS) {
-    const int gi = i / D, c = i % D;
+  for (int i = tid; i < NBITS * ngr * D; i += CANARY_THREADS) {
+    const int bi = i / (ngr * D), gi = i / D % ngr, c = i % D;
     const int r0 = gi * 16, r1 = min(r0 + 16, n);
     if (st.asym) {  // KIVI-style: min/max scale, zero point lo, unsigned codes
       float lo = CUDART_INF_F, hi = -CUDART_INF_F;
@@ -89,49 +89,52 @@ canary_kernel(DevState st, int layer0, const int32_t* __restrict__ slots,
         lo = fminf(lo, W[r * P + c]);
         hi = fmaxf(hi, W[r * P + c]);
       }
-#pragma unroll
-      for (int bi = 0; bi < NBITS; ++bi) {
-        const int L = (1 << (2 << bi)) - 1;
-        const float sf = __half2float(__float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), (float)L)));
-        for (int r = r0; r < r1; ++r) {
-          const float x = W[r * P + c];
-          const int u = sf == 0.f ? 0 : min(max(__float2int_rn(__fdiv_rn(__fsub_rn(x, lo), sf)), 0), L);
-          WQ[(bi * RING + r) * P + c] = __fadd_rn(__fmul_rn((float)u, sf), lo);
-        }
+      const int L = (1 << (2 << bi)) - 1;
+      const float sf = __half2float(__float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), (float)L)));
+      for (int r = r0; r < r1; ++r) {
+        const float x = W[r * P + c];
+        const int u = sf == 0.f ? 0 : min(max(__float2int_rn(__fdiv_rn(__fsub_rn(x, lo), sf)), 0), L);
+        WQ[(bi * RING + r) * P + c] = __fadd_rn(__fmul_rn((float)u, sf), lo);
       }
       continue;
     }
     float m = 0.f;
     for (int r = r0; r < r1; ++r) m = fmaxf(m, fabsf(W[r * P + c]));
     m = fminf(m, st.kclip[((size_t)layer * st.Hkv + h) * D + c]);  // the cache's own quantizer
-#pragma unroll
-    for (int bi = 0; bi < NBITS; ++bi) {
-      const int b = 2 << bi;
-      const int qm = (1 << (b - 1)) - 1;
-      const float sf = __half2float(__float2half_rn(__fdiv_rn(m, (float)qm)));
-      for (int r = r0; r < r1; ++r)
-        WQ[(bi * RING + r) * P + c] = (float)quant_code(W[r * P + c], sf, qm) * sf;
-    }
+    const int qm = (1 << ((2 << bi) - 1)) - 1;
+    const float sf = __half2float(__float2half_rn(__fdiv_rn(m, (float)qm)));
+    for (int r = r0; r < r1; ++r)
+      WQ[(bi * RING + r) * P + c] = (float)quant_code(W[r * P + c], sf, qm) * sf;
   }
   __syncthreads();
 
-  // logits of the reference and the three quantized copies
-  for (int i = tid; i < G * RING; i += CANARY_THREADS) {
-    const int hd = i / RING, j = i % RING;
+  // logits of the reference and the three quantized copies: each task sums one
+  // half of the channels of one (query head, key); the halves are then added
+  constexpr int ZS = (1 + NBITS) * MAX_G * RING;
+  for (int i = tid; i < 2 * G * RING; i += CANARY_THREADS) {
+    const int half = i / (G * RING), hd = i / RING % G, j = i % RING;
     if (j >= n) continue;
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
     const float* qh = Qs + hd * D;
-    for (int c = 0; c < D; ++c) {
+    for (int c = half * (D / 2); c < (half + 1) * (D / 2); ++c) {
       const float qc = qh[c];
       a0 = fmaf(qc, W[j * P + c], a0);
       a1 = fmaf(qc, WQ[(0 * RING + j) * P + c], a1);
       a2 = fmaf(qc, WQ[(1 * RING + j) * P + c], a2);
       a3 = fmaf(qc, WQ[(2 * RING + j) * P + c], a3);
     }
-    Z[(0 * MAX_G + hd) * RING + j] = a0 * st.scale;
-    Z[(1 * MAX_G + hd) * RING + j] = a1 * st.scale;
-    Z[(2 * MAX_G + hd) * RING + j] = a2 * st.scale;
-    Z[(3 * MAX_G + hd) * RING + j] = a3 * st.scale;
+    float* zh = Z + half * ZS;
+    zh[(0 * MAX_G + hd) * RING + j] = a0;
+    zh[(1 * MAX_G + hd) * RING + j] = a1;
+    zh[(2 * MAX_G + hd) * RING + j] = a2;
+    zh[(3 * MAX_G + hd) * RING + j] = a3;
+  }
+  __syncthreads();
+  for (int i = tid; i < (1 + NBITS) * G * RING; i += CANARY_THREADS) {
+    const int v = i / (G * RING), hd = i / RING % G, j = i % RING;
+    if (j >= n) continue;
+    const int o = (v * MAX_G + hd) * RING + j;
+    Z[o] = (Z[o] + Z[ZS + o]) * st.scale;
   }
   __syncthreads();
 
