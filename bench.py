@@ -254,9 +254,11 @@ def main():
         wc = w.scaled(prefill=[min(t, a.calib_tokens) for t in w.prefill])
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        art, _ = artifacts.calibrate(wc, device=dev)
+        # one model-level artifact: rank 0 calibrates, every rank loads its copy
+        art = artifacts.calibrate(wc, device=dev)[0] if rank == 0 else None
         torch.cuda.synchronize()
         cal_s = time.perf_counter() - t0
+        art = replicas.share_artifact(R, art)
         # the percentile select on one layer's full prefill keys and values
         kf, vf = w.prefill_kv(0, list(range(w.batch)), device=dev)
         kf, vf = kf.flatten(0, 1).contiguous(), vf.flatten(0, 1).contiguous()

@@ -106,3 +106,20 @@ def consolidate_tiers(r: Ranks, cache, device="cpu") -> list:
     voted = majority_tiers([g.cpu().tolist() for g in got])
     cache.set_tiers(voted)
     return voted
+
+
+def share_artifact(r: Ranks, artifact=None):
+    """One static artifact for every rank ("Behavior-Guided KV-Cache
+    Quantization": theta* and b* are model-level, frozen before inference):
+    rank 0 passes the artifact it calibrated, the others None, and all get rank
+    0's copy (its arrays read-only).  Alone it returns `artifact`."""
+    if r.world == 1:
+        return artifact
+    if r.rank == 0 and artifact is None:
+        raise ValueError("rank 0 must hold the artifact")
+    box = [artifact if r.rank == 0 else None]
+    dist.broadcast_object_list(box, src=0)
+    art = box[0]
+    for a in (art.k_clip, art.v_clip):
+        a.setflags(write=False)
+    return art

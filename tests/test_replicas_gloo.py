@@ -190,3 +190,43 @@ def test_majority_matches_oracle_on_random_vectors():
         assert replicas.majority_tiers(vecs) == controller.majority_vote(vecs)
     assert controller.majority_vote([[2], [8]]) == [8]            # tie -> widest
     assert controller.majority_vote([[2], [2], [8]]) == [2]       # majority beats width
+
+
+def _artifact_rank(rank: int, world: int, port: int, out) -> None:
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), WORLD_SIZE=str(world),
+                      RANK=str(rank), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        from mixed_precision_quantized_gb300 import artifacts
+        R = replicas.from_env()
+        mine = None
+        if rank == 0:
+            rng = np.random.default_rng(3)
+            mine = artifacts.Artifact([4, 8, 4], [4, 4, 4],
+                                      rng.random((3, 2, 64)).astype(np.float32) + 0.5,
+                                      rng.random((3, 2)).astype(np.float32) + 0.5,
+                                      [1.0, 0.99, 0.9], [1.0, 1.0, 0.99], [0.1, 0.3, 0.2],
+                                      0.5, 4, 8)
+        got = replicas.share_artifact(R, mine)
+        out.put((rank, got.k_bits, got.k_clip.tobytes(), got.v_clip.tobytes(),
+                 got.sensitivity, bool(got.k_clip.flags.writeable)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_static_artifact_shared_by_all_ranks():
+    """Rank 0's calibrated thresholds and bits reach every rank unchanged, read-only."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    ps = [ctx.Process(target=_artifact_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in ps:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in ps)
+    for p in ps:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    (r0, b0, k0, v0, s0, w0), (r1, b1, k1, v1, s1, w1) = res
+    assert (r0, r1) == (0, 1)
+    assert b0 == b1 == [4, 8, 4] and k0 == k1 and v0 == v1 and s0 == s1
+    assert not w0 and not w1
