@@ -299,10 +299,16 @@ def main():
         caches[-1].sync()
     prefill_s = (time.perf_counter() - t0) / NR
     cache = caches[0]
+    # Decode steps list the slots longest sequence first (a scheduler knows its
+    # sequences' lengths): the kernel starts the CTAs of the listed sequences in
+    # that order, so a ragged batch's long sequences do not end up in its last
+    # wave.  Slot s holds sequence s; batch position i holds sequence order[i].
+    order = sorted(range(w.batch), key=lambda s: (-w.prefill[s], s))
+    slots = torch.tensor(order, dtype=torch.int32, device=dev)
 
     def C(i):  # the cache decode step i runs on
         return caches[i % NR]
-    inp = runner.Inputs(w, 0, W + 2 * K, device=dev)
+    inp = runner.Inputs(w, 0, W + 2 * K, device=dev, order=order)
     L, B = w.num_layers, w.batch
     out = torch.empty(L, B, w.num_q_heads, w.head_dim, dtype=torch.float16, device=dev)
     outs = [out[l] for l in range(L)]
@@ -369,7 +375,7 @@ def main():
     tA2 = None
     if fused and not a.no_overlap_check:
         s2 = W + 2 * K + (0 if a.no_e2e else K)
-        inpA2 = runner.Inputs(w, s2, K, device=dev)
+        inpA2 = runner.Inputs(w, s2, K, device=dev, order=order)
         gA2 = capture(lambda: [runner.decode_step(C(i), w, slots, inpA2, i - s2, outs,
                                                   w.fires(i), delta_out=delta_buf, fused=True,
                                                   combine=combine, overlap=False)
@@ -478,7 +484,7 @@ def main():
     e2e = None
     if not a.no_e2e:
         s0 = W + 2 * K
-        inpE = runner.Inputs(w, s0, K, device=dev)
+        inpE = runner.Inputs(w, s0, K, device=dev, order=order)
         per_step = [torch.cat([inpE.q[l][i].reshape(-1) for l in range(L)] +
                               [inpE.k[l][i].reshape(-1) for l in range(L)] +
                               [inpE.v[l][i].reshape(-1) for l in range(L)]) for i in range(K)]

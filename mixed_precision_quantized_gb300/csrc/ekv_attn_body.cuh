@@ -818,10 +818,12 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   __shared__ int s_next, s_last;
   int32_t* s_bt = reinterpret_cast<int32_t*>(smem + AttnCfg<VB>::STAGE_SMEM);
 
-  // Block order: sequence fastest, then KV head, then split, so the CTAs that
-  // start last are the last split of every (sequence, KV head).
+  // Block order: KV head fastest, then sequence (in the order of `slots`), then
+  // split, so the CTAs that start last are the last split of every (sequence,
+  // KV head), and a caller that lists its longest sequences first gets them
+  // started first (longest-first scheduling of a ragged batch).
   const int n_seqs = gridDim.x / (splits * st.Hkv);
-  const int z = blockIdx.x % n_seqs, h = blockIdx.x / n_seqs % st.Hkv;
+  const int h = blockIdx.x % st.Hkv, z = blockIdx.x / st.Hkv % n_seqs;
   const int split = blockIdx.x / (n_seqs * st.Hkv);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;

@@ -17,7 +17,10 @@ from . import ekv, workloads
 class Inputs:
     """Device-resident per-step inputs of a workload (Q, new K, new V per layer)."""
 
-    def __init__(self, w: workloads.Workload, step0: int, n_steps: int, device="cuda"):
+    def __init__(self, w: workloads.Workload, step0: int, n_steps: int, device="cuda",
+                 order=None):
+        """`order`: the batch positions' sequences (default 0 .. B-1); position i
+        holds sequence order[i], to match a slot list in that order."""
         self.k, self.v = [], []
         L = w.num_layers
         # Q of every layer of a step side by side, [n, L, B, Hq, d], for the
@@ -25,8 +28,8 @@ class Inputs:
         self.q_all = torch.empty(n_steps, L, w.batch, w.num_q_heads, w.head_dim,
                                  dtype=torch.float16, device=device)
         for l in range(L):
-            k, v = w.step_kv(l, step0, n_steps, device=device)     # [B, n, Hkv, d]
-            q = w.step_q(l, step0, n_steps, device=device)         # [B, n, Hq, d]
+            k, v = w.step_kv(l, step0, n_steps, seqs=order, device=device)  # [B, n, Hkv, d]
+            q = w.step_q(l, step0, n_steps, seqs=order, device=device)      # [B, n, Hq, d]
             self.k.append(k.transpose(0, 1).contiguous())          # [n, B, Hkv, d]
             self.v.append(v.transpose(0, 1).contiguous())
             self.q_all[:, l] = q.transpose(0, 1)

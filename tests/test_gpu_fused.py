@@ -134,3 +134,36 @@ def test_fused_invalid_arguments_rejected_on_host():
         assert cache.seq_len(0, 0) == 0
     finally:
         cache.close()
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])
+def test_slot_order_is_only_a_schedule(fused):
+    """Listing the slots in another order (longest first) changes which CTAs start
+    first, not the results: twin caches fed the same sequences through slot lists
+    in two orders hold the same lengths and pages, and each sequence's output
+    matches."""
+    w = workloads.llama8b_batch32().scaled(num_layers=2, batch=5, prefill=[37, 300, 129, 64, 200],
+                                           steps=20)
+    order = sorted(range(w.batch), key=lambda s: -w.prefill[s])
+    caches = [ekv.cache_for(w), ekv.cache_for(w)]
+    try:
+        ident = torch.arange(w.batch, dtype=torch.int32, device="cuda")
+        for c in caches:
+            runner.prefill(c, w, ident)
+        slot_lists = [ident, torch.tensor(order, dtype=torch.int32, device="cuda")]
+        inps = [runner.Inputs(w, 0, w.steps), runner.Inputs(w, 0, w.steps, order=order)]
+        outs = [[torch.empty(w.batch, w.num_q_heads, w.head_dim, dtype=torch.float16,
+                             device="cuda") for _ in range(w.num_layers)] for _ in caches]
+        for t in range(w.steps):
+            for c, sl, inp, o in zip(caches, slot_lists, inps, outs):
+                runner.decode_step(c, w, sl, inp, t, o, w.fires(t), fused=fused)
+            for c in caches:
+                c.sync()
+            for l in range(w.num_layers):
+                x = outs[0][l][order].float().cpu().numpy().astype(np.float64)
+                y = outs[1][l].float().cpu().numpy().astype(np.float64)
+                assert np.all(np.abs(x - y) <= ATOL + RTOL * np.abs(x)), (t, l)
+        _compare(caches[0], caches[1], w, range(w.batch))
+    finally:
+        for c in caches:
+            c.close()
