@@ -65,18 +65,22 @@ constexpr int NSMAX = 8;  // stages per warp at most
 // Blocks the last split of an overlapped launch takes less (~6 us of a CTA's
 // page work: how much later its CTAs get an SM).
 constexpr int ATTN_LATE_BLOCKS = 80;
-// One CTA per SM.  Its warps share the split's pages through a counter in shared
-// memory, so a warp that runs ahead takes more pages.  Stage memory: 200 KB,
-// split evenly between the warps (quantized V: 16 warps, five K4/V4 pages each,
-// registers capped at 128; FP16 V pages are 3.5x larger and need more registers:
-// 12 warps).  After the stages come the split's page-table entries.
-template <int VB>
+// PACK CTAs per SM (1, or 2 when a launch has more (sequence, KV head) units
+// than SMs: then every CTA is resident at once and each SM holds a long and a
+// short one instead of running a second wave).  A CTA's warps share the
+// split's pages through a counter in shared memory, so a warp that runs ahead
+// takes more pages.  Stage memory: 200 KB per SM, split evenly between the
+// warps (quantized V: 16 warps, five K4/V4 pages each, registers capped at
+// 128; FP16 V pages are 3.5x larger and need more registers: 12 warps).  After
+// the stages come the split's page-table entries.
+template <int VB, int PACK = 1>
 struct AttnCfg {
-  static constexpr int NW = VB == 16 ? 12 : 16;
+  static constexpr int NW = (VB == 16 ? 12 : 16) / PACK;
   static constexpr int NT = NW * 32;
-  static constexpr int STAGE_SMEM = 200 * 1024;
+  static constexpr int STAGE_SMEM = 200 * 1024 / PACK;
+  static constexpr int BT_CAP = ATTN_BT_CAP / PACK;
   static constexpr int WARP_BYTES = (STAGE_SMEM / NW) & ~127;
-  static constexpr int SMEM = STAGE_SMEM + ATTN_BT_CAP * 4;
+  static constexpr int SMEM = STAGE_SMEM + BT_CAP * 4;
 };
 constexpr int WAIT_LIMIT = 1 << 22;      // bounded mbarrier polls before giving up
 
@@ -804,19 +808,20 @@ __device__ int32_t append_token(const DevState& st, int layer, int slot, int h, 
   return e;
 }
 
-template <int D, int VB, bool FUSED, bool A_ = ASYM>
-__global__ void __launch_bounds__(AttnCfg<VB>::NT, 1)
+template <int D, int VB, bool FUSED, int PACK, bool A_ = ASYM>
+__global__ void __launch_bounds__(AttnCfg<VB, PACK>::NT, PACK)
 decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
                    const __half* __restrict__ q, __half* __restrict__ o, int splits,
                    const __half* __restrict__ knew, const __half* __restrict__ vnew,
                    int late_blocks) {
-  constexpr int NW = AttnCfg<VB>::NW, NT = AttnCfg<VB>::NT;
+  using Cfg = AttnCfg<VB, PACK>;
+  constexpr int NW = Cfg::NW, NT = Cfg::NT;
   constexpr int KCH = D / 4, KW = KCH / 2, VCH = D / 8, NMT = D / 16;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[NW][NSMAX];
   __shared__ float sm_m[NW][MAX_G], sm_l[NW][MAX_G], sm_f[NW][MAX_G], sm_ml[MAX_G][2];
   __shared__ int s_next, s_last;
-  int32_t* s_bt = reinterpret_cast<int32_t*>(smem + AttnCfg<VB>::STAGE_SMEM);
+  int32_t* s_bt = reinterpret_cast<int32_t*>(smem + Cfg::STAGE_SMEM);
 
   // Block order: KV head fastest, then sequence (in the order of `slots`), then
   // split, so the CTAs that start last are the last split of every (sequence,
@@ -862,7 +867,7 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   // open (raw K rows in the staging buffer) or receives this launch's token.
   const bool last_apart = ((T % BLOCK) != 0 || app) && b1 == nb && b1 > b0;
   int np = b1 - b0 - (last_apart ? 1 : 0);  // pipelined pages of this split
-  if (np > ATTN_BT_CAP) {  // the host sizes splits so that this never happens
+  if (np > Cfg::BT_CAP) {  // the host sizes splits so that this never happens
     if (tid == 0) set_error(st, EKV_ESTATE);
     np = 0;
   }
@@ -899,7 +904,7 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   // (at least two stages for every format).
   const int kmax = max(2, st.kmax[layer]);
   const int stage_bytes = (page_bytes(kmax, VB, D, ASYM) + 127) & ~127;
-  constexpr int WARP_BYTES = AttnCfg<VB>::WARP_BYTES;
+  constexpr int WARP_BYTES = Cfg::WARP_BYTES;
   const int ns = min(NSMAX, WARP_BYTES / stage_bytes);
   const uint8_t* wptr = smem + warp * WARP_BYTES;
   const uint32_t wbase = (uint32_t)__cvta_generic_to_shared(wptr);
@@ -1167,41 +1172,42 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   merge_parts<D, NT>(st.attn_acc, st.attn_ml, pbase, 0, ATTN_GROUP, ngrp, G, tid, orow, 0);
 }
 
-template <int D, int VB>
+template <int D, int VB, int PACK>
 cudaError_t launch_t(const DevState& st, int layer, int n_seqs, const int32_t* slots,
                      const __half* q, __half* o, int splits, const __half* knew,
                      const __half* vnew, bool overlap, cudaStream_t s) {
+  using Cfg = AttnCfg<VB, PACK>;
   dim3 grid(splits * st.Hkv * n_seqs);
   if (knew && overlap) {  // programmatic dependent of the launch before it
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(AttnCfg<VB>::NT);
-    cfg.dynamicSmemBytes = AttnCfg<VB>::SMEM;
+    cfg.blockDim = dim3(Cfg::NT);
+    cfg.dynamicSmemBytes = Cfg::SMEM;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_attn_kernel<D, VB, true>, st, layer, slots, q, o,
-                              splits, knew, vnew, ATTN_LATE_BLOCKS);
+    return cudaLaunchKernelEx(&cfg, decode_attn_kernel<D, VB, true, PACK>, st, layer, slots, q,
+                              o, splits, knew, vnew, ATTN_LATE_BLOCKS);
   }
   if (knew)
-    decode_attn_kernel<D, VB, true><<<grid, AttnCfg<VB>::NT, AttnCfg<VB>::SMEM, s>>>(
+    decode_attn_kernel<D, VB, true, PACK><<<grid, Cfg::NT, Cfg::SMEM, s>>>(
         st, layer, slots, q, o, splits, knew, vnew, 0);
   else
-    decode_attn_kernel<D, VB, false><<<grid, AttnCfg<VB>::NT, AttnCfg<VB>::SMEM, s>>>(
+    decode_attn_kernel<D, VB, false, PACK><<<grid, Cfg::NT, Cfg::SMEM, s>>>(
         st, layer, slots, q, o, splits, nullptr, nullptr, 0);
   return cudaGetLastError();
 }
 
-template <int D, int VB>
-cudaError_t init_t() {
+template <int D, int VB, int PACK>
+cudaError_t init_pack() {
   cudaError_t e = cudaSuccess;
-  for (auto fn : {decode_attn_kernel<D, VB, false>, decode_attn_kernel<D, VB, true>}) {
+  for (auto fn : {decode_attn_kernel<D, VB, false, PACK>, decode_attn_kernel<D, VB, true, PACK>}) {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               AttnCfg<VB>::SMEM);
+                               AttnCfg<VB, PACK>::SMEM);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
                                cudaSharedmemCarveoutMaxShared);
@@ -1209,30 +1215,57 @@ cudaError_t init_t() {
   return e;
 }
 
+// Two CTAs per SM are built for d = 128 with quantized V only (the batched
+// shapes); the host never asks for them otherwise.
+template <int D, int VB>
+constexpr bool has_pack2() { return D == 128 && VB < 16; }
+
+template <int D, int VB>
+cudaError_t init_t(bool* pack2_ok) {
+  cudaError_t e = init_pack<D, VB, 1>();
+  if constexpr (has_pack2<D, VB>()) {
+    if (e == cudaSuccess) e = init_pack<D, VB, 2>();
+    // both kernels of the pair must fit twice on an SM, else the host keeps one
+    // CTA per SM
+    for (auto fn : {decode_attn_kernel<D, VB, false, 2>, decode_attn_kernel<D, VB, true, 2>}) {
+      int n = 0;
+      if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, AttnCfg<VB, 2>::NT,
+                                                          AttnCfg<VB, 2>::SMEM);
+      if (n < 2) *pack2_ok = false;
+    }
+  }
+  return e;
+}
+
 }  // namespace
 
-cudaError_t EKV_ATTN_FN(attn_init)() {
+cudaError_t EKV_ATTN_FN(attn_init)(bool* pack2_ok) {
   cudaError_t e = cudaSuccess;
-  cudaError_t (*fns[])() = {init_t<64, 2>,  init_t<64, 4>,  init_t<64, 8>,  init_t<64, 16>,
-                            init_t<128, 2>, init_t<128, 4>, init_t<128, 8>, init_t<128, 16>};
+  cudaError_t (*fns[])(bool*) = {init_t<64, 2>,  init_t<64, 4>,  init_t<64, 8>,  init_t<64, 16>,
+                                 init_t<128, 2>, init_t<128, 4>, init_t<128, 8>, init_t<128, 16>};
   for (auto f : fns)
-    if (e == cudaSuccess) e = f();
+    if (e == cudaSuccess) e = f(pack2_ok);
   return e;
 }
 
 cudaError_t EKV_ATTN_FN(launch_decode_attn)(const DevState& st, int layer, int n_seqs,
                                             const int32_t* slots, const __half* q, __half* o,
-                                            int splits, int vb, cudaStream_t s,
+                                            int splits, int vb, int pack, cudaStream_t s,
                                             const __half* knew, const __half* vnew,
                                             bool overlap) {
   using Fn = cudaError_t (*)(const DevState&, int, int, const int32_t*, const __half*, __half*,
                              int, const __half*, const __half*, bool, cudaStream_t);
   const int vi = vb == 2 ? 0 : vb == 4 ? 1 : vb == 8 ? 2 : 3;
-  static const Fn d64[] = {launch_t<64, 2>, launch_t<64, 4>, launch_t<64, 8>, launch_t<64, 16>};
-  static const Fn d128[] = {launch_t<128, 2>, launch_t<128, 4>, launch_t<128, 8>,
-                            launch_t<128, 16>};
-  return (st.D == 64 ? d64 : d128)[vi](st, layer, n_seqs, slots, q, o, splits, knew, vnew,
-                                       overlap, s);
+  static const Fn tab[2][4] = {
+      {launch_t<64, 2, 1>, launch_t<64, 4, 1>, launch_t<64, 8, 1>, launch_t<64, 16, 1>},
+      {launch_t<128, 2, 1>, launch_t<128, 4, 1>, launch_t<128, 8, 1>, launch_t<128, 16, 1>}};
+  static const Fn tab2[3] = {launch_t<128, 2, 2>, launch_t<128, 4, 2>, launch_t<128, 8, 2>};
+  if (pack == 2 && st.D == 128 && vi < 3)
+    return tab2[vi](st, layer, n_seqs, slots, q, o, splits, knew, vnew, overlap, s);
+  if (pack != 1) return cudaErrorInvalidValue;  // not built (the host never asks)
+  return tab[st.D == 64 ? 0 : 1][vi](st, layer, n_seqs, slots, q, o, splits, knew, vnew,
+                                     overlap, s);
 }
 
 }  // namespace ekv

@@ -42,16 +42,26 @@ void free_all(ekv_cache* c) {
   c->allocs.clear();
 }
 
+// CTAs per SM of a launch: 2 (half-size CTAs) when it has more (sequence, KV
+// head) units than SMs, so all of them are resident at once and a caller's
+// longest-first slot list pairs long and short units on the SMs instead of
+// leaving a second wave; else 1.  Built for d = 128 with quantized V.
+int attn_pack(const ekv_cache* c, int n_seqs, int vb) {
+  return c->st.D == 128 && vb < 16 && n_seqs * c->st.Hkv > c->num_sm && attn_pack2_ok() ? 2 : 1;
+}
+
 int attn_splits(const ekv_cache* c, int n_seqs, int vb) {
   // As many splits as fit in one wave of CTAs (a partial second wave would cost
   // a whole launch's start-up and tail again).
   const int units = n_seqs * c->st.Hkv;
-  const int target = attn_ctas_per_sm(vb) * c->num_sm;
+  const int pack = attn_pack(c, n_seqs, vb);
+  const int target = attn_ctas_per_sm(vb) * pack * c->num_sm;
   int s = target / units;
   if (s < 1) s = 1;
   // A split's page-table entries must fit the kernel's shared-memory copy (the
   // splits but the last share the blocks, hence the one extra).
-  const int need = (c->st.maxblk + ATTN_BT_CAP - 1) / ATTN_BT_CAP + 1;
+  const int cap = ATTN_BT_CAP / pack;
+  const int need = (c->st.maxblk + cap - 1) / cap + 1;
   if (s < need) s = need;
   if (s > ATTN_MAX_SPLITS) s = ATTN_MAX_SPLITS;
   return s;
@@ -66,11 +76,13 @@ bool valid_bits(int b) { return b == 2 || b == 4 || b == 8 || b == 16; }
 }  // namespace
 
 namespace ekv {
-int attn_plan(ekv_cache* c, int layer, int n_seqs, DevState* st, int* splits, int* vb) {
+int attn_plan(ekv_cache* c, int layer, int n_seqs, DevState* st, int* splits, int* vb,
+              int* pack) {
   if (!c || layer < 0 || layer >= c->st.L || n_seqs < 0 || n_seqs > c->st.S) return EKV_EINVAL;
   *st = c->st;
   *vb = c->vbits[layer];
   *splits = attn_splits(c, n_seqs > 0 ? n_seqs : 1, *vb);
+  *pack = attn_pack(c, n_seqs > 0 ? n_seqs : 1, *vb);
   return EKV_OK;
 }
 }  // namespace ekv
@@ -286,7 +298,8 @@ int ekv_decode_attn(ekv_cache* c, int32_t layer, int32_t n_seqs, const int32_t* 
   if (n_seqs * c->st.Hkv * splits > c->st.attn_parts_cap) return EKV_ESTATE;
   return cuda_status(launch_decode_attn(c->st, layer, n_seqs, seq_slots,
                                         static_cast<const __half*>(q), static_cast<__half*>(o),
-                                        splits, c->vbits[layer], as_stream(stream)));
+                                        splits, c->vbits[layer], attn_pack(c, n_seqs, c->vbits[layer]),
+                                        as_stream(stream)));
 }
 
 int ekv_append_decode_attn(ekv_cache* c, int32_t layer, int32_t n_seqs, const int32_t* seq_slots,
@@ -301,8 +314,8 @@ int ekv_append_decode_attn(ekv_cache* c, int32_t layer, int32_t n_seqs, const in
   if (n_seqs * c->st.Hkv * splits > c->st.attn_parts_cap) return EKV_ESTATE;
   return cuda_status(launch_decode_attn(c->st, layer, n_seqs, seq_slots,
                                         static_cast<const __half*>(q), static_cast<__half*>(o),
-                                        splits, c->vbits[layer], as_stream(stream),
-                                        static_cast<const __half*>(k),
+                                        splits, c->vbits[layer], attn_pack(c, n_seqs, c->vbits[layer]),
+                                        as_stream(stream), static_cast<const __half*>(k),
                                         static_cast<const __half*>(v),
                                         (flags & EKV_AFTER_OTHER_LAYER) != 0));
 }

@@ -92,25 +92,28 @@ __host__ __device__ inline size_t lsh_index(const DevState& st, int l, int s, in
 cudaError_t launch_append(const DevState& st, int layer, int n_seqs, const int32_t* slots,
                           int n_new, const __half* k, const __half* v, cudaStream_t s);
 cudaError_t attn_init();   // once per process, before any launch
-cudaError_t attn_init_sym();
-cudaError_t attn_init_asym();
+cudaError_t attn_init_sym(bool* pack2_ok);
+cudaError_t attn_init_asym(bool* pack2_ok);
+bool attn_pack2_ok();      // two half-size attention CTAs fit on an SM
 int attn_ctas_per_sm(int vb);  // resident decode-attention CTAs per SM for V width vb
 // With knew/vnew set ([n_seqs][Hkv][d] fp16 each) the launch first appends that
 // one token to every sequence (the fused decode step), then attends over it too;
 // `overlap` launches it as a programmatic dependent of the stream's previous
 // launch (which must be the fused step of another layer).
+// `pack`: CTAs per SM (1, or 2 for launches with more units than SMs; see
+// attn_pack in the host).
 cudaError_t launch_decode_attn(const DevState& st, int layer, int n_seqs, const int32_t* slots,
-                               const __half* q, __half* o, int splits, int vb, cudaStream_t s,
-                               const __half* knew = nullptr, const __half* vnew = nullptr,
-                               bool overlap = false);
+                               const __half* q, __half* o, int splits, int vb, int pack,
+                               cudaStream_t s, const __half* knew = nullptr,
+                               const __half* vnew = nullptr, bool overlap = false);
 // The two page variants behind launch_decode_attn (st.asym picks one).
 cudaError_t launch_decode_attn_sym(const DevState& st, int layer, int n_seqs,
                                    const int32_t* slots, const __half* q, __half* o, int splits,
-                                   int vb, cudaStream_t s, const __half* knew,
+                                   int vb, int pack, cudaStream_t s, const __half* knew,
                                    const __half* vnew, bool overlap);
 cudaError_t launch_decode_attn_asym(const DevState& st, int layer, int n_seqs,
                                     const int32_t* slots, const __half* q, __half* o, int splits,
-                                    int vb, cudaStream_t s, const __half* knew,
+                                    int vb, int pack, cudaStream_t s, const __half* knew,
                                     const __half* vnew, bool overlap);
 cudaError_t canary_init();  // once per process, before any launch
 // Layers layer0 .. layer0+n_layers-1 in one launch; layer layer0+i reads its
@@ -127,6 +130,7 @@ cudaError_t launch_init_stack(int32_t* stack, int32_t n, cudaStream_t s);
 
 // Argument checks and launch plan of decode attention for a handle: a copy of
 // its device state, the split count and the layer's V bits.
-int attn_plan(ekv_cache* c, int layer, int n_seqs, DevState* st, int* splits, int* vb);
+int attn_plan(ekv_cache* c, int layer, int n_seqs, DevState* st, int* splits, int* vb,
+              int* pack);
 
 }  // namespace ekv

@@ -51,9 +51,9 @@ extern "C" EKV_API int ekv_decode_attn_noalloc(ekv_cache* cache, int32_t layer, 
                                                void* stream) {
   using namespace ekv;
   DevState st;
-  int splits = 0, vb = 0;
+  int splits = 0, vb = 0, pack = 1;
   // Same argument checks, split count and kernel as ekv_decode_attn.
-  int rc = attn_plan(cache, layer, n_seqs, &st, &splits, &vb);
+  int rc = attn_plan(cache, layer, n_seqs, &st, &splits, &vb, &pack);
   if (rc != EKV_OK) return rc;
   if (n_seqs == 0) return EKV_OK;
   if (!seq_slots || !q || !o || (((uintptr_t)q | (uintptr_t)o) & 15)) return EKV_EINVAL;
@@ -80,6 +80,6 @@ extern "C" EKV_API int ekv_decode_attn_noalloc(ekv_cache* cache, int32_t layer, 
   // start at zero.
   if (cudaMemsetAsync(st.attn_ticket, 0, tk_bytes, s) != cudaSuccess) return EKV_ECUDA;
   cudaError_t e = launch_decode_attn(st, layer, n_seqs, seq_slots, static_cast<const __half*>(q),
-                                     static_cast<__half*>(o), splits, vb, s);
+                                     static_cast<__half*>(o), splits, vb, pack, s);
   return e == cudaSuccess ? EKV_OK : EKV_ECUDA;
 }

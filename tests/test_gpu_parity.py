@@ -275,3 +275,12 @@ def test_all_layer_canary_launch_equals_per_layer_calls():
             cache.canary_kl_layers(3, slots, inp.step_q(0)[:2], part)   # past the last layer
     finally:
         cache.close()
+
+
+@FUSED
+def test_more_units_than_sms_two_ctas_per_sm(fused):
+    """20 sequences x 8 KV heads = 160 (sequence, head) units > 152 SMs: the
+    launch packs two half-size CTAs per SM; ragged short contexts, d 128, V4."""
+    w = workloads.llama8b_batch32().scaled(num_layers=1, batch=20,
+                                           prefill=[5 + 13 * i for i in range(20)], steps=6)
+    _full_run(w, 6, fused=fused)
