@@ -45,8 +45,8 @@ METRIC = "quantized-KV decode attn HBM GB/s (% of peak), tokens/s; canary µs/fi
 # (profiles/decode_attn_llama70b_128k.md: 2-layer case, the same per-launch
 # work as one layer of the full workload), valid only for the kernel source it
 # was taken on: any change to that source reports null until re-captured.
-TRAFFIC_BYTES = 156.87e6
-TRAFFIC_SOURCE_SHA = "907e112ffb8427a6"
+TRAFFIC_BYTES = 157.29e6
+TRAFFIC_SOURCE_SHA = "079b9606b822290f"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
