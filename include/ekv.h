@@ -7,9 +7,15 @@
  *
  *   ekv_append       quantize-and-append of new K/V tokens into the paged cache
  *   ekv_decode_attn  single-token GQA decode attention over the mixed-format pages
+ *   ekv_append_decode_attn  both of them as one launch (the decode step of a layer)
  *   ekv_canary_kl    the canary: KL between FP16 attention over the ring and its
- *                    2/4/8-bit quantize-dequantize copies
+ *                    2/4/8-bit quantize-dequantize copies (ekv_canary_kl_layers:
+ *                    every layer of a step in one launch)
  *   ekv_tier_update  EMA of the canary readings and lowest-bit-under-tau tier pick
+ * and, around them: the KIVI-style asymmetric quantizer as a per-handle option
+ * (ekv_config.quantizer), and the static-artifact mode's frozen clipping
+ * thresholds (ekv_set_clip), percentile select (ekv_abs_percentile) and AutoK
+ * layer allocator (ekv_autok).
  *
  * Sources of the operations (page title, section):
  *   - "EchoKV: watching a language model decide its own precision":
