@@ -40,6 +40,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "quantized-KV decode attn HBM GB/s (% of peak), tokens/s; canary µs/firing"
+L2_BYTES = 129 * 2 ** 20        # GB300 L2
 
 # DRAM bytes (read + write) per decode-attention launch from one ncu capture
 # (profiles/decode_attn_llama70b_128k.md: 2-layer case, the same per-launch
@@ -288,6 +289,15 @@ def main():
     NR = max(1, a.rotate)
     if K % NR:
         raise SystemExit("--steps must be a multiple of --rotate")
+    # Timed steps must read from HBM: the caches the steps rotate over must hold
+    # well over L2's worth of pages (estimate at the initial tiers).
+    est = sum(-(-t // 16) * w.num_kv_heads * ekv.page_bytes(w.k_bits_init[l], w.v_bits[l],
+                                                             w.head_dim, w.asym)
+              for l in range(w.num_layers) for t in w.prefill)
+    if NR * est < 1.5 * L2_BYTES:
+        need = int(-(-1.5 * L2_BYTES // est))
+        raise SystemExit(f"{NR} cache(s) of {est / 1e6:.1f} MB of pages are under 1.5 times "
+                         f"the {L2_BYTES / 1e6:.0f} MB L2: use --rotate >= {need}")
     slots = torch.arange(w.batch, dtype=torch.int32, device=dev)
     caches = []
     t0 = time.perf_counter()
@@ -565,7 +575,8 @@ def main():
                    "l2": (f"inputs larger than L2: {step_bytes / 1e9:.2f} GB of pages read per step"
                           if NR == 1 else
                           f"steps rotate over {NR} caches of {step_bytes / 1e9:.3f} GB of pages "
-                          f"each ({NR * step_bytes / 1e6:.0f} MB > L2)"),
+                          f"each ({NR * step_bytes / 1e6:.0f} MB, over 1.5 times the "
+                          f"{L2_BYTES / 1e6:.0f} MB L2)"),
                    "parallelism": f"replicas x{world} (one sequence set per GPU)",
                    "graph": "CUDA graph of the timed steps", "canary_fires_in_timed": fired_A,
                    "step": ("one fused append + attention launch per layer" if fused
