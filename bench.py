@@ -148,6 +148,33 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def hold_gpu(us: float = 200.0) -> None:
+    """Queue a short device-side sleep on the current stream right before a timed
+    region's start event, so the region's work is already submitted when the
+    event fires and host submission latency stays out of the device timing."""
+    import torch
+    torch.cuda._sleep(int(us * 2e3))  # ~2 GHz SM clock: cycles for `us` microseconds
+
+
+def graph_upload(g, stream) -> bool:
+    """Upload a captured graph to the device before it is timed (cuGraphUpload),
+    so its first replay does not pay the upload; False when this torch does not
+    expose the executable graph."""
+    import ctypes
+    get = getattr(g, "raw_cuda_graph_exec", None)
+    if get is None:
+        return False
+    try:
+        handle = get()
+        cu = ctypes.CDLL("libcuda.so.1")
+        cu.cuGraphUpload.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+        ok = cu.cuGraphUpload(ctypes.c_void_p(int(handle)), ctypes.c_void_p(stream.cuda_stream)) == 0
+        stream.synchronize()
+        return ok
+    except Exception:  # noqa: BLE001
+        return False
+
+
 def attn_bytes_per_layer(cache, w, layer: int) -> float:
     """Algorithmic bytes one decode-attention launch reads and writes for a layer."""
     from mixed_precision_quantized_gb300 import ekv
@@ -289,6 +316,8 @@ def main():
     NR = max(1, a.rotate)
     if K % NR:
         raise SystemExit("--steps must be a multiple of --rotate")
+    if W < NR:
+        raise SystemExit("--warmup must cover every rotated cache (>= --rotate)")
     # Timed steps must read from HBM: the caches the steps rotate over must hold
     # well over L2's worth of pages (estimate at the initial tiers).
     est = sum(-(-t // 16) * w.num_kv_heads * ekv.page_bytes(w.k_bits_init[l], w.v_bits[l],
@@ -353,10 +382,13 @@ def main():
     stream = torch.cuda.Stream(device=dev)
     stream.wait_stream(torch.cuda.current_stream())
 
+    uploaded = []
+
     def capture(fn):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             fn()
+        uploaded.append(graph_upload(g, stream))
         return g
 
     # ---- A: K steps as one graph -------------------------------------------------
@@ -370,6 +402,7 @@ def main():
     clk = Clocks(local).__enter__()
     replicas.barrier(R)
     with torch.cuda.stream(stream):
+        hold_gpu()  # the GPU is busy while the host submits what follows
         ev0.record(stream)
         gA.replay()
         ev1.record(stream)
@@ -394,6 +427,7 @@ def main():
         replicas.barrier(R)
         with torch.cuda.stream(stream):
             f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            hold_gpu()  # the GPU is busy while the host submits what follows
             f0.record(stream)
             gA2.replay()
             f1.record(stream)
@@ -456,6 +490,7 @@ def main():
     with torch.cuda.stream(stream):
         gC.replay()
         c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        hold_gpu()  # the GPU is busy while the host submits what follows
         c0.record(stream)
         for _ in range(reps):
             gC.replay()
@@ -481,6 +516,7 @@ def main():
     with torch.cuda.stream(stream):
         gD.replay()
         d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        hold_gpu()  # the GPU is busy while the host submits what follows
         d0.record(stream)
         for _ in range(5):
             gD.replay()
@@ -532,6 +568,7 @@ def main():
         replicas.barrier(R)
         with torch.cuda.stream(stream):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            hold_gpu()  # the GPU is busy while the host submits what follows
             e0.record(stream)
             gE.replay()
             e1.record(stream)
@@ -578,7 +615,10 @@ def main():
                           f"each ({NR * step_bytes / 1e6:.0f} MB, over 1.5 times the "
                           f"{L2_BYTES / 1e6:.0f} MB L2)"),
                    "parallelism": f"replicas x{world} (one sequence set per GPU)",
-                   "graph": "CUDA graph of the timed steps", "canary_fires_in_timed": fired_A,
+                   "graph": ("CUDA graph of the timed steps, uploaded before timing"
+                             if uploaded and all(uploaded) else
+                             "CUDA graph of the timed steps (first replay includes its upload)"),
+                   "canary_fires_in_timed": fired_A,
                    "step": ("one fused append + attention launch per layer" if fused
                             else "append and attention launches per layer")
                            + ("; static artifact: calibrated per-layer K bits and clipping "
