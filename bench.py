@@ -74,6 +74,10 @@ def parse():
                         "the workload's first --calib-tokens prefill tokens, load them, and "
                         "time the same step with the canary off")
     p.add_argument("--calib-tokens", type=int, default=8192)
+    p.add_argument("--tau-ctx0", type=int, default=0,
+                   help="controller budget tau * sqrt(L / tau_ctx0) (0: plain tau)")
+    p.add_argument("--hysteresis", type=float, default=0.0, help="controller demotion margin")
+    p.add_argument("--vote", type=int, default=1, help="consecutive firings a tier change needs")
     p.add_argument("--asym", action="store_true",
                    help="KIVI-style asymmetric quantizer for the pages and the canary")
     p.add_argument("--separate", action="store_true",
@@ -331,7 +335,8 @@ def main():
     caches = []
     t0 = time.perf_counter()
     for _ in range(NR):
-        caches.append(ekv.cache_for(w, device=dev))
+        caches.append(ekv.cache_for(w, device=dev, tau_ctx0=a.tau_ctx0,
+                                    hysteresis=a.hysteresis, vote=a.vote))
         if static is not None:
             art.apply(caches[-1])
         runner.prefill(caches[-1], w, slots, device=dev)
@@ -619,6 +624,8 @@ def main():
                              if uploaded and all(uploaded) else
                              "CUDA graph of the timed steps (first replay includes its upload)"),
                    "canary_fires_in_timed": fired_A,
+                   "controller": {"tau_ctx0": a.tau_ctx0, "hysteresis": a.hysteresis,
+                                  "vote": a.vote},
                    "step": ("one fused append + attention launch per layer" if fused
                             else "append and attention launches per layer")
                            + ("; static artifact: calibrated per-layer K bits and clipping "

@@ -387,9 +387,11 @@ def autok(sensitivity, frac: float):
     return k.value, list(order[:n])
 
 
-def cache_for(w, device=None, max_seqs: int | None = None, torch_alloc: bool = True) -> Cache:
-    """A cache sized for a `workloads.Workload`."""
+def cache_for(w, device=None, max_seqs: int | None = None, torch_alloc: bool = True,
+              **controller) -> Cache:
+    """A cache sized for a `workloads.Workload`; `controller` passes the
+    controller variants (tau_ctx0, hysteresis, vote)."""
     return Cache(w.num_layers, max_seqs or w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim,
                  w.max_seq_len, w.pool_pages(), w.k_bits_init, w.v_bits, alpha=w.alpha,
                  tau=w.tau, device=device, torch_alloc=torch_alloc,
-                 asym=getattr(w, "asym", False))
+                 asym=getattr(w, "asym", False), **controller)
