@@ -73,15 +73,18 @@ class Run:
     """A workload on the GPU next to its oracle."""
 
     def __init__(self, w: workloads.Workload, steps: int, layers=None, seqs=None, heads=None,
-                 gen_device="cuda", trace=None, pool_pages=None, fused=False, clips=None):
+                 gen_device="cuda", trace=None, pool_pages=None, fused=False, clips=None,
+                 max_seq_len=None):
         """clips: {layer: (K thresholds [Hkv, d], V thresholds [Hkv])} loaded into
-        the cache before the prefill and given to the oracle."""
+        the cache before the prefill and given to the oracle.  max_seq_len: the
+        cache's capacity per sequence (default the workload's need)."""
         self.w, self.steps, self.fused = w, steps, fused
-        if pool_pages is None:
+        if pool_pages is None and max_seq_len is None:
             self.cache = ekv.cache_for(w)
         else:
             self.cache = ekv.Cache(w.num_layers, w.batch, w.num_q_heads, w.num_kv_heads,
-                                   w.head_dim, w.max_seq_len, pool_pages, w.k_bits_init,
+                                   w.head_dim, max_seq_len or w.max_seq_len,
+                                   pool_pages or w.pool_pages(), w.k_bits_init,
                                    w.v_bits, alpha=w.alpha, tau=w.tau,
                                    asym=getattr(w, "asym", False))
         for l, (kc, vc) in (clips or {}).items():

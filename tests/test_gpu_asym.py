@@ -102,3 +102,12 @@ def test_clipping_thresholds_unsupported_with_the_asymmetric_quantizer():
         assert raw.shape[1] == ekv.page_bytes(16, 16, 64, asym=True)
     finally:
         cache.close()
+
+
+@FUSED
+def test_more_units_than_sms_two_ctas_per_sm(fused):
+    """160 (sequence, head) units: the packed two-CTA launch on asymmetric pages."""
+    w = workloads.llama8b_batch32().scaled(num_layers=1, batch=20,
+                                           prefill=[5 + 13 * i for i in range(20)], steps=6,
+                                           asym=True)
+    _full_run(w, 6, fused)

@@ -284,3 +284,20 @@ def test_more_units_than_sms_two_ctas_per_sm(fused):
     w = workloads.llama8b_batch32().scaled(num_layers=1, batch=20,
                                            prefill=[5 + 13 * i for i in range(20)], steps=6)
     _full_run(w, 6, fused=fused)
+
+
+@FUSED
+def test_two_ctas_per_sm_with_split_merges(fused):
+    """160 units with a 40K-token capacity: the page table of a split holds 2,048
+    entries in the two-CTA configuration, so each unit takes 3 splits (most of
+    them empty for these short sequences) and the split merge runs."""
+    w = workloads.llama8b_batch32().scaled(num_layers=1, batch=20,
+                                           prefill=[5 + 13 * i for i in range(20)], steps=5)
+    r = Run(w, 5, fused=fused, max_seq_len=40000)
+    try:
+        for _ in range(5):
+            r.step()
+        r.check_all_pages()
+    finally:
+        r.close()
+

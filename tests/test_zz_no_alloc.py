@@ -89,3 +89,25 @@ def test_noalloc_rejects_requests_beyond_its_scratch():
         cache.sync()
     finally:
         cache.close()
+
+
+def test_two_ctas_per_sm_allocation_free_entry_point():
+    """The allocation-free attention under the two-CTA configuration matches the
+    handle's own."""
+    w = workloads.llama8b_batch32().scaled(num_layers=1, batch=20,
+                                           prefill=[40 + 9 * i for i in range(20)], steps=1)
+    cache = ekv.cache_for(w)
+    try:
+        slots = torch.arange(w.batch, dtype=torch.int32, device="cuda")
+        runner.prefill(cache, w, slots)
+        q = w.step_q(0, 0, 1, device="cuda")[:, 0].contiguous()
+        a = torch.empty_like(q)
+        b = torch.empty_like(q)
+        cache.decode_attn(0, slots, q, a)
+        cache.decode_attn_noalloc(0, slots, q, b)
+        cache.sync()
+        x = a.float().cpu().numpy().astype(np.float64)
+        y = b.float().cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(x - y) <= 2e-3 + 1e-2 * np.abs(x))
+    finally:
+        cache.close()
