@@ -203,32 +203,42 @@ def attn_bytes_per_layer(cache, w, layer: int) -> float:
     return total
 
 
-def cpu_baseline(w, sample_layers: int, device):
-    """Time the oracle (as it stands) on a bounded sample of one decode step."""
+def cpu_baseline(w, sample_layers: int, device, steps: int = 1, warmup: int = 1):
+    """Time the oracle (as it stands) on a bounded sample of the decode steps:
+    `warmup` untimed then `steps` timed steps over the first `sample_layers`
+    layers (append + attention of every sequence and head), scaled to all
+    layers."""
     import numpy as np  # noqa: F401
     from oracle import decoder
     layers = list(range(min(sample_layers, w.num_layers)))
+    if warmup + steps > w.steps:
+        raise SystemExit(f"workload holds {w.steps} decode steps; asked for {warmup + steps}")
     tr = decoder.Trace()
     tr.tiers = [list(w.k_bits_init)] * (w.steps + 1)
     ref = decoder.ReferenceRun(w, tr, layers=layers, device=device)
     ref.prefill()
-    ref.advance()                      # step 0 (untimed: fills sealed-block memo)
-    for l in layers:
-        for s in ref.seqs:
-            ref.attend(l, s)
+
+    def step():
+        ref.advance()
+        for l in layers:
+            for s in ref.seqs:
+                ref.attend(l, s)
+
+    for _ in range(max(1, warmup)):    # untimed (the first fills the sealed-block memo)
+        step()
     c0, t0 = time.process_time(), time.perf_counter()
-    ref.advance()                      # step 1, timed: append + attention
-    for l in layers:
-        for s in ref.seqs:
-            ref.attend(l, s)
+    for _ in range(steps):
+        step()
     wall = time.perf_counter() - t0
     cpu = time.process_time() - c0
-    per_step = wall * w.num_layers / len(layers)
+    per_step = wall / steps * w.num_layers / len(layers)
     return {"value": w.batch / per_step, "unit": "tokens/s",
             "cores": round(max(1.0, cpu / wall), 1), "kind": "oracle",
-            "sample": f"{len(layers)} of {w.num_layers} layers of one decode step at the full "
-                      f"context, all {w.batch} sequence(s) and heads; per-step time scaled by "
-                      f"{w.num_layers / len(layers):g}; wall {wall:.2f} s",
+            "sample": f"{len(layers)} of {w.num_layers} layers of {steps} decode step(s) at the "
+                      f"full context after {max(1, warmup)} untimed, all {w.batch} sequence(s) "
+                      f"and heads; per-step time scaled by {w.num_layers / len(layers):g}; "
+                      f"wall {wall:.2f} s",
+            "ms_per_step": 1e3 * per_step, "steps": steps, "warmup": max(1, warmup),
             "host": os.uname().machine, "nproc": os.cpu_count()}
 
 
@@ -256,9 +266,10 @@ def main():
         if rank != 0:
             return
         dev = "cuda:0" if torch.cuda.is_available() else "cpu"
-        cb = cpu_baseline(w, a.cpu_sample_layers, dev)
+        cb = cpu_baseline(w, a.cpu_sample_layers, dev, steps=a.steps, warmup=a.warmup)
         line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "tokens/s",
-                "n_gpus": 0, "steps": 1, "warmup": 1, "ms_per_step": 1e3 * w.batch / cb["value"],
+                "n_gpus": 0, "steps": cb["steps"], "warmup": cb["warmup"],
+                "ms_per_step": cb["ms_per_step"],
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f64", "data": "synthetic",
                 "config": {"workload": w.name}, "cpu_baseline": cb,
