@@ -553,31 +553,59 @@ def main():
         host_in = torch.stack(per_step).cpu().pin_memory()
         del per_step, inpE
         nq, nkv = B * w.num_q_heads * w.head_dim, B * w.num_kv_heads * w.head_dim
-        dbuf = torch.empty(host_in.shape[1], dtype=torch.float16, device=dev)
-        qd_all = dbuf[:L * nq].view(L, B, w.num_q_heads, w.head_dim)
-        qd = [qd_all[l] for l in range(L)]
-        kd = [dbuf[L * nq + l * nkv:L * nq + (l + 1) * nkv].view(B, 1, w.num_kv_heads, w.head_dim)
-              for l in range(L)]
-        vd = [dbuf[L * (nq + nkv) + l * nkv:L * (nq + nkv) + (l + 1) * nkv]
-              .view(B, 1, w.num_kv_heads, w.head_dim) for l in range(L)]
+        # Double-buffered: step n+1's inputs are uploaded and step n's outputs
+        # read back on a copy stream while step n computes; every step still
+        # pays its own host copies.
+        def views(buf):
+            qa = buf[:L * nq].view(L, B, w.num_q_heads, w.head_dim)
+            ks = [buf[L * nq + l * nkv:L * nq + (l + 1) * nkv]
+                  .view(B, 1, w.num_kv_heads, w.head_dim) for l in range(L)]
+            vs = [buf[L * (nq + nkv) + l * nkv:L * (nq + nkv) + (l + 1) * nkv]
+                  .view(B, 1, w.num_kv_heads, w.head_dim) for l in range(L)]
+            return qa, ks, vs
+
+        dbufs = [torch.empty(host_in.shape[1], dtype=torch.float16, device=dev) for _ in range(2)]
+        dviews = [views(b) for b in dbufs]
+        obufs = [torch.empty_like(out) for _ in range(2)]
         host_out = torch.empty(K, *out.shape, dtype=torch.float16).pin_memory()
+        cs = torch.cuda.Stream(device=dev)
+        ev_in = [torch.cuda.Event() for _ in range(K)]
+        ev_done = [torch.cuda.Event() for _ in range(K)]
+        ev_out = [torch.cuda.Event() for _ in range(K)]
 
         def e2e_steps():
+            cs.wait_stream(stream)
+            with torch.cuda.stream(cs):
+                dbufs[0].copy_(host_in[0], non_blocking=True)
+                ev_in[0].record(cs)
             for n in range(K):
-                i = s0 + n
+                i, b = s0 + n, n % 2
                 c = C(i)
-                dbuf.copy_(host_in[n], non_blocking=True)
+                qa, ks, vs = dviews[b]
+                stream.wait_event(ev_in[n])
+                if n >= 2:
+                    stream.wait_event(ev_out[n - 2])      # obufs[b] read back
                 for l in range(L):
                     if fused:
-                        c.append_decode_attn(l, slots, kd[l], vd[l], qd[l], outs[l],
+                        c.append_decode_attn(l, slots, ks[l], vs[l], qa[l], obufs[b][l],
                                              after_other_layer=l > 0)
                     else:
-                        c.append(l, slots, kd[l], vd[l])
-                        c.decode_attn(l, slots, qd[l], outs[l])
+                        c.append(l, slots, ks[l], vs[l])
+                        c.decode_attn(l, slots, qa[l], obufs[b][l])
                 if w.fires(i):
-                    canary(c, qd_all)
+                    canary(c, qa)
                     fire_end(c)
-                host_out[n].copy_(out, non_blocking=True)
+                ev_done[n].record(stream)
+                with torch.cuda.stream(cs):
+                    if n + 1 < K:
+                        if n >= 1:
+                            cs.wait_event(ev_done[n - 1])  # dbufs[1 - b] consumed
+                        dbufs[1 - b].copy_(host_in[n + 1], non_blocking=True)
+                        ev_in[n + 1].record(cs)
+                    cs.wait_event(ev_done[n])
+                    host_out[n].copy_(obufs[b], non_blocking=True)
+                    ev_out[n].record(cs)
+            stream.wait_stream(cs)
 
         gE = capture(e2e_steps)
         torch.cuda.synchronize()
