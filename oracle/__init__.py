@@ -5,9 +5,13 @@ computes, written from the three pages it follows:
 
   * "EchoKV: watching a language model decide its own precision" — the FP16
     K_ref ring, the canary KL, the EMA and the lowest-bit-under-tau pick, and
-    forward-only (admit-time) tier changes;
+    forward-only (admit-time) tier changes; the KIVI-style asymmetric
+    quantizer (`quant.quantize_asym`); the controller variants and the
+    majority vote over ranks (`controller`);
   * "Behavior-Guided KV-Cache Quantization" — K quantized per channel, V per
-    token, symmetric; packed low-bit storage; GQA head mapping;
+    token, symmetric; packed low-bit storage; GQA head mapping; the
+    static-artifact mode (percentile clipping thresholds, role-specific
+    candidate scores, AutoK layer allocation: `artifacts`);
   * "KV-Kaizen" — symmetric uniform quantization, bits-per-token accounting.
 
 Only `tests/`, `__graft_entry__.smoke()` and `bench.py`'s CPU-baseline leg
