@@ -159,3 +159,54 @@ def test_pool_sizing_covers_growth():
     need = w.pool_pages()
     assert need[(4, 4)] == 80 * 8 * (8192 + 32)
     assert need[(2, 4)] == need[(8, 4)] == 80 * 8 * 32
+
+
+def _ragged_small():
+    # three sequences, one shorter than the ring that grows past it during the
+    # steps, one whose window straddles the prefill/decode boundary
+    return workloads.llama8b_batch32().scaled(num_layers=2, batch=3, prefill=[37, 80, 130],
+                                               steps=30)
+
+
+@pytest.mark.parametrize("make", [workloads.tiny, _ragged_small], ids=["tiny", "ragged"])
+def test_layer_windows_equal_the_appended_ring(make):
+    # layer_windows regenerates each ring window from the seeded draws; it must
+    # equal the ring a step-by-step run holds after each step's append: the
+    # newest min(T, 64) K's, oldest first, this step's K included ("EchoKV",
+    # "Show the math" and "Do we store the whole cache in FP16? -- No.").
+    w = make()
+    tr = decoder.Trace()
+    tr.tiers = [list(w.k_bits_init)] * (w.steps + 1)
+    ref = decoder.ReferenceRun(w, tr)
+    ref.prefill()
+    for t in range(w.steps):
+        ref.advance()
+        for l in range(w.num_layers):
+            wins = decoder.layer_windows(w, l, t)
+            assert len(wins) == w.batch
+            for i, s in enumerate(ref.seqs):
+                want = ref.state[(l, s)].window().transpose(1, 0, 2)    # [Hkv, n, d]
+                assert wins[i].shape == (w.num_kv_heads, min(64, w.prefill[s] + t + 1),
+                                         w.head_dim)
+                assert np.array_equal(wins[i], want)
+
+
+def test_layer_windows_newest_is_this_steps_k_and_oldest_is_64_back():
+    w = _ragged_small()
+    l, t = 1, 5
+    wins = decoder.layer_windows(w, l, t)
+    k_step, _ = w.step_kv(l, t, 1)                      # [B, 1, Hkv, d]
+    for s in range(w.batch):
+        T = w.prefill[s] + t + 1
+        newest = wins[s][:, -1]                          # [Hkv, d]
+        assert np.array_equal(newest, k_step[s, 0].numpy())
+        k_first, _ = w.prefill_kv(l, [s], tok0=[max(0, T - 64)], n_tok=1)
+        assert np.array_equal(wins[s][:, 0], k_first[0, 0].numpy())
+    # a window one step behind, or one that drops this step's K, differs
+    behind = decoder.layer_windows(w, l, t - 1)
+    for s in range(w.batch):
+        assert not np.array_equal(behind[s][:, -1], wins[s][:, -1])
+    short = wins[0]                                       # 37 + 6 = 43 tokens, under 64
+    assert short.shape[1] == 43
+    k_all, _ = w.prefill_kv(l, [0], n_tok=37)
+    assert np.array_equal(short[:, :37], k_all[0].permute(1, 0, 2).numpy())
