@@ -874,7 +874,16 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
 
   const int32_t* bt = st.bt + lsh_index(st, layer, slot_ok ? slot : 0, h) * st.maxblk;
   const __half* stg = st.staging + lsh_index(st, layer, slot_ok ? slot : 0, h) * (BLOCK * D);
-  for (int i = tid; i < np; i += NT) s_bt[i] = bt[b0 + i];
+  // Copy the split's page-table entries and check whether every pipelined page
+  // has one format (the common case: a layer whose tier did not change over the
+  // split's range); such a split runs a loop specialized to that format.
+  const int32_t e_first = np > 0 ? bt[b0] : -1;
+  int mixed = 0;
+  for (int i = tid; i < np; i += NT) {
+    const int32_t e = bt[b0 + i];
+    s_bt[i] = e;
+    mixed |= (e == -1) | (((uint32_t)(e ^ e_first) >> 28) != 0);
+  }
   if (tid == 0) s_next = 0;
 
   // Q fragment words for head g of the group, paired like the K codes of the
@@ -913,21 +922,33 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
     for (int i = 0; i < ns; ++i) mbar_init(bar0 + 8 * i, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  __syncthreads();  // page-table copy, counter and barriers ready
+  // page-table copy, counter and barriers ready
+  const bool uniform = !__syncthreads_or(mixed) && np > 0 && e_first != -1;
 
   // Lane i < ns holds `pg`, the split page index in stage i (-1: none).  Stages
   // are filled in the order the counter hands pages out and consumed in the same
   // ring order, so the pages still to come are a prefix of the ring.  A page
   // whose table entry is missing (-1) is flagged and neither copied nor read.
+  // The pool of a uniform split's pages (its only format).
+  const int fmt_u = uniform ? entry_fmt(e_first) : 0;
+  const uint32_t bytes_u = (uint32_t)st.pool_page_bytes[fmt_u];
+  const uint8_t* base_u = st.pool_base[fmt_u];
   auto issue = [&](int si, int k) {  // one lane: page k -> stage si
     const int32_t e = s_bt[k];
-    if (e == -1) {
-      set_error(st, EKV_ESTATE);
-      return;
+    uint32_t bytes;
+    const uint8_t* src;
+    if (uniform) {
+      bytes = bytes_u;
+      src = base_u + (size_t)entry_idx(e) * bytes_u;
+    } else {
+      if (e == -1) {
+        set_error(st, EKV_ESTATE);
+        return;
+      }
+      const int fmt = entry_fmt(e);
+      bytes = (uint32_t)st.pool_page_bytes[fmt];
+      src = st.pool_base[fmt] + (size_t)entry_idx(e) * bytes;
     }
-    const int fmt = entry_fmt(e);
-    const uint32_t bytes = (uint32_t)st.pool_page_bytes[fmt];
-    const uint8_t* src = st.pool_base[fmt] + (size_t)entry_idx(e) * bytes;
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     mbar_expect_tx(bar0 + 8 * si, bytes);
     bulk_g2s(wbase + si * stage_bytes, src, bytes, bar0 + 8 * si);
@@ -979,63 +1000,99 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   // already in flight, so none lands after it exits.
   uint32_t phases = 0;
   bool ok = true;
-  auto ready = [&](int k, int si) -> int32_t {  // entry of page k once its stage landed
-    if (k < 0) return -1;
-    const int32_t e = s_bt[k];
-    if (e == -1) return -1;
-    // warp-uniform outcome: the MMAs that follow need every lane
+  // Wait for stage si (warp-uniform outcome: the MMAs that follow need every lane).
+  auto wait_stage = [&](int si) {
     if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * si, (phases >> si) & 1)) && ok) {
       ok = false;
       if (lane == 0) set_error(st, EKV_ETIMEOUT);
     }
     phases ^= 1u << si;
-    return ok ? e : -1;
   };
-  int sidx = 0;
-  while (true) {
-    const int s0 = sidx, s1 = (sidx + 1 == ns) ? 0 : sidx + 1;
-    const int ka = __shfl_sync(0xffffffffu, pg, s0);
-    if (ka < 0) break;
-    const int kb = __shfl_sync(0xffffffffu, pg, s1);
-    const int32_t ea = ready(ka, s0);
-    const int32_t eb = ready(kb, s1);
-    const uint8_t* sa = wptr + s0 * stage_bytes;
-    const uint8_t* sb = wptr + s1 * stage_bytes;
-    const int kba = ea != -1 ? bits_of_code(entry_fmt(ea) >> 2) : 0;
-    const int kbb = eb != -1 ? bits_of_code(entry_fmt(eb) >> 2) : 0;
-    if (kba != 0 && kba == kbb) {  // the common case: both pages share a K width
-      with_kbits(kba, [&](auto kbc) {
-        constexpr int KB = decltype(kbc)::value;
-        constexpr int KP = k_part_bytes(KB, D, ASYM);
-        pair_q(kbc);
-        attend_pages<D, VB, true, KB>(SLd{sa}, SLd{sa + KP}, BLOCK, SLd{sb}, SLd{sb + KP},
-                                      BLOCK, qw, A, sl, g, c);
-      });
-    } else {  // one page at a time, through one call site per K width
-#pragma unroll 1
-      for (int pass = 0; pass < 2; ++pass) {
-        const int kbx = pass ? kbb : kba;
-        if (kbx == 0) continue;
-        const uint8_t* x = pass ? sb : sa;
-        with_kbits(kbx, [&](auto kbc) {
-          constexpr int KB = decltype(kbc)::value;
-          pair_q(kbc);
-          attend_pages<D, VB, true, KB>(SLd{x}, SLd{x + k_part_bytes(KB, D, ASYM)}, BLOCK, SLd{x},
-                                        SLd{x}, 0, qw, A, sl, g, c);
-        });
-      }
-    }
-    __syncwarp();
-    // Refill both stages with the split's next two pages (none once the pages
-    // ran out or a wait failed); lanes 0 and 1 issue the two copies.
+  // Refill stages s0 and s1 with the split's next two pages (none once the pages
+  // ran out or a wait failed); lanes 0 and 1 issue the two copies.
+  auto refill = [&](int s0, int s1, bool more) {
     int kn = np;
-    if (lane == 0 && ok && kb >= 0) kn = atomicAdd(&s_next, 2);
+    if (lane == 0 && ok && more) kn = atomicAdd(&s_next, 2);
     kn = __shfl_sync(0xffffffffu, kn, 0);
     if (lane == s0) pg = kn < np ? kn : -1;
     if (lane == s1) pg = kn + 1 < np ? kn + 1 : -1;
-    if (lane == 0 && kn < np) issue(s0, kn);
-    if (lane == 1 && kn + 1 < np) issue(s1, kn + 1);
-    sidx = (s1 + 1 == ns) ? 0 : s1 + 1;
+    if (lane < 2 && kn + lane < np) issue(lane ? s1 : s0, kn + lane);
+  };
+  int sidx = 0;
+  if (uniform) {
+    // Every pipelined page of this split has format fmt_u: one K width, one
+    // stage layout, no per-page format decode.
+    with_kbits(bits_of_code(fmt_u >> 2), [&](auto kbc) {
+      constexpr int KB = decltype(kbc)::value;
+      constexpr int KP = k_part_bytes(KB, D, ASYM);
+      pair_q(kbc);
+      while (true) {
+        const int s0 = sidx, s1 = (sidx + 1 == ns) ? 0 : sidx + 1;
+        const int ka = __shfl_sync(0xffffffffu, pg, s0);
+        if (ka < 0) break;
+        const int kb = __shfl_sync(0xffffffffu, pg, s1);
+        wait_stage(s0);
+        if (kb >= 0) wait_stage(s1);
+        const uint8_t* sa = wptr + s0 * stage_bytes;
+        const uint8_t* sb = wptr + s1 * stage_bytes;
+        if (ok) {
+          if (kb >= 0)
+            attend_pages<D, VB, true, KB>(SLd{sa}, SLd{sa + KP}, BLOCK, SLd{sb}, SLd{sb + KP},
+                                          BLOCK, qw, A, sl, g, c);
+          else
+            attend_pages<D, VB, true, KB>(SLd{sa}, SLd{sa + KP}, BLOCK, SLd{sa}, SLd{sa}, 0, qw,
+                                          A, sl, g, c);
+        }
+        __syncwarp();
+        refill(s0, s1, kb >= 0);
+        sidx = (s1 + 1 == ns) ? 0 : s1 + 1;
+      }
+    });
+  } else {
+    auto ready = [&](int k, int si) -> int32_t {  // entry of page k once its stage landed
+      if (k < 0) return -1;
+      const int32_t e = s_bt[k];
+      if (e == -1) return -1;
+      wait_stage(si);
+      return ok ? e : -1;
+    };
+    while (true) {
+      const int s0 = sidx, s1 = (sidx + 1 == ns) ? 0 : sidx + 1;
+      const int ka = __shfl_sync(0xffffffffu, pg, s0);
+      if (ka < 0) break;
+      const int kb = __shfl_sync(0xffffffffu, pg, s1);
+      const int32_t ea = ready(ka, s0);
+      const int32_t eb = ready(kb, s1);
+      const uint8_t* sa = wptr + s0 * stage_bytes;
+      const uint8_t* sb = wptr + s1 * stage_bytes;
+      const int kba = ea != -1 ? bits_of_code(entry_fmt(ea) >> 2) : 0;
+      const int kbb = eb != -1 ? bits_of_code(entry_fmt(eb) >> 2) : 0;
+      if (kba != 0 && kba == kbb) {  // both pages share a K width
+        with_kbits(kba, [&](auto kbc) {
+          constexpr int KB = decltype(kbc)::value;
+          constexpr int KP = k_part_bytes(KB, D, ASYM);
+          pair_q(kbc);
+          attend_pages<D, VB, true, KB>(SLd{sa}, SLd{sa + KP}, BLOCK, SLd{sb}, SLd{sb + KP},
+                                        BLOCK, qw, A, sl, g, c);
+        });
+      } else {  // one page at a time, through one call site per K width
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+          const int kbx = pass ? kbb : kba;
+          if (kbx == 0) continue;
+          const uint8_t* x = pass ? sb : sa;
+          with_kbits(kbx, [&](auto kbc) {
+            constexpr int KB = decltype(kbc)::value;
+            pair_q(kbc);
+            attend_pages<D, VB, true, KB>(SLd{x}, SLd{x + k_part_bytes(KB, D, ASYM)}, BLOCK,
+                                          SLd{x}, SLd{x}, 0, qw, A, sl, g, c);
+          });
+        }
+      }
+      __syncwarp();
+      refill(s0, s1, kb >= 0);
+      sidx = (s1 + 1 == ns) ? 0 : s1 + 1;
+    }
   }
   __syncthreads();  // every stage drained before the stage memory is reused
 
