@@ -347,6 +347,42 @@ EKV_API int ekv_read_pages(ekv_cache* cache, int32_t layer, int32_t seq_slot, in
                    int32_t first_block, int32_t n_blocks, void* dst, size_t dst_stride,
                    void* stream);
 
+/* ---- Realized precision ("EchoKV: watching a language model decide its own
+ * precision": the simulation's running "avg bits / element" and "memory saved
+ * vs FP16", and "What the controller costs you in memory"; "KV-Kaizen":
+ * "Action Space and Cost Model", c(a) = (d + d_R) * b bits per token against
+ * the 16-bit cost C0).  What the cache of layers first_layer ..
+ * first_layer+n_layers-1 holds over every sequence slot, one page per
+ * (layer, slot, KV head, 16-token block):
+ *   sealed_pages[f]  pages of format f whose block holds 16 tokens
+ *   open_pages[f]    pages of format f of a sequence's still-open last block
+ *   open_rows[f]     the tokens in those open blocks
+ *   tokens           cached (layer, slot, KV head) tokens
+ *   k_bits, v_bits   mean stored bits per cached K / V element: a page's K or V
+ *                    width; K rows of an open block count 16 (they are held raw
+ *                    in fp16 until the block seals)
+ *   cost_vs_c0       (k_bits + v_bits) / 32: the code bits against C0 (no rank
+ *                    truncation, d_R = 0)
+ *   page_bytes       bytes of the pages in use, scales and zero points included
+ *   fp16_bytes       the same tokens' K and V in fp16: tokens * head_dim * 4
+ *   saved_vs_fp16    1 - page_bytes / fp16_bytes
+ * Zero tokens give zero means.  Syncs stream; EKV_ESTATE if a block in use has
+ * no page. */
+typedef struct ekv_stats_t {
+  int64_t sealed_pages[EKV_NUM_FORMATS];
+  int64_t open_pages[EKV_NUM_FORMATS];
+  int64_t open_rows[EKV_NUM_FORMATS];
+  int64_t tokens;
+  double k_bits;
+  double v_bits;
+  double cost_vs_c0;
+  double page_bytes;
+  double fp16_bytes;
+  double saved_vs_fp16;
+} ekv_stats_t;
+EKV_API int ekv_stats(ekv_cache* cache, int32_t first_layer, int32_t n_layers, ekv_stats_t* out,
+                      void* stream);
+
 /* Free pages left in the pool of one format (syncs stream). */
 EKV_API int ekv_pool_free(ekv_cache* cache, int32_t format, int64_t* out, void* stream);
 

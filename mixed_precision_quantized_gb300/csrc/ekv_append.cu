@@ -159,6 +159,38 @@ __global__ void read_pages_kernel(DevState st, int layer, int slot, int h, int f
     reinterpret_cast<uint4*>(dst + (size_t)i * stride)[c] = reinterpret_cast<const uint4*>(page)[c];
 }
 
+// Page census of layers l0 .. l0 + gridDim.x / S - 1: one CTA per (layer, slot).
+// cnt (dev uint64 [3 * NFMT + 1], zeroed by the caller): sealed pages per format,
+// open pages per format (a sequence's last block while it holds under 16
+// tokens), the tokens of those open blocks per format, and blocks in use
+// without a page.
+__global__ void stats_kernel(DevState st, int l0, unsigned long long* cnt) {
+  __shared__ unsigned long long sc[3 * NFMT + 1];
+  const int l = l0 + blockIdx.x / st.S, s = blockIdx.x % st.S;
+  for (int i = threadIdx.x; i <= 3 * NFMT; i += blockDim.x) sc[i] = 0;
+  __syncthreads();
+  const int T = st.len[ls_index(st, l, s)];
+  const int nb = (T + BLOCK - 1) / BLOCK, open = T % BLOCK;
+  for (int i = threadIdx.x; i < st.Hkv * nb; i += blockDim.x) {
+    const int h = i / nb, j = i % nb;
+    const int32_t e = st.bt[lsh_index(st, l, s, h) * st.maxblk + j];
+    if (e == -1) {  // a block in use must have a page
+      atomicAdd(&sc[3 * NFMT], 1ull);
+      continue;
+    }
+    const int f = entry_fmt(e);
+    if (open && j == nb - 1) {
+      atomicAdd(&sc[NFMT + f], 1ull);
+      atomicAdd(&sc[2 * NFMT + f], (unsigned long long)open);
+    } else {
+      atomicAdd(&sc[f], 1ull);
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i <= 3 * NFMT; i += blockDim.x)
+    if (sc[i]) atomicAdd(cnt + i, sc[i]);
+}
+
 __global__ void init_stack_kernel(int32_t* stack, int32_t n) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
     stack[i] = i;
@@ -186,6 +218,14 @@ cudaError_t launch_seq_reset(const DevState& st, int slot, cudaStream_t s) {
 cudaError_t launch_read_pages(const DevState& st, int layer, int slot, int h, int first, int n,
                               uint8_t* dst, size_t stride, cudaStream_t s) {
   read_pages_kernel<<<n, 128, 0, s>>>(st, layer, slot, h, first, dst, stride);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_stats(const DevState& st, int l0, int nl, unsigned long long* cnt,
+                         cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(cnt, 0, (3 * NFMT + 1) * sizeof(unsigned long long), s);
+  if (e != cudaSuccess) return e;
+  stats_kernel<<<nl * st.S, 256, 0, s>>>(st, l0, cnt);
   return cudaGetLastError();
 }
 

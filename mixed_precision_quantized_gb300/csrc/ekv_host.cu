@@ -16,6 +16,7 @@ struct ekv_cache {
   std::vector<void*> allocs;
   std::vector<int> vbits;   // host copy (fixed per layer)
   int num_sm = 0;
+  unsigned long long* census = nullptr;  // dev [3 * NFMT + 1], ekv_stats scratch
 };
 
 namespace {
@@ -209,6 +210,7 @@ int ekv_create(const ekv_config* cfg, const uint8_t* k_bits_init, const uint8_t*
   st.attn_ticket = (int32_t*)A(S * H * ATTN_TICKETS * 4);
   st.canary_part = (float*)A(L * S * H * 3 * 4);
   st.canary_ticket = (int32_t*)A(L * 4);
+  c->census = (unsigned long long*)A((3 * NFMT + 1) * sizeof(unsigned long long));
   if (!ok) {
     free_all(c);
     delete c;
@@ -461,6 +463,49 @@ int ekv_read_pages(ekv_cache* c, int32_t layer, int32_t seq_slot, int32_t kv_hea
   if (n_blocks == 0) return EKV_OK;
   return cuda_status(launch_read_pages(c->st, layer, seq_slot, kv_head, first_block, n_blocks,
                                        static_cast<uint8_t*>(dst), dst_stride, as_stream(stream)));
+}
+
+int ekv_stats(ekv_cache* c, int32_t first_layer, int32_t n_layers, ekv_stats_t* out,
+              void* stream) {
+  if (!c || !out || first_layer < 0 || n_layers <= 0 || first_layer + n_layers > c->st.L)
+    return EKV_EINVAL;
+  cudaStream_t s = as_stream(stream);
+  unsigned long long cnt[3 * NFMT + 1];
+  std::vector<int32_t> len((size_t)n_layers * c->st.S);
+  cudaError_t e = launch_stats(c->st, first_layer, n_layers, c->census, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(cnt, c->census, sizeof(cnt), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(len.data(), c->st.len + ls_index(c->st, first_layer, 0),
+                        len.size() * 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return EKV_ECUDA;
+  if (cnt[3 * NFMT] != 0) return EKV_ESTATE;  // blocks in use without a page
+  memset(out, 0, sizeof(*out));
+  const int D = c->st.D;
+  double kbits = 0, vbits = 0, bytes = 0;
+  int64_t tokens = 0;
+  for (int32_t t : len) tokens += (int64_t)t * c->st.Hkv;
+  for (int f = 0; f < NFMT; ++f) {
+    out->sealed_pages[f] = (int64_t)cnt[f];
+    out->open_pages[f] = (int64_t)cnt[NFMT + f];
+    out->open_rows[f] = (int64_t)cnt[2 * NFMT + f];
+    const int kb = bits_of_code(f >> 2), vb = bits_of_code(f & 3);
+    const double sealed_tok = (double)BLOCK * out->sealed_pages[f];
+    kbits += sealed_tok * kb + (double)out->open_rows[f] * 16;
+    vbits += (sealed_tok + (double)out->open_rows[f]) * vb;
+    bytes += (double)(out->sealed_pages[f] + out->open_pages[f]) * page_bytes(kb, vb, D, c->st.asym);
+  }
+  out->tokens = tokens;
+  if (tokens > 0) {
+    out->k_bits = kbits / (double)tokens;
+    out->v_bits = vbits / (double)tokens;
+    out->cost_vs_c0 = (out->k_bits + out->v_bits) / 32.0;
+    out->page_bytes = bytes;
+    out->fp16_bytes = (double)tokens * D * 4.0;
+    out->saved_vs_fp16 = 1.0 - bytes / out->fp16_bytes;
+  }
+  return EKV_OK;
 }
 
 int ekv_pool_free(ekv_cache* c, int32_t format, int64_t* out, void* stream) {

@@ -127,6 +127,11 @@ cudaError_t launch_seq_reset(const DevState& st, int slot, cudaStream_t s);
 cudaError_t launch_read_pages(const DevState& st, int layer, int slot, int h, int first, int n,
                               uint8_t* dst, size_t stride, cudaStream_t s);
 cudaError_t launch_init_stack(int32_t* stack, int32_t n, cudaStream_t s);
+// Page census of layers l0 .. l0+nl-1 into cnt (dev uint64 [3 * NFMT + 1]: sealed
+// pages, open pages and open-block tokens per format, then blocks in use without
+// a page); zeroes cnt first.
+cudaError_t launch_stats(const DevState& st, int l0, int nl, unsigned long long* cnt,
+                         cudaStream_t s);
 
 // Argument checks and launch plan of decode attention for a handle: a copy of
 // its device state, the split count and the layer's V bits.

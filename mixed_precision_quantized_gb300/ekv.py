@@ -46,6 +46,21 @@ class EkvConfig(ctypes.Structure):
     ]
 
 
+class EkvStats(ctypes.Structure):
+    _fields_ = [
+        ("sealed_pages", ctypes.c_int64 * NUM_FORMATS),
+        ("open_pages", ctypes.c_int64 * NUM_FORMATS),
+        ("open_rows", ctypes.c_int64 * NUM_FORMATS),
+        ("tokens", ctypes.c_int64),
+        ("k_bits", ctypes.c_double),
+        ("v_bits", ctypes.c_double),
+        ("cost_vs_c0", ctypes.c_double),
+        ("page_bytes", ctypes.c_double),
+        ("fp16_bytes", ctypes.c_double),
+        ("saved_vs_fp16", ctypes.c_double),
+    ]
+
+
 ALLOC_FN = ctypes.CFUNCTYPE(ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p)
 FREE_FN = ctypes.CFUNCTYPE(None, ctypes.c_void_p, ctypes.c_void_p)
 
@@ -72,6 +87,7 @@ _SIGS = {
     "ekv_block_table": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _I32, _P, _P]),
     "ekv_read_pages": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _I32, _P, ctypes.c_size_t, _P]),
     "ekv_pool_free": (ctypes.c_int, [_P, _I32, _P, _P]),
+    "ekv_stats": (ctypes.c_int, [_P, _I32, _I32, ctypes.POINTER(EkvStats), _P]),
     "ekv_sync": (ctypes.c_int, [_P, _P]),
     "ekv_state_size": (ctypes.c_int64, [_P]),
     "ekv_state_save": (ctypes.c_int, [_P, _P, ctypes.c_int64, _P]),
@@ -296,6 +312,18 @@ class Cache:
         _check(lib().ekv_get_state(self._h, t, e, d, v, _stream(stream)), "ekv_get_state")
         return {"tiers": list(t), "ema": [list(e[3 * i:3 * i + 3]) for i in range(L)],
                 "delta": [list(d[3 * i:3 * i + 3]) for i in range(L)], "ema_valid": list(v)}
+
+    def stats(self, first_layer: int = 0, n_layers: int | None = None, stream=None) -> dict:
+        """What the cache of the given layers holds (ekv_stats): pages per format,
+        mean stored K/V bits per element, page bytes against fp16."""
+        n = self.num_layers - first_layer if n_layers is None else n_layers
+        out = EkvStats()
+        _check(lib().ekv_stats(self._h, first_layer, n, ctypes.byref(out), _stream(stream)),
+               "ekv_stats")
+        d = {name: getattr(out, name) for name, _ in EkvStats._fields_}
+        for k in ("sealed_pages", "open_pages", "open_rows"):
+            d[k] = list(d[k])
+        return d
 
     def seq_len(self, layer: int, slot: int, stream=None) -> int:
         out = ctypes.c_int32()
