@@ -42,10 +42,10 @@ sys.path.insert(0, ROOT)
 METRIC = "quantized-KV decode attn HBM GB/s (% of peak), tokens/s; canary µs/firing"
 L2_BYTES = 129 * 2 ** 20        # GB300 L2
 
-# DRAM bytes (read + write) per decode-attention launch from one ncu capture
-# (profiles/decode_attn_llama70b_128k.md: 2-layer case, the same per-launch
-# work as one layer of the full workload), valid only for the kernel source it
-# was taken on: any change to that source reports null until re-captured.
+# DRAM bytes (read + write) per decode-attention launch from one ncu capture of
+# the 2-layer case of the 70B workload (the same per-launch work as one layer of
+# the full workload), valid only for the kernel source it was taken on: any
+# change to that source reports null until re-captured.
 TRAFFIC_BYTES = 157.29e6
 TRAFFIC_SOURCE_SHA = "079b9606b822290f"
 NOMINAL_HBM_GBS = 8000.0
@@ -82,6 +82,14 @@ def parse():
                    help="KIVI-style asymmetric quantizer for the pages and the canary")
     p.add_argument("--separate", action="store_true",
                    help="append and attention as two launches per layer (default: one fused launch)")
+    p.add_argument("--split", default="batch", choices=["batch", "heads"],
+                   help="several GPUs: each holds its own sequences (batch, weak scaling) or "
+                        "a share of every sequence's KV heads (heads, strong scaling)")
+    p.add_argument("--no-short", action="store_true",
+                   help="skip the extra 32K-context figure (Qwen2.5-14B shape) of the default run")
+    p.add_argument("--force-kbits", type=int, default=0,
+                   help="create the cache with every layer at this K width and keep the canary "
+                        "off (per-width measurement at the workload's context)")
     return p.parse_args()
 
 
@@ -242,6 +250,68 @@ def cpu_baseline(w, sample_layers: int, device, steps: int = 1, warmup: int = 1)
             "host": os.uname().machine, "nproc": os.cpu_count()}
 
 
+def amortized_region(t_region: float, fired: int, canary_s: float, steps: int,
+                     period: int) -> float:
+    """A timed region's time with the canary at its 1-in-`period` share: the
+    firings it happened to hold replaced by steps / period firings."""
+    if not period:
+        return t_region
+    return t_region - fired * canary_s + steps / period * canary_s
+
+
+def short_context_figure(dev, K: int = 16, W: int = 3) -> dict:
+    """The fused decode step at 32K context (Qwen2.5-14B shape: 48 layers, 40 q /
+    8 kv heads, K 2/4/8 mixed, V4): per-launch time and HBM fraction with and
+    without the overlap of consecutive layers, CUDA-graph replay, events on the
+    launching stream."""
+    import torch
+    from mixed_precision_quantized_gb300 import ekv, runner, workloads
+    w = workloads.qwen14b_32k()
+    L = w.num_layers
+    slots = torch.arange(w.batch, dtype=torch.int32, device=dev)
+    cache = ekv.cache_for(w, device=dev)
+    runner.prefill(cache, w, slots, device=dev)
+    inp = runner.Inputs(w, 0, W + 2 * K, device=dev)
+    outs = [torch.empty(w.batch, w.num_q_heads, w.head_dim, dtype=torch.float16, device=dev)
+            for _ in range(L)]
+    for i in range(W):
+        runner.decode_step(cache, w, slots, inp, i, outs, False, fused=True)
+    cache.sync()
+    stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream())
+    res = {}
+    for name, first, overlap in (("overlap", W, True), ("no_overlap", W + K, False)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(first, first + K):
+                runner.decode_step(cache, w, slots, inp, i, outs, False, fused=True,
+                                   overlap=overlap)
+        graph_upload(g, stream)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            hold_gpu()
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        cache.sync()
+        res[name] = e0.elapsed_time(e1) / 1e3
+        del g
+    nbytes = sum(attn_bytes_per_layer(cache, w, l) for l in range(L)) / L
+    peak, _ = peaks()
+    cache.close()
+    out = {"workload": f"{w.name}: {L} layers, batch 1, {w.num_q_heads} q / {w.num_kv_heads} kv "
+                       f"heads, d {w.head_dim}, {w.prefill[0]} cached tokens, K 2/4/8 mixed "
+                       f"per layer, V INT4, fused step, {K} steps",
+           "bytes_per_launch": nbytes}
+    for name, t in res.items():
+        us = t / (K * L) * 1e6
+        out[name] = {"tokens_s": K * w.batch / t, "avg_launch_us": us,
+                     "achieved_gbs": nbytes / us / 1e3, "frac": nbytes / us / 1e3 / peak}
+    return out
+
+
 def main():
     a = parse()
     import torch
@@ -254,9 +324,18 @@ def main():
     if world > 1:
         dist.init_process_group("nccl" if a.impl == "ekv" else "gloo")
 
-    w = replicas.shard(workloads.by_name(a.workload), rank)
+    heads = a.split == "heads" and world > 1
+    w = (replicas.head_shard(workloads.by_name(a.workload), rank, world) if heads
+         else replicas.shard(workloads.by_name(a.workload), rank))
+    # tokens/s over the job: every rank's own sequences (batch split), or the
+    # same sequences' tokens once (head split: the ranks share each token)
+    rate = (lambda units, t: units / t) if heads else (
+        lambda units, t: replicas.whole_job_rate(R, units, t))
     if a.layers:
         w = w.scaled(num_layers=a.layers)
+    if a.force_kbits:
+        w = w.scaled(k_bits_init=[a.force_kbits] * w.num_layers, canary_period=0,
+                     name=f"{w.name}_k{a.force_kbits}")
     if a.asym:
         if a.static:
             raise SystemExit("the static artifact's thresholds cap the symmetric quantizer")
@@ -290,6 +369,12 @@ def main():
     n_steps_total = W + (3 if not a.no_e2e else 2) * K + (K if not a.no_overlap_check else 0)
     if n_steps_total > w.steps:
         raise SystemExit(f"workload holds {w.steps} decode steps; asked for {n_steps_total}")
+    # Region F: `period` steps that hold exactly one canary firing (the first
+    # firing step after the other regions), timed like region A.
+    P = w.canary_period
+    sF = -(-n_steps_total // P) * P if P else None
+    if sF is not None and sF + P > w.steps:
+        sF = None
 
     static = None
     if a.static:
@@ -622,33 +707,90 @@ def main():
         for c in caches:
             c.sync()
         tE = replicas.max_over_ranks(R, tE, dev)
-        e2e = {"value": replicas.whole_job_rate(R, B * K, tE), "unit": "tokens/s",
+        e2e = {"value": rate(B * K, tE), "unit": "tokens/s",
                "h2d_bytes_per_step": int(host_in.shape[1] * 2),
                "d2h_bytes_per_step": int(out.numel() * 2)}
 
+    # ---- F: one period of steps holding one canary firing ------------------------
+    canary_in_loop = None
+    if sF is not None:
+        inpF = runner.Inputs(w, sF, P, device=dev, order=order)
+        gF = capture(lambda: [runner.decode_step(C(i), w, slots, inpF, i - sF, outs, w.fires(i),
+                                                 delta_out=delta_buf, fused=fused,
+                                                 combine=combine)
+                              for i in range(sF, sF + P)])
+        torch.cuda.synchronize()
+        replicas.barrier(R)
+        with torch.cuda.stream(stream):
+            g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            hold_gpu()  # the GPU is busy while the host submits what follows
+            g0.record(stream)
+            gF.replay()
+            g1.record(stream)
+        torch.cuda.synchronize()
+        replicas.barrier(R)
+        tF = replicas.max_over_ranks(R, g0.elapsed_time(g1) / 1e3, dev)
+        for c in caches:
+            c.sync()
+        del gF, inpF
+        fired_F = sum(1 for i in range(sF, sF + P) if w.fires(i))
+        t_step_nofire = (tA - fired_A * canary_us * 1e-6) / K   # region A's steps, firings out
+        canary_in_loop = {
+            "steps": P, "first_step": sF, "firings": fired_F, "ms": 1e3 * tF,
+            "ms_per_step": 1e3 * tF / P,
+            "overhead_frac_measured": (tF - P * t_step_nofire) / (P * t_step_nofire),
+            "overhead_frac_derived": canary_us * 1e-6 / P / t_step_nofire,
+            "note": "region F (one period of steps with its one firing) against region A's "
+                    "steps without firings; derived = standalone firing time / period / step"}
+
+    precision = None
+    try:
+        st_ = cache.stats()
+        precision = {"k_bits_per_element": st_["k_bits"], "v_bits_per_element": st_["v_bits"],
+                     "avg_bits_per_element": (st_["k_bits"] + st_["v_bits"]) / 2,
+                     "memory_saved_vs_fp16": st_["saved_vs_fp16"],
+                     "code_bits_vs_c0": st_["cost_vs_c0"],
+                     "page_bytes": st_["page_bytes"], "fp16_bytes": st_["fp16_bytes"],
+                     "pages_by_k_bits": {str(2 << kc): sum(st_["sealed_pages"][kc * 4 + vc] +
+                                                           st_["open_pages"][kc * 4 + vc]
+                                                           for vc in range(4))
+                                         for kc in range(4)
+                                         if any(st_["sealed_pages"][kc * 4 + vc] +
+                                                st_["open_pages"][kc * 4 + vc]
+                                                for vc in range(4))},
+                     "source": "ekv_stats over every layer of the first cache after the timed "
+                               "regions"}
+    except Exception as ex:  # noqa: BLE001
+        precision = {"error": repr(ex)}
+
     clk.__exit__(None, None, None)
-    tA = replicas.max_over_ranks(R, tA, dev)
+    tA_raw = replicas.max_over_ranks(R, tA, dev)
+    # `value` carries the canary at its 1-in-period share whatever firings the
+    # timed window happened to hold.
+    tA = amortized_region(tA_raw, fired_A, canary_us * 1e-6, K, P)
 
     peak, peak_kind = peaks()
     achieved = bytes_per_launch / attn_avg_s / 1e9 if attn_avg_s else None
     step_bytes = sum(layer_bytes)
     line = {
         "metric": METRIC,
-        "value": replicas.whole_job_rate(R, B * K, tA),
+        "value": rate(B * K, tA),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": K,
         "warmup": W,
         "ms_per_step": 1e3 * tA / K,
         "higher_is_better": True,
-        "scaling": "weak",
+        "scaling": "strong" if heads else "weak",
         "vs_baseline": None,
         "dtype": "f16",
         "data": "synthetic",
         "config": {"workload": f"{w.name}: {w.num_layers} layers, batch {B}, "
                                f"{w.num_q_heads} q / {w.num_kv_heads} kv heads, d {w.head_dim}, "
                                f"{w.prefill[0] if len(set(w.prefill)) == 1 else 'ragged'} cached "
-                               + (f"tokens, K tier by canary every {w.canary_period} steps "
+                               + (f"tokens, K fixed at INT{a.force_kbits} (canary off), "
+                                  if a.force_kbits else
+                                  f"tokens, K tier by canary every {w.canary_period} steps "
                                   f"(tau {w.tau}), " if static is None else
                                   "tokens, K bits per layer from the static artifact, ")
                                + f"V INT{w.v_bits[0]}"
@@ -658,7 +800,9 @@ def main():
                           f"steps rotate over {NR} caches of {step_bytes / 1e9:.3f} GB of pages "
                           f"each ({NR * step_bytes / 1e6:.0f} MB, over 1.5 times the "
                           f"{L2_BYTES / 1e6:.0f} MB L2)"),
-                   "parallelism": f"replicas x{world} (one sequence set per GPU)",
+                   "parallelism": (f"KV heads split over {world} GPUs ({w.num_kv_heads} each)"
+                                   if heads else
+                                   f"replicas x{world} (one sequence set per GPU)"),
                    "graph": ("CUDA graph of the timed steps, uploaded before timing"
                              if uploaded and all(uploaded) else
                              "CUDA graph of the timed steps (first replay includes its upload)"),
@@ -696,12 +840,35 @@ def main():
                      "attn_only_avg_us": attn_only_us},
         "e2e": e2e,
         "no_overlap": (None if tA2 is None else
-                       {"value": replicas.whole_job_rate(R, B * K, tA2), "unit": "tokens/s",
+                       {"value": rate(B * K, amortized_region(tA2, fired_A, canary_us * 1e-6,
+                                                              K, P)),
+                        "unit": "tokens/s",
+                        "avg_launch_us": (tA2 - fired_A * canary_us * 1e-6) / (K * L) * 1e6,
+                        "roofline_frac": (bytes_per_launch /
+                                          ((tA2 - fired_A * canary_us * 1e-6) / (K * L)) / 1e9
+                                          / peak),
                         "note": "same steps, each layer's launch waiting for the previous "
-                                "one (inputs that depend on the previous layer's output)"}),
+                                "one (inputs that depend on the previous layer's output); "
+                                "canary at its 1-in-period share"}),
+        "canary_amortized": {"firings_in_region_A": fired_A,
+                             "firings_counted": K / P if P else 0,
+                             "value_before_amortizing": rate(B * K, tA_raw),
+                             "note": "value and ms_per_step carry K/period canary firings "
+                                     "(timed standalone) in place of those region A held"},
+        "canary_in_loop": canary_in_loop,
+        "precision": precision,
         "gpu_launches": launches,
         "clocks": clk.summary(),
     }
+    if (rank == 0 and world == 1 and not a.no_short and not a.layers and not a.static
+            and not a.asym and not a.force_kbits and w.name == "llama70b_128k"):
+        for c in caches:
+            c.close()
+        caches = []
+        try:
+            line["ctx32k"] = short_context_figure(dev)
+        except Exception as ex:  # noqa: BLE001
+            line["ctx32k"] = {"error": repr(ex)}
     if rank == 0 and world == 1 and not a.no_cpu:
         try:
             line["cpu_baseline"] = cpu_baseline(w, a.cpu_sample_layers, dev)

@@ -223,7 +223,10 @@ EKV_API int ekv_append_decode_attn(ekv_cache* cache, int32_t layer, int32_t n_se
  *   - Every GPU that loads the library holds the array until the process
  *     exits.  The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is kept for the life of the
+ *     process: after cudaDeviceReset (or any other teardown of the device's
+ *     primary context) it is stale, so do not call this entry point again in
+ *     that process.
  *   - All calls share the array and it keeps the last call's contents; each
  *     call clears the tickets it uses (cudaMemsetAsync on `stream`) before
  *     launching.  Calls that overlap on the GPU race on the array: serialize
@@ -385,6 +388,19 @@ EKV_API int ekv_stats(ekv_cache* cache, int32_t first_layer, int32_t n_layers, e
 
 /* Free pages left in the pool of one format (syncs stream). */
 EKV_API int ekv_pool_free(ekv_cache* cache, int32_t format, int64_t* out, void* stream);
+
+/* Test hooks (off in a new handle).
+ *   EKV_DEBUG_WAIT_EXPIRY  value != 0: every bounded device-side wait of decode
+ *                          attention reports that it gave up once the copy it
+ *                          waits for has landed.  The kernel then takes the path
+ *                          of a real expiry (the warp stops taking pages, waits
+ *                          for its copies still in flight, the launch returns and
+ *                          ekv_sync reports EKV_ETIMEOUT; that launch's o is not
+ *                          valid), with nothing left in flight and no stall.
+ *                          0 restores normal waits.
+ * Unknown knob: EKV_EINVAL. */
+#define EKV_DEBUG_WAIT_EXPIRY 1
+EKV_API int ekv_debug_set(ekv_cache* cache, int32_t knob, int64_t value);
 
 /* Wait for the stream, then return and clear the device error word. */
 EKV_API int ekv_sync(ekv_cache* cache, void* stream);

@@ -1001,8 +1001,12 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   uint32_t phases = 0;
   bool ok = true;
   // Wait for stage si (warp-uniform outcome: the MMAs that follow need every lane).
+  // (With the test hook dbg_wait_expiry set, a wait that saw its copy land still
+  // reports expiry, so the timeout path runs with no copy left in flight.)
+  const bool expire = st.dbg_wait_expiry != 0;
   auto wait_stage = [&](int si) {
-    if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * si, (phases >> si) & 1)) && ok) {
+    const bool landed = mbar_wait(bar0 + 8 * si, (phases >> si) & 1);
+    if (!__all_sync(0xffffffffu, landed && !expire) && ok) {
       ok = false;
       if (lane == 0) set_error(st, EKV_ETIMEOUT);
     }

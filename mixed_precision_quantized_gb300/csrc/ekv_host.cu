@@ -166,6 +166,16 @@ int ekv_create(const ekv_config* cfg, const uint8_t* k_bits_init, const uint8_t*
     return EKV_ECUDA;
   }
 
+  // The kernels' launch attributes and the two-CTA occupancy check come first:
+  // the split plan below (hence the split scratch) depends on them.
+  cudaError_t e = canary_init();
+  if (e == cudaSuccess) e = attn_init();
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    delete c;
+    return EKV_ECUDA;
+  }
+
   const size_t L = st.L, S = st.S, H = st.Hkv, D = st.D, MB = st.maxblk;
   bool ok = true;
   auto A = [&](size_t bytes) -> void* {
@@ -199,11 +209,14 @@ int ekv_create(const ekv_config* cfg, const uint8_t* k_bits_init, const uint8_t*
   st.vclip = (float*)A(L * H * 4);
   st.err = (int32_t*)A(4);
   st.append_ticket = (int32_t*)A(L * S * 4);
+  // Split scratch for the largest plan any launch can ask for: every batch size
+  // and every V width (the plan follows the same rules as the launch).
   int parts = 0;
-  for (int n = 1; n <= k.max_seqs; ++n) {
-    const int p = n * k.num_kv_heads * std::max(attn_splits(c, n, 4), attn_splits(c, n, 16));
-    if (p > parts) parts = p;
-  }
+  for (int n = 1; n <= k.max_seqs; ++n)
+    for (int vb = 2; vb <= 16; vb *= 2) {
+      const int p = n * k.num_kv_heads * attn_splits(c, n, vb);
+      if (p > parts) parts = p;
+    }
   st.attn_parts_cap = parts;
   st.attn_acc = (float*)A((size_t)parts * MAX_G * D * 4);
   st.attn_ml = (float*)A((size_t)parts * MAX_G * 2 * 4);
@@ -217,8 +230,6 @@ int ekv_create(const ekv_config* cfg, const uint8_t* k_bits_init, const uint8_t*
     return EKV_ENOMEM;
   }
 
-  cudaError_t e = canary_init();
-  if (e == cudaSuccess) e = attn_init();
   auto Z = [&](void* p, size_t bytes) {
     if (e == cudaSuccess) e = cudaMemset(p, 0, bytes);
   };
@@ -516,6 +527,14 @@ int ekv_pool_free(ekv_cache* c, int32_t format, int64_t* out, void* stream) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   *out = t;
   return cuda_status(e);
+}
+
+int ekv_debug_set(ekv_cache* c, int32_t knob, int64_t value) {
+  if (!c) return EKV_EINVAL;
+  switch (knob) {
+    case EKV_DEBUG_WAIT_EXPIRY: c->st.dbg_wait_expiry = value != 0; return EKV_OK;
+    default: return EKV_EINVAL;
+  }
 }
 
 int ekv_sync(ekv_cache* c, void* stream) {

@@ -77,6 +77,7 @@ struct DevState {
   int32_t attn_parts_cap;
   float* canary_part;       // [L][S*Hkv][3]
   int32_t* canary_ticket;   // [L]
+  int dbg_wait_expiry;      // test hook: bounded waits report expiry once their copy landed
 };
 
 __device__ inline void set_error(const DevState& st, int code) { atomicCAS(st.err, 0, code); }

@@ -76,8 +76,9 @@ extern "C" EKV_API int ekv_decode_attn_noalloc(ekv_cache* cache, int32_t layer, 
   st.attn_ticket = reinterpret_cast<int32_t*>(b + tk_off);
   st.attn_parts_cap = (int32_t)parts;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // The array keeps whatever the previous call left: the merge tickets must
-  // start at zero.
+  // Each ticket returns to zero when the last CTA of its group arrives, so a
+  // completed call leaves them clear; this clear only guards against a launch
+  // that never completed (an aborted kernel would leave counts behind).
   if (cudaMemsetAsync(st.attn_ticket, 0, tk_bytes, s) != cudaSuccess) return EKV_ECUDA;
   cudaError_t e = launch_decode_attn(st, layer, n_seqs, seq_slots, static_cast<const __half*>(q),
                                      static_cast<__half*>(o), splits, vb, pack, s);

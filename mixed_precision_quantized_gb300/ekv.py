@@ -18,6 +18,7 @@ BITS = (2, 4, 8, 16)
 _CODE = {2: 0, 4: 1, 8: 2, 16: 3}
 NUM_FORMATS = 16
 AFTER_OTHER_LAYER = 1  # ekv_append_decode_attn flag
+DEBUG_WAIT_EXPIRY = 1  # ekv_debug_set knob
 
 
 def fmt_index(k_bits: int, v_bits: int) -> int:
@@ -88,6 +89,7 @@ _SIGS = {
     "ekv_read_pages": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _I32, _P, ctypes.c_size_t, _P]),
     "ekv_pool_free": (ctypes.c_int, [_P, _I32, _P, _P]),
     "ekv_stats": (ctypes.c_int, [_P, _I32, _I32, ctypes.POINTER(EkvStats), _P]),
+    "ekv_debug_set": (ctypes.c_int, [_P, _I32, ctypes.c_int64]),
     "ekv_sync": (ctypes.c_int, [_P, _P]),
     "ekv_state_size": (ctypes.c_int64, [_P]),
     "ekv_state_save": (ctypes.c_int, [_P, _P, ctypes.c_int64, _P]),
@@ -356,6 +358,10 @@ class Cache:
 
     def reset(self, slot: int, stream=None):
         _check(lib().ekv_seq_reset(self._h, slot, _stream(stream)), "ekv_seq_reset")
+
+    def debug_set(self, knob: int, value: int):
+        """Set a test hook (ekv_debug_set; DEBUG_WAIT_EXPIRY)."""
+        _check(lib().ekv_debug_set(self._h, knob, int(value)), "ekv_debug_set")
 
     def sync(self, stream=None):
         """Wait for the stream and raise if a kernel recorded a device-side error."""

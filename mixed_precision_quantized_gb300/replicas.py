@@ -1,8 +1,11 @@
-"""Data-parallel decode: one process per GPU, each with its own sequences.
+"""Multi-GPU decode: one process per GPU.
 
-Attention and the append are independent per (sequence, KV head), so N GPUs
-hold N shards of the batch (weak scaling), each drawing its own sequences from
-a rank-offset seed.  The one exchange is the controller's: a layer's tier is
+Attention and the append are independent per (sequence, KV head), so the path
+shards two ways.  By batch (`shard`): N GPUs hold N shards of the batch (weak
+scaling), each drawing its own sequences from a rank-offset seed.  By KV heads
+(`head_shard`, the layout for a batch of one): every GPU holds every sequence
+but only Hkv/N of its KV heads and their query heads (strong scaling).  Either
+way the one exchange is the controller's: a layer's tier is
 shared by the whole batch ("EchoKV: watching a language model decide its own
 precision", "Show the math — what the canary actually computes": the KL is
 averaged over the step's queries), so at a canary firing the ranks add their
@@ -36,6 +39,28 @@ def from_env() -> Ranks:
 def shard(workload, rank: int):
     """This rank's replica: the same shapes, its own sequences (seed offset by rank)."""
     return workload if rank == 0 else workload.scaled(seed=workload.seed + 1000003 * rank)
+
+
+def head_shard(workload, rank: int, world: int):
+    """This rank's part of a split by KV heads (the pages' tensor-parallel layout:
+    "EchoKV: watching a language model decide its own precision", "Hardware &
+    serving configuration", TP = 4/8): the same sequences, KV heads
+    [rank * Hkv / world, (rank + 1) * Hkv / world) and the query heads of their
+    groups.  Every draw is the full workload's, sliced to those heads, so the
+    ranks together hold exactly the unsplit workload.  Attention and the append
+    stay on the rank that owns the heads; the one exchange is again the
+    canary's (combine_readings with this rank's B * Hq / world queries)."""
+    H, Hq = workload.num_kv_heads, workload.num_q_heads
+    if world < 1 or H % world:
+        raise ValueError(f"{H} KV heads do not split over {world} ranks")
+    if world == 1:
+        return workload
+    n = H // world
+    return HeadShard(**{f.name: getattr(workload, f.name)
+                        for f in dataclasses.fields(workload)
+                        if f.name not in ("num_kv_heads", "num_q_heads")},
+                     num_kv_heads=n, num_q_heads=Hq // world, kv_head0=rank * n,
+                     full_kv_heads=H, full_q_heads=Hq)
 
 
 def barrier(r: Ranks) -> None:
@@ -123,3 +148,47 @@ def share_artifact(r: Ranks, artifact=None):
     for a in (art.k_clip, art.v_clip):
         a.setflags(write=False)
     return art
+
+
+def _head_shard_class():
+    from . import workloads
+
+    @dataclasses.dataclass
+    class HeadShard(workloads.Workload):
+        """A workload restricted to a contiguous range of KV heads (and their
+        query heads): draws of the full workload, sliced."""
+        kv_head0: int = 0
+        full_kv_heads: int = 0
+        full_q_heads: int = 0
+
+        def full(self):
+            base = {f.name: getattr(self, f.name) for f in dataclasses.fields(workloads.Workload)}
+            base.update(num_kv_heads=self.full_kv_heads, num_q_heads=self.full_q_heads)
+            return workloads.Workload(**base)
+
+        def _kv(self):
+            return slice(self.kv_head0, self.kv_head0 + self.num_kv_heads)
+
+        def _q(self):
+            G = self.full_q_heads // self.full_kv_heads
+            return slice(self.kv_head0 * G, (self.kv_head0 + self.num_kv_heads) * G)
+
+        def k_gain(self, layer: int):
+            return self.full().k_gain(layer)[self._kv()]
+
+        def prefill_kv(self, layer, seqs, device="cpu", tok0=None, n_tok=None):
+            k, v = self.full().prefill_kv(layer, seqs, device=device, tok0=tok0, n_tok=n_tok)
+            return k[:, :, self._kv()].contiguous(), v[:, :, self._kv()].contiguous()
+
+        def step_kv(self, layer, step0, n_steps, seqs=None, device="cpu"):
+            k, v = self.full().step_kv(layer, step0, n_steps, seqs=seqs, device=device)
+            return k[:, :, self._kv()].contiguous(), v[:, :, self._kv()].contiguous()
+
+        def step_q(self, layer, step0, n_steps, seqs=None, device="cpu"):
+            q = self.full().step_q(layer, step0, n_steps, seqs=seqs, device=device)
+            return q[:, :, self._q()].contiguous()
+
+    return HeadShard
+
+
+HeadShard = _head_shard_class()

@@ -72,18 +72,32 @@ def check(cache, ref, layers, asym=False):
 
 
 def test_stats_after_canary_driven_tier_changes():
-    """70B-shaped 2 layers, canary every 64 steps over 130 steps: pages admitted at
-    several widths in one layer; the census follows the oracle's admit-time bits."""
-    w = workloads.llama70b_128k().scaled(num_layers=2, prefill=[700], steps=130)
-    r = Run(w, 130, fused=True)
+    """The tiny workload (canary at every step) over 40 steps: layer 1 starts at
+    K8 and the controller moves it to K4 at step 1, so its pages hold both
+    widths from the block that opens at step 16 on; the census follows the
+    oracle's admit-time bits throughout."""
+    w = workloads.tiny().scaled(steps=40)
+    r = Run(w, 40, fused=True)
     try:
-        for t in range(130):
-            r.step(check_attn_now=t in (0, 129))
-            if t in (0, 63, 64, 129):
+        for t in range(40):
+            r.step(check_attn_now=t in (0, 39))
+            if t in (0, 1, 15, 16, 17, 39):
                 check(r.cache, r.ref, [0, 1])
                 check(r.cache, r.ref, [1])
-        kinds = {tuple(r.ref.state[(l, 0)].kbits) for l in range(2)}
-        assert any(len(set(k)) > 1 for k in kinds), "the run should hold mixed widths"
+        assert len(set(r.ref.state[(1, 0)].kbits)) > 1, "layer 1 should hold two widths"
+    finally:
+        r.close()
+
+
+def test_stats_70b_shape():
+    """G = 8, d = 128, 8 KV heads: sealed and open blocks of a 700-token prefill."""
+    w = workloads.llama70b_128k().scaled(num_layers=2, prefill=[700], steps=20)
+    r = Run(w, 20, fused=True)
+    try:
+        for t in range(20):
+            r.step(check_attn_now=t in (0, 19))
+            if t in (0, 3, 4, 19):
+                check(r.cache, r.ref, [0, 1])
     finally:
         r.close()
 

@@ -230,3 +230,106 @@ def test_static_artifact_shared_by_all_ranks():
     assert (r0, r1) == (0, 1)
     assert b0 == b1 == [4, 8, 4] and k0 == k1 and v0 == v1 and s0 == s1
     assert not w0 and not w1
+
+
+# ---- split by KV heads (batch-1 multi-GPU layout) ---------------------------------
+
+
+def _head_split_workload():
+    # 70B-shaped, two layers, a short context, the canary at every step
+    return workloads.llama70b_128k().scaled(num_layers=2, prefill=[150], steps=3,
+                                            canary_period=1)
+
+
+def _head_split_main(rank: int, world: int, port: int, out) -> None:
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), WORLD_SIZE=str(world),
+                      RANK=str(rank), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        from oracle import controller, decoder
+        R = replicas.from_env()
+        w = _head_split_workload()
+        mine = replicas.head_shard(w, rank, world)
+        nq = mine.batch * mine.num_q_heads
+        total = replicas.total_queries(R, nq, "cpu")
+        ctl = controller.Controller(w.k_bits_init, w.alpha, w.tau)
+        tr = decoder.Trace()
+        res = {"rank": rank, "heads": (mine.kv_head0, mine.num_kv_heads), "total": total,
+               "delta": {}, "tiers": {}, "out": {}, "pages": {}}
+        for t in range(w.steps):
+            tr.tiers.append(list(ctl.tiers))
+            delta = torch.zeros(w.num_layers, 3, dtype=torch.float64)
+            for l in range(w.num_layers):
+                q = mine.step_q(l, t, 1)[:, 0].numpy()
+                delta[l] = torch.from_numpy(canary.layer_delta(q, decoder.layer_windows(mine, l, t)))
+            replicas.combine_readings(R, delta, nq, total)     # the one exchange
+            res["delta"][t] = delta.numpy().copy()
+            ctl.update(delta.numpy().astype(np.float32))
+            res["tiers"][t] = list(ctl.tiers)
+        tr.tiers.append(list(ctl.tiers))
+        run = decoder.ReferenceRun(mine, tr)
+        run.prefill()
+        for t in range(w.steps):
+            o = run.step()
+            res["out"][t] = {k: v.copy() for k, v in o.items()}
+        st = run.state[(0, 0)]
+        res["pages"] = {(j, h): st.page_expect(j, h) for j in range((st.T + 15) // 16)
+                        for h in range(mine.num_kv_heads)}
+        out.put(res)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_kv_head_split_two_ranks_on_gloo():
+    """Two ranks owning 4 of the 8 KV heads each (and their 32 query heads): each
+    rank's attention outputs and page bytes equal the unsplit oracle's for its
+    heads, the canary readings combined over the ranks equal the unsplit
+    readings, and both ranks reach the unsplit controller's tiers."""
+    from oracle import decoder
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    ps = [ctx.Process(target=_head_split_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in ps:
+        p.start()
+    res = sorted((q.get(timeout=300) for _ in ps), key=lambda x: x["rank"])
+    for p in ps:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    w = _head_split_workload()
+    G = w.group
+    full = decoder.controller_trace(w, w.steps)
+    ref = decoder.ReferenceRun(w, full)
+    ref.prefill()
+    outs = [ref.step() for _ in range(w.steps)]
+    st = ref.state[(0, 0)]
+    for r in res:
+        h0, n = r["heads"]
+        assert r["total"] == w.batch * w.num_q_heads
+        for t in range(w.steps):
+            assert np.allclose(r["delta"][t], full.delta[t], rtol=1e-12, atol=1e-15)
+            assert r["tiers"][t] == full.after[t]
+            for key, o in r["out"][t].items():
+                assert np.array_equal(o, outs[t][key][h0 * G:(h0 + n) * G]), (t, key)
+        for (j, h), exp in r["pages"].items():
+            want = st.page_expect(j, h0 + h)
+            assert exp.keys() == want.keys()
+            for name in exp:
+                assert np.array_equal(exp[name], want[name]), (j, h, name)
+    assert np.array_equal(res[0]["delta"][0], res[1]["delta"][0])
+
+
+def test_head_shard_slices_the_unsplit_draws():
+    w = workloads.tiny()
+    with pytest.raises(ValueError):
+        replicas.head_shard(w, 0, 3)                      # 2 KV heads over 3 ranks
+    assert replicas.head_shard(w, 0, 1) is w
+    parts = [replicas.head_shard(w, r, 2) for r in range(2)]
+    k, v = w.prefill_kv(1, [0], n_tok=40)
+    q = w.step_q(1, 2, 1)
+    assert torch.equal(torch.cat([p.prefill_kv(1, [0], n_tok=40)[0] for p in parts], 2), k)
+    assert torch.equal(torch.cat([p.prefill_kv(1, [0], n_tok=40)[1] for p in parts], 2), v)
+    assert torch.equal(torch.cat([p.step_q(1, 2, 1) for p in parts], 2), q)
+    assert torch.equal(torch.cat([p.k_gain(1) for p in parts], 0), w.k_gain(1))
+    assert [p.group for p in parts] == [w.group] * 2
+    assert parts[1].scaled(steps=2).kv_head0 == 1          # survives scaling

@@ -33,7 +33,7 @@ def _cache_after_one_step(w):
     cache = ekv.cache_for(w)
     slots = torch.arange(w.batch, dtype=torch.int32, device="cuda")
     runner.prefill(cache, w, slots)
-    inp = runner.Inputs(w, 0, 1)
+    inp = runner.Inputs(w, 0, 2)   # step 1's queries serve as a second, different query set
     for l in range(w.num_layers):
         _, k, v = inp.layer(l, 0)
         cache.append(l, slots, k, v)
@@ -47,18 +47,26 @@ def _cache_after_one_step(w):
     workloads.tiny(),
 ], ids=["batch2_int4", "one_seq_many_splits", "tiny_d64"])
 def test_noalloc_matches_decode_attn_on_two_calls(w):
+    """Two calls in a row with different queries, each against ekv_decode_attn on
+    the same query.  The split partials of the first call are still in the
+    shared array when the second runs, and the two calls' outputs differ by far
+    more than the tolerance, so a second call that read any stale partial
+    would fail.  (The two entry points' outputs are not compared bit for bit:
+    pages go to warps in the order the warps reach them, so the fp32 summation
+    order differs from launch to launch.)"""
     build.build()
     lib = ekv.lib()
     cache, slots, inp = _cache_after_one_step(w)
     try:
         for l in range(w.num_layers):
-            q = inp.layer(l, 0)[0]
-            ref = torch.empty_like(q)
-            assert lib.ekv_decode_attn(cache.handle, l, w.batch, _ptr(slots), _ptr(q), _ptr(ref),
-                                       _stream()) == 0
-            cache.sync()
-            r = ref.float().cpu().numpy().astype(np.float64)
+            outs = []
             for call in range(2):
+                q = inp.layer(l, call)[0]
+                ref = torch.empty_like(q)
+                assert lib.ekv_decode_attn(cache.handle, l, w.batch, _ptr(slots), _ptr(q),
+                                           _ptr(ref), _stream()) == 0
+                cache.sync()
+                r = ref.float().cpu().numpy().astype(np.float64)
                 o = torch.full_like(q, float("nan"))
                 rc = lib.ekv_decode_attn_noalloc(cache.handle, l, w.batch, _ptr(slots), _ptr(q),
                                                  _ptr(o), _stream())
@@ -68,6 +76,46 @@ def test_noalloc_matches_decode_attn_on_two_calls(w):
                 assert np.all(np.isfinite(g)), f"layer {l} call {call}: unwritten outputs"
                 assert np.all(np.abs(g - r) <= ATOL + RTOL * np.abs(r)), (
                     f"layer {l} call {call}: max diff {np.abs(g - r).max():.3e}")
+                outs.append(g)
+            # the test's sensitivity: most outputs of the two query sets lie further
+            # apart than the tolerance
+            apart = np.abs(outs[0] - outs[1]) > ATOL + RTOL * np.abs(outs[1])
+            assert apart.mean() > 0.5, f"layer {l}: the two query sets give close outputs"
+    finally:
+        cache.close()
+
+
+@pytest.mark.parametrize("w", [
+    workloads.tiny(),
+    workloads.llama70b_128k().scaled(num_layers=1, prefill=[3000], steps=1),
+], ids=["tiny_d64", "int4_g8_many_splits"])
+def test_noalloc_matches_the_oracle(w):
+    """The allocation-free attention against the CPU oracle's attention over the
+    same pages (prefill plus one appended step), at the attention tolerance."""
+    from oracle import decoder
+    build.build()
+    lib = ekv.lib()
+    cache, slots, inp = _cache_after_one_step(w)
+    try:
+        tr = decoder.Trace()
+        tr.tiers = [list(w.k_bits_init)] * 2
+        ref = decoder.ReferenceRun(w, tr)
+        ref.prefill()
+        ref.advance()
+        qh = ref.q_heads()
+        for l in range(w.num_layers):
+            q = inp.layer(l, 0)[0]
+            o = torch.full_like(q, float("nan"))
+            rc = lib.ekv_decode_attn_noalloc(cache.handle, l, w.batch, _ptr(slots), _ptr(q),
+                                             _ptr(o), _stream())
+            assert rc == 0, lib.ekv_status_string(rc)
+            cache.sync()
+            for s in range(w.batch):
+                want = ref.attend(l, s)
+                g = o[s][qh].float().cpu().numpy().astype(np.float64)
+                err = np.abs(g - want)
+                assert np.all(err <= ATOL + RTOL * np.abs(want)), (
+                    f"layer {l} seq {s}: max diff {err.max():.3e}")
     finally:
         cache.close()
 
