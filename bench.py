@@ -85,6 +85,10 @@ def parse():
     p.add_argument("--split", default="batch", choices=["batch", "heads"],
                    help="several GPUs: each holds its own sequences (batch, weak scaling) or "
                         "a share of every sequence's KV heads (heads, strong scaling)")
+    p.add_argument("--overlap", default="dependent", choices=["dependent", "independent", "none"],
+                   help="how each timed step's fused launches overlap (region A): starting while "
+                        "the previous launch ends and reading q, k, v after it (dependent, as in "
+                        "a model), reading them before it too (independent), or not at all")
     p.add_argument("--no-short", action="store_true",
                    help="skip the extra 32K-context figure (Qwen2.5-14B shape) of the default run")
     p.add_argument("--force-kbits", type=int, default=0,
@@ -280,7 +284,7 @@ def short_context_figure(dev, K: int = 16, W: int = 3) -> dict:
     stream = torch.cuda.Stream(device=dev)
     stream.wait_stream(torch.cuda.current_stream())
     res = {}
-    for name, first, overlap in (("overlap", W, True), ("no_overlap", W + K, False)):
+    for name, first, overlap in (("overlap", W, "dependent"), ("no_overlap", W + K, False)):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for i in range(first, first + K):
@@ -366,7 +370,7 @@ def main():
     fused = not a.separate
     if W < 3:
         raise SystemExit("at least 3 warm-up steps")
-    n_steps_total = W + (3 if not a.no_e2e else 2) * K + (K if not a.no_overlap_check else 0)
+    n_steps_total = W + (3 if not a.no_e2e else 2) * K + (2 * K if not a.no_overlap_check else 0)
     if n_steps_total > w.steps:
         raise SystemExit(f"workload holds {w.steps} decode steps; asked for {n_steps_total}")
     # Region F: `period` steps that hold exactly one canary firing (the first
@@ -473,10 +477,11 @@ def main():
             combine(delta_buf)
             c.tier_update(delta_buf, freeze=freeze)
 
+    ovA = {"dependent": "dependent", "independent": "independent", "none": False}[a.overlap]
     # warm-up (eager)
     for i in range(W):
         runner.decode_step(C(i), w, slots, inp, i, outs, w.fires(i), delta_out=delta_buf,
-                           fused=fused, combine=combine)
+                           fused=fused, combine=combine, overlap=ovA)
     for c in caches:
         c.sync()
 
@@ -494,7 +499,8 @@ def main():
 
     # ---- A: K steps as one graph -------------------------------------------------
     gA = capture(lambda: [runner.decode_step(C(i), w, slots, inp, i, outs, w.fires(i),
-                                             delta_out=delta_buf, fused=fused, combine=combine)
+                                             delta_out=delta_buf, fused=fused, combine=combine,
+                                             overlap=ovA)
                           for i in range(W, W + K)])
     per_layer = 1 if fused else 2
     launches = sum(per_layer * L + (2 if w.fires(i) else 0) for i in range(W, W + K))
@@ -514,30 +520,38 @@ def main():
         c.sync()
     fired_A = sum(1 for i in range(W, W + K) if w.fires(i))
 
-    # ---- A': the same steps without the overlap of consecutive layers ------------
-    # (what a model whose layer inputs come from the previous layer's output gets)
-    tA2 = None
+    # ---- A', A'': the same steps without any overlap of consecutive launches, and
+    # with each layer reading its inputs before the previous launch ends (valid
+    # only for this workload's fresh-draw inputs)
+    tA2 = tA3 = None
     if fused and not a.no_overlap_check:
-        s2 = W + 2 * K + (0 if a.no_e2e else K)
-        inpA2 = runner.Inputs(w, s2, K, device=dev, order=order)
-        gA2 = capture(lambda: [runner.decode_step(C(i), w, slots, inpA2, i - s2, outs,
-                                                  w.fires(i), delta_out=delta_buf, fused=True,
-                                                  combine=combine, overlap=False)
-                               for i in range(s2, s2 + K)])
-        torch.cuda.synchronize()
-        replicas.barrier(R)
-        with torch.cuda.stream(stream):
-            f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            hold_gpu()  # the GPU is busy while the host submits what follows
-            f0.record(stream)
-            gA2.replay()
-            f1.record(stream)
-        torch.cuda.synchronize()
-        replicas.barrier(R)
-        tA2 = replicas.max_over_ranks(R, f0.elapsed_time(f1) / 1e3, dev)
-        for c in caches:
-            c.sync()
-        del gA2, inpA2
+        for which in ("none", "independent"):
+            s2 = W + 2 * K + (0 if a.no_e2e else K) + (K if which == "independent" else 0)
+            inpA2 = runner.Inputs(w, s2, K, device=dev, order=order)
+            ov = False if which == "none" else "independent"
+            gA2 = capture(lambda: [runner.decode_step(C(i), w, slots, inpA2, i - s2, outs,
+                                                      w.fires(i), delta_out=delta_buf,
+                                                      fused=True, combine=combine, overlap=ov)
+                                   for i in range(s2, s2 + K)])
+            torch.cuda.synchronize()
+            replicas.barrier(R)
+            with torch.cuda.stream(stream):
+                f0, f1 = (torch.cuda.Event(enable_timing=True),
+                          torch.cuda.Event(enable_timing=True))
+                hold_gpu()  # the GPU is busy while the host submits what follows
+                f0.record(stream)
+                gA2.replay()
+                f1.record(stream)
+            torch.cuda.synchronize()
+            replicas.barrier(R)
+            t = replicas.max_over_ranks(R, f0.elapsed_time(f1) / 1e3, dev)
+            if which == "none":
+                tA2 = t
+            else:
+                tA3 = t
+            for c in caches:
+                c.sync()
+            del gA2, inpA2
 
     # ---- B: next K steps, attention launches bracketed by timing events --------
     try:
@@ -672,8 +686,10 @@ def main():
                     stream.wait_event(ev_out[n - 2])      # obufs[b] read back
                 for l in range(L):
                     if fused:
+                        # (a one-layer step's previous launch appends to this layer)
                         c.append_decode_attn(l, slots, ks[l], vs[l], qa[l], obufs[b][l],
-                                             after_other_layer=l > 0)
+                                             after_producer=ovA == "dependent" and L > 1,
+                                             after_other_layer=ovA == "independent" and l > 0)
                     else:
                         c.append(l, slots, ks[l], vs[l])
                         c.decode_attn(l, slots, qa[l], obufs[b][l])
@@ -717,7 +733,7 @@ def main():
         inpF = runner.Inputs(w, sF, P, device=dev, order=order)
         gF = capture(lambda: [runner.decode_step(C(i), w, slots, inpF, i - sF, outs, w.fires(i),
                                                  delta_out=delta_buf, fused=fused,
-                                                 combine=combine)
+                                                 combine=combine, overlap=ovA)
                               for i in range(sF, sF + P)])
         torch.cuda.synchronize()
         replicas.barrier(R)
@@ -809,7 +825,15 @@ def main():
                    "canary_fires_in_timed": fired_A,
                    "controller": {"tau_ctx0": a.tau_ctx0, "hysteresis": a.hysteresis,
                                   "vote": a.vote},
-                   "step": ("one fused append + attention launch per layer" if fused
+                   "step": ("one fused append + attention launch per layer" +
+                            {"dependent": ", each starting while the previous launch ends and "
+                                          "reading its q, k, v only after it (valid when they "
+                                          "come from the previous layer's output, as in a "
+                                          "model)",
+                             "independent": ", each starting while the previous launch ends "
+                                            "and reading its q, k, v before it (valid only for "
+                                            "inputs independent of the previous layer)",
+                             "none": ", each after the previous one"}[a.overlap] if fused
                             else "append and attention launches per layer")
                            + ("; static artifact: calibrated per-layer K bits and clipping "
                               "thresholds loaded, canary off" if static else "")},
@@ -850,6 +874,18 @@ def main():
                         "note": "same steps, each layer's launch waiting for the previous "
                                 "one (inputs that depend on the previous layer's output); "
                                 "canary at its 1-in-period share"}),
+        "independent_inputs": (None if tA3 is None else
+                               {"value": rate(B * K, amortized_region(tA3, fired_A,
+                                                                       canary_us * 1e-6, K, P)),
+                                "unit": "tokens/s",
+                                "avg_launch_us": (tA3 - fired_A * canary_us * 1e-6) / (K * L)
+                                * 1e6,
+                                "roofline_frac": (bytes_per_launch /
+                                                  ((tA3 - fired_A * canary_us * 1e-6) / (K * L))
+                                                  / 1e9 / peak),
+                                "note": "each layer's launch also reads its q, k, v before the "
+                                        "previous layer's launch ends: valid for this "
+                                        "workload's fresh-draw inputs only, not for a model"}),
         "canary_amortized": {"firings_in_region_A": fired_A,
                              "firings_counted": K / P if P else 0,
                              "value_before_amortizing": rate(B * K, tA_raw),

@@ -190,17 +190,27 @@ EKV_API int ekv_decode_attn(ekv_cache* cache, int32_t layer, int32_t n_seqs, con
  * before attention reads it); fusing them is this library's choice.
  *   k, v [n_seqs][Hkv][d] fp16 dev — the new token of each sequence
  *   q, o as ekv_decode_attn.  All four 16-byte aligned.
- *   flags   0 or EKV_AFTER_OTHER_LAYER: the caller states that the work queued
- *           on `stream` just before this call is an ekv_append_decode_attn of
- *           another layer of the same handle, and that it writes none of this
- *           call's seq_slots, k, v and q.  The launch then starts on the SMs the
- *           previous launch frees and streams this layer's pages while that
- *           launch finishes; it waits for it before writing o or the handle's
- *           shared split scratch.  Any other flag bit: EKV_EINVAL.
+ *   flags   0, EKV_AFTER_OTHER_LAYER or EKV_AFTER_PRODUCER; either lets the
+ *           launch start before the work queued just before it on `stream`
+ *           has finished (programmatic dependent launch): it takes the SMs
+ *           that work frees and streams this layer's pages meanwhile.
+ *           EKV_AFTER_OTHER_LAYER: the caller states that the previous work is
+ *           an ekv_append_decode_attn of another layer of the same handle and
+ *           writes none of this call's seq_slots, k, v and q.  The launch reads
+ *           them early and waits for that work only before writing o or the
+ *           handle's shared split scratch.
+ *           EKV_AFTER_PRODUCER: the previous work may write k, v and q (as the
+ *           projections feeding this layer do in a model), but writes none of
+ *           seq_slots and no state of this handle's layer `layer` (it is not an
+ *           append to this layer).  Before that work finishes the launch reads
+ *           only seq_slots and this layer's lengths, page table and pages; it
+ *           waits before its first read of q, k or v and before any write.
+ *           Both bits: as EKV_AFTER_PRODUCER.  Any other bit: EKV_EINVAL.
  * Errors as the two calls: EKV_ENOMEM on the device when a pool runs empty;
  * a sequence whose table is full gets EKV_ESTATE, no append, and attention
  * over its old tokens. */
 #define EKV_AFTER_OTHER_LAYER 1
+#define EKV_AFTER_PRODUCER 2
 EKV_API int ekv_append_decode_attn(ekv_cache* cache, int32_t layer, int32_t n_seqs,
                                    const int32_t* seq_slots, const void* k, const void* v,
                                    const void* q, void* o, int32_t flags, void* stream);

@@ -25,7 +25,7 @@ cudaError_t attn_init() {
 cudaError_t launch_decode_attn(const DevState& st, int layer, int n_seqs, const int32_t* slots,
                                const __half* q, __half* o, int splits, int vb, int pack,
                                cudaStream_t s, const __half* knew, const __half* vnew,
-                               bool overlap) {
+                               int overlap) {
   return (st.asym ? launch_decode_attn_asym : launch_decode_attn_sym)(
       st, layer, n_seqs, slots, q, o, splits, vb, pack, s, knew, vnew, overlap);
 }

@@ -61,7 +61,7 @@ namespace {
 
 constexpr bool ASYM = EKV_ATTN_ASYM != 0;
 
-constexpr int NSMAX = 8;  // stages per warp at most
+constexpr int RING_MAX = 96;             // stages of a CTA's page ring at most (even)
 // Blocks the last split of an overlapped launch takes less (~6 us of a CTA's
 // page work: how much later its CTAs get an SM).
 constexpr int ATTN_LATE_BLOCKS = 80;
@@ -154,6 +154,9 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
                                          uint32_t bar) {
@@ -813,12 +816,13 @@ __global__ void __launch_bounds__(AttnCfg<VB, PACK>::NT, PACK)
 decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
                    const __half* __restrict__ q, __half* __restrict__ o, int splits,
                    const __half* __restrict__ knew, const __half* __restrict__ vnew,
-                   int late_blocks) {
+                   int late_blocks, int dep_inputs) {
   using Cfg = AttnCfg<VB, PACK>;
   constexpr int NW = Cfg::NW, NT = Cfg::NT;
-  constexpr int KCH = D / 4, KW = KCH / 2, VCH = D / 8, NMT = D / 16;
+  constexpr int KCH = D / 4, KW = KCH / 2, NMT = D / 16;
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bars[NW][NSMAX];
+  __shared__ __align__(8) uint64_t bars[RING_MAX];
+  __shared__ int s_issued[RING_MAX];  // last page copied into each stage (-1: none)
   __shared__ float sm_m[NW][MAX_G], sm_l[NW][MAX_G], sm_f[NW][MAX_G], sm_ml[MAX_G][2];
   __shared__ int s_next, s_last;
   int32_t* s_bt = reinterpret_cast<int32_t*>(smem + Cfg::STAGE_SMEM);
@@ -887,11 +891,11 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   if (tid == 0) s_next = 0;
 
   // Q fragment words for head g of the group, paired like the K codes of the
-  // page format in use (re-paired when a page of another pairing class comes).
+  // page format in use (re-paired when a page of another pairing class comes);
+  // loaded once the first page copies are in flight.
   const __half* qrow = q + ((size_t)z * st.Hq + h * G + (g < G ? g : 0)) * D + c * KCH;
   uint32_t qw[KW];
   int qpc = 0;
-  load_q<D>(qrow, g < G, 0, qw);
   auto pair_q = [&](auto kbc) {
     constexpr int PC = pair_class<decltype(kbc)::value>();
     if (qpc != PC) {
@@ -909,63 +913,67 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   A.z0 = A.z1 = 0.f;
   const float sl = st.scale_log2;
 
-  // Stage geometry: sized for the widest page this layer has admitted so far
-  // (at least two stages for every format).
+  // Stage ring of the CTA: ns stages (even, at most RING_MAX) sized for the
+  // widest page this layer has admitted so far.  Page j of the split always goes
+  // to stage j % ns; its copy is the (j / ns)-th completion of that stage's
+  // barrier.  Pages 0 .. ns-1 are copied at the start; the warp that finishes
+  // page j copies page j + ns into the stage it just emptied, and records it in
+  // s_issued, which the warp that takes page j + ns reads before it waits (so
+  // it never waits on a barrier phase other than its page's).
   const int kmax = max(2, st.kmax[layer]);
   const int stage_bytes = (page_bytes(kmax, VB, D, ASYM) + 127) & ~127;
-  constexpr int WARP_BYTES = Cfg::WARP_BYTES;
-  const int ns = min(NSMAX, WARP_BYTES / stage_bytes);
-  const uint8_t* wptr = smem + warp * WARP_BYTES;
-  const uint32_t wbase = (uint32_t)__cvta_generic_to_shared(wptr);
-  const uint32_t bar0 = (uint32_t)__cvta_generic_to_shared(&bars[warp][0]);
-  if (lane == 0) {
-    for (int i = 0; i < ns; ++i) mbar_init(bar0 + 8 * i, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  const int ns = min(RING_MAX, Cfg::STAGE_SMEM / stage_bytes) & ~1;
+  // j / ns as a multiply-high (exact for j < 2^32 / ns^2, far above the pages of a split)
+  const uint32_t ns_magic = (uint32_t)((0x100000000ull + ns - 1) / ns);
+  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
+  const uint32_t bar0 = (uint32_t)__cvta_generic_to_shared(&bars[0]);
+  if (tid < ns) {
+    mbar_init(bar0 + 8 * tid, 1);
+    s_issued[tid] = -1;
   }
+  if (tid == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   // page-table copy, counter and barriers ready
   const bool uniform = !__syncthreads_or(mixed) && np > 0 && e_first != -1;
 
-  // Lane i < ns holds `pg`, the split page index in stage i (-1: none).  Stages
-  // are filled in the order the counter hands pages out and consumed in the same
-  // ring order, so the pages still to come are a prefix of the ring.  A page
-  // whose table entry is missing (-1) is flagged and neither copied nor read.
   // The pool of a uniform split's pages (its only format).
   const int fmt_u = uniform ? entry_fmt(e_first) : 0;
   const uint32_t bytes_u = (uint32_t)st.pool_page_bytes[fmt_u];
   const uint8_t* base_u = st.pool_base[fmt_u];
-  auto issue = [&](int si, int k) {  // one lane: page k -> stage si
+  // One thread: page k into stage si (= k % ns).  A page whose table entry is
+  // missing (-1) is flagged and not copied, but still completes its barrier
+  // phase (an arrival with no bytes), so the stage's phase count stays k / ns.
+  auto issue = [&](int k, int si) {
     const int32_t e = s_bt[k];
-    uint32_t bytes;
-    const uint8_t* src;
+    uint32_t bytes = 0;
+    const uint8_t* src = nullptr;
     if (uniform) {
       bytes = bytes_u;
       src = base_u + (size_t)entry_idx(e) * bytes_u;
-    } else {
-      if (e == -1) {
-        set_error(st, EKV_ESTATE);
-        return;
-      }
+    } else if (e != -1) {
       const int fmt = entry_fmt(e);
       bytes = (uint32_t)st.pool_page_bytes[fmt];
       src = st.pool_base[fmt] + (size_t)entry_idx(e) * bytes;
     }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    mbar_expect_tx(bar0 + 8 * si, bytes);
-    bulk_g2s(wbase + si * stage_bytes, src, bytes, bar0 + 8 * si);
-  };
-  int pg = -1;
-  {
-    int k0 = 0;
-    if (lane == 0) k0 = atomicAdd(&s_next, ns);
-    k0 = __shfl_sync(0xffffffffu, k0, 0);
-    if (lane < ns && k0 + lane < np) {
-      pg = k0 + lane;
-      issue(lane, pg);
+    if (src) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_expect_tx(bar0 + 8 * si, bytes);
+      bulk_g2s(sbase + si * stage_bytes, src, bytes, bar0 + 8 * si);
+    } else {
+      set_error(st, EKV_ESTATE);
+      mbar_arrive(bar0 + 8 * si);
     }
-  }
+    *reinterpret_cast<volatile int*>(&s_issued[si]) = k;
+  };
+  if (tid < ns && tid < np) issue(tid, tid);
+
+  // Dependent-inputs overlap: everything above read only this layer's cache
+  // state (length, page table, pages) and the slot list; the launch before may
+  // still be writing Q, K and V, so wait for it before the first read of them.
+  if (dep_inputs) asm volatile("griddepcontrol.wait;" ::: "memory");
+  load_q<D>(qrow, g < G, 0, qw);
 
   // The last block first (with the fused append, after appending to it), while
-  // this warp's copies are in flight.
+  // the first copies are in flight.
   if (last_apart && warp == NW - 1) {
     int32_t e;
     if (app) {
@@ -995,34 +1003,40 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
     }
   }
 
-  // Two stages per iteration.  After a wait times out the warp computes and
-  // takes nothing more but still waits, each wait bounded, for the copies
-  // already in flight, so none lands after it exits.
-  uint32_t phases = 0;
+  // Warps take the split's pages two at a time from the shared counter.  After
+  // a wait gives up the warp takes nothing more; the copies still in flight are
+  // waited for (bounded) before the CTA reuses the stage memory.
   bool ok = true;
-  // Wait for stage si (warp-uniform outcome: the MMAs that follow need every lane).
   // (With the test hook dbg_wait_expiry set, a wait that saw its copy land still
   // reports expiry, so the timeout path runs with no copy left in flight.)
   const bool expire = st.dbg_wait_expiry != 0;
-  auto wait_stage = [&](int si) {
-    const bool landed = mbar_wait(bar0 + 8 * si, (phases >> si) & 1);
+  // Wait for page j in stage si, the (q)-th copy into that stage: first until the
+  // copy was issued (the stage's previous page done), then for its barrier phase.
+  // Warp-uniform outcome: the MMAs that follow need every lane.
+  auto wait_page = [&](int j, int si, uint32_t q) {
+    bool landed = true;
+    for (int i = 0; *reinterpret_cast<volatile int*>(&s_issued[si]) != j; ++i)
+      if (i == WAIT_LIMIT) {
+        landed = false;
+        break;
+      }
+    landed = landed && mbar_wait(bar0 + 8 * si, q & 1u);
     if (!__all_sync(0xffffffffu, landed && !expire) && ok) {
       ok = false;
       if (lane == 0) set_error(st, EKV_ETIMEOUT);
     }
-    phases ^= 1u << si;
   };
-  // Refill stages s0 and s1 with the split's next two pages (none once the pages
-  // ran out or a wait failed); lanes 0 and 1 issue the two copies.
-  auto refill = [&](int s0, int s1, bool more) {
-    int kn = np;
-    if (lane == 0 && ok && more) kn = atomicAdd(&s_next, 2);
-    kn = __shfl_sync(0xffffffffu, kn, 0);
-    if (lane == s0) pg = kn < np ? kn : -1;
-    if (lane == s1) pg = kn + 1 < np ? kn + 1 : -1;
-    if (lane < 2 && kn + lane < np) issue(lane ? s1 : s0, kn + lane);
+  // Lanes 0 and 1 copy pages k + ns and k + 1 + ns into the stages si, si + 1 of
+  // pages k and k + 1.
+  auto refill = [&](int k, int si, bool two) {
+    const int j = k + ns + lane;
+    if (lane < (two ? 2 : 1) && j < np && ok) issue(j, si + lane);
   };
-  int sidx = 0;
+  auto take = [&]() {
+    int k = np;
+    if (lane == 0 && ok) k = atomicAdd(&s_next, 2);
+    return __shfl_sync(0xffffffffu, k, 0);
+  };
   if (uniform) {
     // Every pipelined page of this split has format fmt_u: one K width, one
     // stage layout, no per-page format decode.
@@ -1031,16 +1045,17 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
       constexpr int KP = k_part_bytes(KB, D, ASYM);
       pair_q(kbc);
       while (true) {
-        const int s0 = sidx, s1 = (sidx + 1 == ns) ? 0 : sidx + 1;
-        const int ka = __shfl_sync(0xffffffffu, pg, s0);
-        if (ka < 0) break;
-        const int kb = __shfl_sync(0xffffffffu, pg, s1);
-        wait_stage(s0);
-        if (kb >= 0) wait_stage(s1);
-        const uint8_t* sa = wptr + s0 * stage_bytes;
-        const uint8_t* sb = wptr + s1 * stage_bytes;
+        const int k = take();
+        if (k >= np) break;
+        const bool two = k + 1 < np;
+        const uint32_t q = __umulhi((uint32_t)k, ns_magic);  // k even, ns even: k+1 in si+1
+        const int si = k - (int)q * ns;
+        wait_page(k, si, q);
+        if (two) wait_page(k + 1, si + 1, q);
+        const uint8_t* sa = smem + si * stage_bytes;
+        const uint8_t* sb = sa + stage_bytes;
         if (ok) {
-          if (kb >= 0)
+          if (two)
             attend_pages<D, VB, true, KB>(SLd{sa}, SLd{sa + KP}, BLOCK, SLd{sb}, SLd{sb + KP},
                                           BLOCK, qw, A, sl, g, c);
           else
@@ -1048,29 +1063,24 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
                                           A, sl, g, c);
         }
         __syncwarp();
-        refill(s0, s1, kb >= 0);
-        sidx = (s1 + 1 == ns) ? 0 : s1 + 1;
+        refill(k, si, two);
       }
     });
   } else {
-    auto ready = [&](int k, int si) -> int32_t {  // entry of page k once its stage landed
-      if (k < 0) return -1;
-      const int32_t e = s_bt[k];
-      if (e == -1) return -1;
-      wait_stage(si);
-      return ok ? e : -1;
-    };
     while (true) {
-      const int s0 = sidx, s1 = (sidx + 1 == ns) ? 0 : sidx + 1;
-      const int ka = __shfl_sync(0xffffffffu, pg, s0);
-      if (ka < 0) break;
-      const int kb = __shfl_sync(0xffffffffu, pg, s1);
-      const int32_t ea = ready(ka, s0);
-      const int32_t eb = ready(kb, s1);
-      const uint8_t* sa = wptr + s0 * stage_bytes;
-      const uint8_t* sb = wptr + s1 * stage_bytes;
-      const int kba = ea != -1 ? bits_of_code(entry_fmt(ea) >> 2) : 0;
-      const int kbb = eb != -1 ? bits_of_code(entry_fmt(eb) >> 2) : 0;
+      const int k = take();
+      if (k >= np) break;
+      const bool two = k + 1 < np;
+      const uint32_t q = __umulhi((uint32_t)k, ns_magic);
+      const int si = k - (int)q * ns;
+      const int32_t ea = s_bt[k];
+      const int32_t eb = two ? s_bt[k + 1] : -1;
+      if (ea != -1) wait_page(k, si, q);
+      if (eb != -1) wait_page(k + 1, si + 1, q);
+      const uint8_t* sa = smem + si * stage_bytes;
+      const uint8_t* sb = sa + stage_bytes;
+      const int kba = ea != -1 && ok ? bits_of_code(entry_fmt(ea) >> 2) : 0;
+      const int kbb = eb != -1 && ok ? bits_of_code(entry_fmt(eb) >> 2) : 0;
       if (kba != 0 && kba == kbb) {  // both pages share a K width
         with_kbits(kba, [&](auto kbc) {
           constexpr int KB = decltype(kbc)::value;
@@ -1094,10 +1104,14 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
         }
       }
       __syncwarp();
-      refill(s0, s1, kb >= 0);
-      sidx = (s1 + 1 == ns) ? 0 : s1 + 1;
+      refill(k, si, two);
     }
   }
+  // Copies still in flight (pages no warp took after a wait gave up) land before
+  // the stage memory is reused: each stage waits, bounded, for its last copy.
+  __syncthreads();
+  if (tid < ns && s_issued[tid] >= 0)
+    mbar_wait(bar0 + 8 * tid, __umulhi((uint32_t)s_issued[tid], ns_magic) & 1u);
   __syncthreads();  // every stage drained before the stage memory is reused
 
   // ---- remove the V code bias: o_c = (o_c - vbias(c) * sum P') / vmul(c) ------------
@@ -1236,7 +1250,7 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
 template <int D, int VB, int PACK>
 cudaError_t launch_t(const DevState& st, int layer, int n_seqs, const int32_t* slots,
                      const __half* q, __half* o, int splits, const __half* knew,
-                     const __half* vnew, bool overlap, cudaStream_t s) {
+                     const __half* vnew, int overlap, cudaStream_t s) {
   using Cfg = AttnCfg<VB, PACK>;
   dim3 grid(splits * st.Hkv * n_seqs);
   if (knew && overlap) {  // programmatic dependent of the launch before it
@@ -1251,14 +1265,15 @@ cudaError_t launch_t(const DevState& st, int layer, int n_seqs, const int32_t* s
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, decode_attn_kernel<D, VB, true, PACK>, st, layer, slots, q,
-                              o, splits, knew, vnew, ATTN_LATE_BLOCKS);
+                              o, splits, knew, vnew, ATTN_LATE_BLOCKS,
+                              overlap == OVERLAP_DEPENDENT ? 1 : 0);
   }
   if (knew)
     decode_attn_kernel<D, VB, true, PACK><<<grid, Cfg::NT, Cfg::SMEM, s>>>(
-        st, layer, slots, q, o, splits, knew, vnew, 0);
+        st, layer, slots, q, o, splits, knew, vnew, 0, 0);
   else
     decode_attn_kernel<D, VB, false, PACK><<<grid, Cfg::NT, Cfg::SMEM, s>>>(
-        st, layer, slots, q, o, splits, nullptr, nullptr, 0);
+        st, layer, slots, q, o, splits, nullptr, nullptr, 0, 0);
   return cudaGetLastError();
 }
 
@@ -1314,9 +1329,9 @@ cudaError_t EKV_ATTN_FN(launch_decode_attn)(const DevState& st, int layer, int n
                                             const int32_t* slots, const __half* q, __half* o,
                                             int splits, int vb, int pack, cudaStream_t s,
                                             const __half* knew, const __half* vnew,
-                                            bool overlap) {
+                                            int overlap) {
   using Fn = cudaError_t (*)(const DevState&, int, int, const int32_t*, const __half*, __half*,
-                             int, const __half*, const __half*, bool, cudaStream_t);
+                             int, const __half*, const __half*, int, cudaStream_t);
   const int vi = vb == 2 ? 0 : vb == 4 ? 1 : vb == 8 ? 2 : 3;
   static const Fn tab[2][4] = {
       {launch_t<64, 2, 1>, launch_t<64, 4, 1>, launch_t<64, 8, 1>, launch_t<64, 16, 1>},

@@ -318,7 +318,7 @@ int ekv_decode_attn(ekv_cache* c, int32_t layer, int32_t n_seqs, const int32_t* 
 int ekv_append_decode_attn(ekv_cache* c, int32_t layer, int32_t n_seqs, const int32_t* seq_slots,
                            const void* k, const void* v, const void* q, void* o, int32_t flags,
                            void* stream) {
-  if (flags & ~EKV_AFTER_OTHER_LAYER) return EKV_EINVAL;
+  if (flags & ~(EKV_AFTER_OTHER_LAYER | EKV_AFTER_PRODUCER)) return EKV_EINVAL;
   if (!c || layer < 0 || layer >= c->st.L || n_seqs < 0 || n_seqs > c->st.S) return EKV_EINVAL;
   if (n_seqs == 0) return EKV_OK;
   if (!seq_slots || !k || !v || !q || !o) return EKV_EINVAL;
@@ -330,7 +330,9 @@ int ekv_append_decode_attn(ekv_cache* c, int32_t layer, int32_t n_seqs, const in
                                         splits, c->vbits[layer], attn_pack(c, n_seqs, c->vbits[layer]),
                                         as_stream(stream), static_cast<const __half*>(k),
                                         static_cast<const __half*>(v),
-                                        (flags & EKV_AFTER_OTHER_LAYER) != 0));
+                                        (flags & EKV_AFTER_PRODUCER) ? OVERLAP_DEPENDENT
+                                        : (flags & EKV_AFTER_OTHER_LAYER) ? OVERLAP_INDEPENDENT
+                                                                          : OVERLAP_NONE));
 }
 
 int ekv_canary_kl(ekv_cache* c, int32_t layer, int32_t n_seqs, const int32_t* seq_slots,

@@ -98,24 +98,28 @@ cudaError_t attn_init_asym(bool* pack2_ok);
 bool attn_pack2_ok();      // two half-size attention CTAs fit on an SM
 int attn_ctas_per_sm(int vb);  // resident decode-attention CTAs per SM for V width vb
 // With knew/vnew set ([n_seqs][Hkv][d] fp16 each) the launch first appends that
-// one token to every sequence (the fused decode step), then attends over it too;
-// `overlap` launches it as a programmatic dependent of the stream's previous
-// launch (which must be the fused step of another layer).
+// one token to every sequence (the fused decode step), then attends over it too.
+// `overlap` (fused step only) launches it as a programmatic dependent of the
+// stream's previous launch: OVERLAP_INDEPENDENT when that launch is the fused
+// step of another layer and writes none of this call's inputs (the launch waits
+// only before its writes), OVERLAP_DEPENDENT when it may write q, k and v (the
+// launch reads only this layer's cache state and the slot list before it waits).
 // `pack`: CTAs per SM (1, or 2 for launches with more units than SMs; see
 // attn_pack in the host).
+constexpr int OVERLAP_NONE = 0, OVERLAP_INDEPENDENT = 1, OVERLAP_DEPENDENT = 2;
 cudaError_t launch_decode_attn(const DevState& st, int layer, int n_seqs, const int32_t* slots,
                                const __half* q, __half* o, int splits, int vb, int pack,
                                cudaStream_t s, const __half* knew = nullptr,
-                               const __half* vnew = nullptr, bool overlap = false);
+                               const __half* vnew = nullptr, int overlap = OVERLAP_NONE);
 // The two page variants behind launch_decode_attn (st.asym picks one).
 cudaError_t launch_decode_attn_sym(const DevState& st, int layer, int n_seqs,
                                    const int32_t* slots, const __half* q, __half* o, int splits,
                                    int vb, int pack, cudaStream_t s, const __half* knew,
-                                   const __half* vnew, bool overlap);
+                                   const __half* vnew, int overlap);
 cudaError_t launch_decode_attn_asym(const DevState& st, int layer, int n_seqs,
                                     const int32_t* slots, const __half* q, __half* o, int splits,
                                     int vb, int pack, cudaStream_t s, const __half* knew,
-                                    const __half* vnew, bool overlap);
+                                    const __half* vnew, int overlap);
 cudaError_t canary_init();  // once per process, before any launch
 // Layers layer0 .. layer0+n_layers-1 in one launch; layer layer0+i reads its
 // queries at q + i * q_layer_stride and writes delta_out[i][3] (if not null).

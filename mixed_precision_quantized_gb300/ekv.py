@@ -17,7 +17,8 @@ from . import build as _build
 BITS = (2, 4, 8, 16)
 _CODE = {2: 0, 4: 1, 8: 2, 16: 3}
 NUM_FORMATS = 16
-AFTER_OTHER_LAYER = 1  # ekv_append_decode_attn flag
+AFTER_OTHER_LAYER = 1  # ekv_append_decode_attn flags
+AFTER_PRODUCER = 2
 DEBUG_WAIT_EXPIRY = 1  # ekv_debug_set knob
 
 
@@ -230,14 +231,18 @@ class Cache:
 
     def append_decode_attn(self, layer: int, seq_slots: torch.Tensor, k: torch.Tensor,
                            v: torch.Tensor, q: torch.Tensor, out: torch.Tensor | None = None,
-                           after_other_layer: bool = False, stream=None) -> torch.Tensor:
+                           after_other_layer: bool = False, after_producer: bool = False,
+                           stream=None) -> torch.Tensor:
         """One decode step of a layer in one launch: append one token (k, v of shape
         [n, 1, Hkv, d] or [n, Hkv, d]) to every sequence, then attend over it too.
         `after_other_layer`: the previous work on the stream is this call for
-        another layer (lets the launch overlap its start with that one's end)."""
+        another layer and writes none of this call's inputs; `after_producer`:
+        the previous work may write q, k, v (but not this layer's cache).  Either
+        lets the launch overlap its start with that work's end."""
         if out is None:
             out = torch.empty_like(q)
-        flags = AFTER_OTHER_LAYER if after_other_layer else 0
+        flags = ((AFTER_OTHER_LAYER if after_other_layer else 0) |
+                 (AFTER_PRODUCER if after_producer else 0))
         _check(lib().ekv_append_decode_attn(self._h, layer, seq_slots.numel(), _ptr(seq_slots),
                                             _ptr(k), _ptr(v), _ptr(q), _ptr(out), flags,
                                             _stream(stream)), "ekv_append_decode_attn")

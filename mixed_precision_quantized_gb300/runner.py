@@ -64,23 +64,32 @@ def prefill(cache: ekv.Cache, w: workloads.Workload, slots: torch.Tensor, device
 
 def decode_step(cache: ekv.Cache, w: workloads.Workload, slots: torch.Tensor, inp: Inputs,
                 i: int, out: list, fires: bool, delta_out: torch.Tensor | None = None,
-                fused: bool = False, combine=None, overlap: bool = True):
+                fused: bool = False, combine=None, overlap="dependent"):
     """One decode step over all layers; out[l] ([B,Hq,d]) receives each layer's O.
-    With `fused` each layer's append and attention run as one launch, each but the
-    first overlapping the previous layer's (`overlap`; valid here because a
-    layer's inputs do not come from the previous layer's output).  With
+    With `fused` each layer's append and attention run as one launch.  `overlap`
+    lets each launch start before the work before it has finished:
+    "dependent" (every layer; as in a model, where a layer's q, k, v come from
+    the previous layer's output: the launch streams pages early and reads them
+    after that work finishes), "independent" or True (every layer but the first,
+    reading its inputs early too: valid here only because the workload's inputs
+    are fresh draws, not the previous layer's output), or False/None (none).  With
     `combine` (several GPUs, each holding a shard of the batch) the canary
     readings, written to `delta_out` ([L, 3] fp32), are combined over the ranks
     by combine(delta_out) before the tier update."""
     if fires and combine is not None and delta_out is None:
         raise ValueError("combining readings over ranks needs delta_out")
-    for l in range(w.num_layers):
+    L = w.num_layers
+    for l in range(L):
         q, k, v = inp.layer(l, i)
         if fused:
-            # the previous launch is the fused step of layer l-1 unless this is
-            # the first layer
+            # independent: the previous launch is the fused step of layer l-1
+            # unless this is the first layer.  dependent: the previous launch must
+            # not append to this layer, so a one-layer workload (whose previous
+            # launch is this layer's own last step) does not overlap.
             cache.append_decode_attn(l, slots, k, v, q, out[l],
-                                     after_other_layer=overlap and l > 0)
+                                     after_other_layer=(overlap is True or
+                                                        overlap == "independent") and l > 0,
+                                     after_producer=overlap == "dependent" and L > 1)
         else:
             cache.append(l, slots, k, v)
             cache.decode_attn(l, slots, q, out[l])

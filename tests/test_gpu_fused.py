@@ -54,8 +54,12 @@ def _compare(a: ekv.Cache, b: ekv.Cache, w, slots_list):
                         f"layer {l} seq {s} head {h} block {j}: page bytes differ")
 
 
+@pytest.mark.parametrize("overlap", ["dependent", "independent", False])
 @pytest.mark.parametrize("wname", ["tiny", "d128_v4_batch3"])
-def test_fused_equals_separate(wname):
+def test_fused_equals_separate(wname, overlap):
+    """Each overlap mode of consecutive fused launches (a launch starting before
+    the previous layer's ends: reading q, k, v after it, or before it, or no
+    overlap) gives the separate calls' results."""
     if wname == "tiny":
         w = workloads.tiny().scaled(prefill=[29], steps=40)
     else:
@@ -74,7 +78,7 @@ def test_fused_equals_separate(wname):
                 for c in caches:
                     c.set_tiers([8 if kb != 8 else 2 for kb in w.k_bits_init])
             for c, o, fused in zip(caches, outs, (False, True)):
-                runner.decode_step(c, w, slots, inp, t, o, False, fused=fused)
+                runner.decode_step(c, w, slots, inp, t, o, False, fused=fused, overlap=overlap)
             for c in caches:
                 c.sync()
             for l in range(w.num_layers):
@@ -128,7 +132,7 @@ def test_fused_invalid_arguments_rejected_on_host():
         lib = ekv.lib()
         P = lambda t: ctypes.c_void_p(t.data_ptr())
         assert lib.ekv_append_decode_attn(cache.handle, 0, 1, P(slots), P(good), P(good), P(q),
-                                          P(q), 2, None) == 1     # unknown flag bit
+                                          P(q), 4, None) == 1     # unknown flag bit
         cache.append_decode_attn(0, slots[:0], good[:0], good[:0], q[:0])   # no-op
         cache.sync()
         assert cache.seq_len(0, 0) == 0
