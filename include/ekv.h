@@ -329,6 +329,16 @@ EKV_API int ekv_abs_percentile(const void* x, int64_t n_rows, int64_t row_stride
 /* Scratch bytes ekv_abs_percentile needs for n_groups groups (host only). */
 EKV_API int ekv_abs_percentile_scratch_bytes(int32_t n_groups, int64_t* out);
 
+/* The sums behind the Value score of the calibration ("Behavior-Guided KV-Cache
+ * Quantization", "K/V Role-Aware Low-Bit Quantization": Value candidates are
+ * scored by the perturbation of the attention output): over n fp16 elements,
+ * out[0] = sum (o_hat - o_ref)^2 and out[1] = sum o_ref^2, accumulated in fp64
+ * (the order of the additions varies between calls).  o_hat, o_ref dev fp16
+ * (2-byte aligned; may be NULL when n = 0); out host double[2]; scratch dev,
+ * 8-byte aligned, 16 bytes (caller-owned, overwritten).  Syncs stream. */
+EKV_API int ekv_output_error(const void* o_hat, const void* o_ref, int64_t n, double* out,
+                             void* scratch, void* stream);
+
 /* AutoK: the smallest number k of layers whose sensitivities, taken largest
  * first (equal values: lower index first), sum in fp64 to >= frac times the
  * sum of all n.  sensitivity host double[n] (finite, >= 0); 0 <= frac <= 1.

@@ -159,8 +159,6 @@ def calibrate(w: workloads.Workload, candidates=(1.0, 0.999, 0.99), frac: float 
                 vscore = [0.0] * len(candidates)
             else:                    # Value: attention output, 16-bit K, V at the layer's bits
                 ref.decode_attn(0, slots, Q, o)
-                o64 = o.double()
-                den = float((o64 ** 2).sum())
                 quant = one_layer(16, vb)
                 try:
                     vscore = []
@@ -168,7 +166,7 @@ def calibrate(w: workloads.Workload, candidates=(1.0, 0.999, 0.99), frac: float 
                         quant.set_clip(0, None, c.cpu())
                         fill(quant, ks, vs)
                         quant.decode_attn(0, slots, Q, oq)
-                        num = float(((oq.double() - o64) ** 2).sum())
+                        num, den = ekv.output_error(oq, o)      # fp64 sums on the GPU
                         vscore.append(num / den if den > 0 else 0.0)
                     quant.sync()
                 finally:

@@ -151,6 +151,30 @@ __global__ void select_pick_kernel(uint32_t* __restrict__ G, int n_groups, int p
   }
 }
 
+// Sums of (a - b)^2 and b^2 over n fp16 elements, in fp64: a grid-stride loop,
+// a warp reduction and one atomic add per warp into acc[2] (zeroed by the caller).
+__global__ void __launch_bounds__(256) output_error_kernel(const __half* __restrict__ a,
+                                                           const __half* __restrict__ b, int64_t n,
+                                                           double* __restrict__ acc) {
+  double e = 0.0, r = 0.0;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const double y = (double)__half2float(b[i]);
+    const double d = (double)__half2float(a[i]) - y;
+    e = fma(d, d, e);
+    r = fma(y, y, r);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    e += __shfl_xor_sync(0xffffffffu, e, off);
+    r += __shfl_xor_sync(0xffffffffu, r, off);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    atomicAdd(acc, e);
+    atomicAdd(acc + 1, r);
+  }
+}
+
 }  // namespace
 
 size_t abs_percentile_scratch_bytes(int n_groups) {
@@ -221,6 +245,31 @@ int ekv_abs_percentile(const void* x, int64_t n_rows, int64_t row_stride, int32_
                                static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? EKV_OK
              : EKV_ECUDA;
+}
+
+int ekv_output_error(const void* o_hat, const void* o_ref, int64_t n, double* out,
+                     void* scratch, void* stream) {
+  if (!out || !scratch || n < 0 || (n > 0 && (!o_hat || !o_ref)) ||
+      ((reinterpret_cast<uintptr_t>(o_hat) | reinterpret_cast<uintptr_t>(o_ref)) & 1) ||
+      (reinterpret_cast<uintptr_t>(scratch) & 7))
+    return EKV_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  double* acc = static_cast<double*>(scratch);
+  int dev = 0, num_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&num_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return EKV_ECUDA;
+  cudaError_t e = cudaMemsetAsync(acc, 0, 2 * sizeof(double), s);
+  if (e == cudaSuccess && n > 0) {
+    const int64_t blocks = std::min<int64_t>((n + 255) / 256, 4 * (int64_t)num_sm);
+    output_error_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const __half*>(o_hat),
+                                                          static_cast<const __half*>(o_ref), n,
+                                                          acc);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) e = cudaMemcpyAsync(out, acc, 2 * sizeof(double), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return e == cudaSuccess ? EKV_OK : EKV_ECUDA;
 }
 
 int ekv_autok(const double* sensitivity, int32_t n, double frac, int32_t* order_out,

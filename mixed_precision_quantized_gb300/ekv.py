@@ -102,6 +102,7 @@ _SIGS = {
                                           ctypes.c_int64, _P]),
     "ekv_abs_percentile_scratch_bytes": (ctypes.c_int, [_I32, _P]),
     "ekv_autok": (ctypes.c_int, [_P, _I32, ctypes.c_double, _P, _P]),
+    "ekv_output_error": (ctypes.c_int, [_P, _P, ctypes.c_int64, _P, _P, _P]),
 }
 EXPORTS = tuple(_SIGS)
 
@@ -413,6 +414,19 @@ def v_thresholds(v: torch.Tensor, q: float, stream=None) -> torch.Tensor:
     T, H, d = v.shape
     v = v.contiguous()
     return abs_percentile(v, q, T, H * d, H, d, d, stream=stream)
+
+
+def output_error(o_hat: torch.Tensor, o_ref: torch.Tensor, stream=None):
+    """(sum (o_hat - o_ref)^2, sum o_ref^2) over two fp16 CUDA tensors of one
+    shape, in fp64 on the GPU (ekv_output_error)."""
+    if o_hat.shape != o_ref.shape or o_hat.dtype != torch.float16 or o_ref.dtype != torch.float16:
+        raise TypeError("two fp16 tensors of one shape")
+    a, b = o_hat.contiguous(), o_ref.contiguous()
+    scratch = torch.empty(2, dtype=torch.float64, device=a.device)
+    out = (ctypes.c_double * 2)()
+    _check(lib().ekv_output_error(_ptr(a), _ptr(b), a.numel(), out, _ptr(scratch),
+                                  _stream(stream)), "ekv_output_error")
+    return out[0], out[1]
 
 
 def autok(sensitivity, frac: float):

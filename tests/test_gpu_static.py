@@ -193,3 +193,18 @@ def test_static_mode_decode_matches_oracle(fused):
         assert run.cache.state()["tiers"] == art.k_bits      # read-only: never fired
     finally:
         run.close()
+
+
+def test_output_error_sums_match_fp64():
+    """ekv_output_error: sum (a - b)^2 and sum b^2 of two fp16 tensors, fp64 on the
+    GPU, against numpy's fp64 sums (rounding order aside); empty input gives 0."""
+    g = torch.Generator().manual_seed(7)
+    for n in (1, 31, 1000, 70001):
+        a = torch.randn(n, generator=g).half()
+        b = (a.float() + 0.01 * torch.randn(n, generator=g)).half()
+        num, den = ekv.output_error(a.cuda(), b.cuda())
+        a64, b64 = a.double().numpy(), b.double().numpy()
+        assert num == pytest.approx(float(((a64 - b64) ** 2).sum()), rel=1e-12)
+        assert den == pytest.approx(float((b64 ** 2).sum()), rel=1e-12)
+    z = torch.zeros(0, dtype=torch.float16, device="cuda")
+    assert ekv.output_error(z, z) == (0.0, 0.0)
