@@ -91,6 +91,8 @@ def parse():
                         "a model), reading them before it too (independent), or not at all")
     p.add_argument("--no-short", action="store_true",
                    help="skip the extra 32K-context figure (Qwen2.5-14B shape) of the default run")
+    p.add_argument("--context", type=int, default=0,
+                   help="cached tokens per sequence before the timed steps (0: the workload's)")
     p.add_argument("--force-kbits", type=int, default=0,
                    help="create the cache with every layer at this K width and keep the canary "
                         "off (per-width measurement at the workload's context)")
@@ -340,6 +342,8 @@ def main():
     if a.force_kbits:
         w = w.scaled(k_bits_init=[a.force_kbits] * w.num_layers, canary_period=0,
                      name=f"{w.name}_k{a.force_kbits}")
+    if a.context:
+        w = w.scaled(prefill=[a.context] * w.batch, name=f"{w.name}_ctx{a.context}")
     if a.asym:
         if a.static:
             raise SystemExit("the static artifact's thresholds cap the symmetric quantizer")

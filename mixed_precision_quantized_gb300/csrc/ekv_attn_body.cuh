@@ -742,17 +742,77 @@ __device__ __noinline__ void merge_parts(float* __restrict__ part_acc, float* __
   }
 }
 
+// Merge `count` (<= ATTN_GROUP) split partials at slots pbase + j into O, in one
+// round of loads: every thread loads its slots of all the partials, while warp w
+// < MAX_G loads head w's (max, sum) pairs, reduces them across its lanes and
+// leaves the partials' weights 2^(m_j - M) and 1 / L in shared memory
+// (s_f[j][head], s_inv[head]); after one barrier each thread folds its slots.
+// Called by every thread of the CTA (NT >= MAX_G * 32).
+template <int D, int NT>
+__device__ __noinline__ void merge_final(const float* __restrict__ part_acc,
+                                         const float* __restrict__ part_ml, size_t pbase,
+                                         int count, int G, int tid, __half* __restrict__ orow,
+                                         float (*s_f)[MAX_G], float* s_inv) {
+  constexpr int SLOTS = MergeShape<D, NT>::SLOTS, PTS = MergeShape<D, NT>::PTS;
+  static_assert(NT >= MAX_G * 32, "one warp per head of the group");
+  const int hd = slot_head<D>(tid);
+  const bool active = hd < G;
+  float a[ATTN_GROUP][PTS];
+#pragma unroll
+  for (int j = 0; j < ATTN_GROUP; ++j)
+#pragma unroll
+    for (int k = 0; k < PTS; ++k)
+      a[j][k] = active && j < count && tid + k * NT < SLOTS
+                    ? __ldcg(part_acc + (pbase + j) * SLOTS + tid + k * NT)
+                    : 0.f;
+  const int w = tid >> 5, lane = tid & 31;
+  if (w < G) {
+    float2 ml = make_float2(-CUDART_INF_F, 0.f);
+    if (lane < count)
+      ml = __ldcg(reinterpret_cast<const float2*>(part_ml + ((pbase + lane) * MAX_G + w) * 2));
+    float M = ml.x;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float f = ml.x == -CUDART_INF_F ? 0.f : exp2f(ml.x - M);
+    float L = f * ml.y;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    if (lane < count) s_f[lane][w] = f;
+    if (lane == 0) s_inv[w] = L > 0.f ? 1.f / L : 0.f;
+  }
+  __syncthreads();
+  if (!active) return;
+  float acc[PTS];
+#pragma unroll
+  for (int k = 0; k < PTS; ++k) acc[k] = 0.f;
+#pragma unroll
+  for (int j = 0; j < ATTN_GROUP; ++j) {
+    if (j < count) {
+      const float f = s_f[j][hd];
+#pragma unroll
+      for (int k = 0; k < PTS; ++k) acc[k] = fmaf(f, a[j][k], acc[k]);
+    }
+  }
+  const float inv = s_inv[hd];
+#pragma unroll
+  for (int k = 0; k < PTS; ++k)
+    if (tid + k * NT < SLOTS)
+      orow[hd * D + slot_ch<D>(tid + k * NT)] = __float2half_rn(acc[k] * inv);
+}
+
 // Arrive on a merge ticket that `expected` CTAs share: publish this CTA's
 // writes, count it in, and return (to every thread) whether it came last.  The
 // last one resets the ticket for the next launch and sees all the others' writes.
+// The barrier orders every thread's writes before thread 0's release; thread 0's
+// acquire and the second barrier order the other CTAs' writes before every
+// thread's reads (which go through L2: __ldcg).
 __device__ __forceinline__ bool last_arrival(int* ticket, int expected, int tid, int* s_flag) {
   __syncthreads();
   if (tid == 0) {
-    __threadfence();
-    const int t = atomicAdd(ticket, 1);
+    int t;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(t) : "l"(ticket) : "memory");
     *s_flag = (t == expected - 1);
-    if (*s_flag) *ticket = 0;
-    __threadfence();
+    if (*s_flag) *ticket = 0;  // the next launch's arrivals come after this launch ends
   }
   __syncthreads();
   return *s_flag != 0;
@@ -824,6 +884,7 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   __shared__ __align__(8) uint64_t bars[RING_MAX];
   __shared__ int s_issued[RING_MAX];  // last page copied into each stage (-1: none)
   __shared__ float sm_m[NW][MAX_G], sm_l[NW][MAX_G], sm_f[NW][MAX_G], sm_ml[MAX_G][2];
+  __shared__ float sm_mf[ATTN_GROUP][MAX_G], sm_inv[MAX_G];  // final merge weights
   __shared__ int s_next, s_last;
   int32_t* s_bt = reinterpret_cast<int32_t*>(smem + Cfg::STAGE_SMEM);
 
@@ -878,6 +939,26 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
 
   const int32_t* bt = st.bt + lsh_index(st, layer, slot_ok ? slot : 0, h) * st.maxblk;
   const __half* stg = st.staging + lsh_index(st, layer, slot_ok ? slot : 0, h) * (BLOCK * D);
+  // Stage ring of the CTA: ns stages (even, at most RING_MAX) sized for the
+  // widest page this layer has admitted so far.  Page j of the split always goes
+  // to stage j % ns; its copy is the (j / ns)-th completion of that stage's
+  // barrier.  Pages 0 .. ns-1 are copied at the start; the warp that finishes
+  // page j copies page j + ns into the stage it just emptied, and records it in
+  // s_issued, which the warp that takes page j + ns reads before it waits (so
+  // it never waits on a barrier phase other than its page's).
+  const int kmax = max(2, st.kmax[layer]);
+  const int stage_bytes = (page_bytes(kmax, VB, D, ASYM) + 127) & ~127;
+  const int ns = min(RING_MAX, Cfg::STAGE_SMEM / stage_bytes) & ~1;
+  // j / ns as a multiply-high (exact for j < 2^32 / ns^2, far above the pages of a split)
+  const uint32_t ns_magic = (uint32_t)((0x100000000ull + ns - 1) / ns);
+  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
+  const uint32_t bar0 = (uint32_t)__cvta_generic_to_shared(&bars[0]);
+  if (tid < ns) {
+    mbar_init(bar0 + 8 * tid, 1);
+    s_issued[tid] = -1;
+  }
+  if (tid == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+
   // Copy the split's page-table entries and check whether every pipelined page
   // has one format (the common case: a layer whose tier did not change over the
   // split's range); such a split runs a loop specialized to that format.
@@ -913,25 +994,6 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   A.z0 = A.z1 = 0.f;
   const float sl = st.scale_log2;
 
-  // Stage ring of the CTA: ns stages (even, at most RING_MAX) sized for the
-  // widest page this layer has admitted so far.  Page j of the split always goes
-  // to stage j % ns; its copy is the (j / ns)-th completion of that stage's
-  // barrier.  Pages 0 .. ns-1 are copied at the start; the warp that finishes
-  // page j copies page j + ns into the stage it just emptied, and records it in
-  // s_issued, which the warp that takes page j + ns reads before it waits (so
-  // it never waits on a barrier phase other than its page's).
-  const int kmax = max(2, st.kmax[layer]);
-  const int stage_bytes = (page_bytes(kmax, VB, D, ASYM) + 127) & ~127;
-  const int ns = min(RING_MAX, Cfg::STAGE_SMEM / stage_bytes) & ~1;
-  // j / ns as a multiply-high (exact for j < 2^32 / ns^2, far above the pages of a split)
-  const uint32_t ns_magic = (uint32_t)((0x100000000ull + ns - 1) / ns);
-  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
-  const uint32_t bar0 = (uint32_t)__cvta_generic_to_shared(&bars[0]);
-  if (tid < ns) {
-    mbar_init(bar0 + 8 * tid, 1);
-    s_issued[tid] = -1;
-  }
-  if (tid == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   // page-table copy, counter and barriers ready
   const bool uniform = !__syncthreads_or(mixed) && np > 0 && e_first != -1;
 
@@ -1217,16 +1279,24 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
       }
     }
   }
-  if constexpr (FUSED) {
-    if (app && tid == 0) {  // every CTA of this sequence has read the old length
-      int* tk = st.append_ticket + ls_index(st, layer, slot);
-      if (atomicAdd(tk, 1) == splits * st.Hkv - 1) {
-        st.len[ls_index(st, layer, slot)] = T;
-        *tk = 0;
+  // The new length is published once every CTA of the sequence has read the old
+  // one: one arrival per KV head, from its only CTA or from the CTA that merges
+  // its splits (all of which have arrived by then).
+  auto publish_length = [&]() {
+    if constexpr (FUSED) {
+      if (app && tid == 0) {
+        int* tk = st.append_ticket + ls_index(st, layer, slot);
+        if (atomicAdd(tk, 1) == st.Hkv - 1) {
+          st.len[ls_index(st, layer, slot)] = T;
+          *tk = 0;
+        }
       }
     }
+  };
+  if (splits == 1) {
+    publish_length();
+    return;
   }
-  if (splits == 1) return;
 
   // ---- merge of the splits ------------------------------------------------------------
   // Up to ATTN_GROUP splits: the last CTA to finish merges them all into O.  More:
@@ -1238,13 +1308,18 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   int* tk = st.attn_ticket + ((size_t)z * st.Hkv + h) * ATTN_TICKETS;
   if (!last_arrival(tk + 1 + grp, gsize, tid, &s_last)) return;
   if (ngrp == 1) {
-    merge_parts<D, NT>(st.attn_acc, st.attn_ml, pbase, 0, 1, splits, G, tid, orow, 0);
+    if constexpr (MergeShape<D, NT>::PTS <= 2)  // every partial's slots fit the registers
+      merge_final<D, NT>(st.attn_acc, st.attn_ml, pbase, splits, G, tid, orow, sm_mf, sm_inv);
+    else
+      merge_parts<D, NT>(st.attn_acc, st.attn_ml, pbase, 0, 1, splits, G, tid, orow, 0);
+    publish_length();
     return;
   }
   merge_parts<D, NT>(st.attn_acc, st.attn_ml, pbase, grp * ATTN_GROUP, 1, gsize, G, tid,
                      nullptr, pbase + grp * ATTN_GROUP);
   if (!last_arrival(tk, ngrp, tid, &s_last)) return;
   merge_parts<D, NT>(st.attn_acc, st.attn_ml, pbase, 0, ATTN_GROUP, ngrp, G, tid, orow, 0);
+  publish_length();
 }
 
 template <int D, int VB, int PACK>
