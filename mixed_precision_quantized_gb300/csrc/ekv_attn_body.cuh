@@ -633,6 +633,10 @@ template <int N>
 struct KBits {
   static constexpr int value = N;
 };
+template <bool B>
+struct BoolC {
+  static constexpr bool value = B;
+};
 // Call f(KBits<kb>{}) with the page K width as a compile-time constant.
 template <class F>
 __device__ __forceinline__ void with_kbits(int kb, F&& f) {
@@ -948,7 +952,17 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   // it never waits on a barrier phase other than its page's).
   const int kmax = max(2, st.kmax[layer]);
   const int stage_bytes = (page_bytes(kmax, VB, D, ASYM) + 127) & ~127;
-  const int ns = min(RING_MAX, Cfg::STAGE_SMEM / stage_bytes) & ~1;
+  // Static assignment when the ring holds two pairs per warp or more: warp w
+  // takes pairs w, w + NW, ... and ns is a multiple of 2 NW, so page j + ns is
+  // the same warp's page as page j and each warp refills only its own stages
+  // (no shared counter, no issue check).  Larger pages keep the deeper ring and
+  // a shared counter (any warp takes the next pair).
+  const int ns_fit = min(RING_MAX, Cfg::STAGE_SMEM / stage_bytes) & ~1;
+  const int ns_static = ns_fit / (2 * NW) * (2 * NW);
+  // (Launches of two CTAs per SM keep the shared counter: with static assignment
+  // their batched, two-wave launches ran up to milliseconds long.)
+  const bool stat = PACK == 1 && ns_static >= 4 * NW;
+  const int ns = stat ? ns_static : ns_fit;
   // j / ns as a multiply-high (exact for j < 2^32 / ns^2, far above the pages of a split)
   const uint32_t ns_magic = (uint32_t)((0x100000000ull + ns - 1) / ns);
   const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
@@ -1094,8 +1108,15 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
     const int j = k + ns + lane;
     if (lane < (two ? 2 : 1) && j < np && ok) issue(j, si + lane);
   };
+  // The first page of this warp's next pair (np once there are none left).
+  int next_static = 2 * warp;
   auto take = [&]() {
     int k = np;
+    if (stat) {
+      if (ok) k = next_static;
+      next_static += 2 * NW;
+      return k;
+    }
     if (lane == 0 && ok) k = atomicAdd(&s_next, 2);
     return __shfl_sync(0xffffffffu, k, 0);
   };
@@ -1106,27 +1127,49 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
       constexpr int KB = decltype(kbc)::value;
       constexpr int KP = k_part_bytes(KB, D, ASYM);
       pair_q(kbc);
-      while (true) {
-        const int k = take();
-        if (k >= np) break;
-        const bool two = k + 1 < np;
-        const uint32_t q = __umulhi((uint32_t)k, ns_magic);  // k even, ns even: k+1 in si+1
-        const int si = k - (int)q * ns;
-        wait_page(k, si, q);
-        if (two) wait_page(k + 1, si + 1, q);
-        const uint8_t* sa = smem + si * stage_bytes;
-        const uint8_t* sb = sa + stage_bytes;
-        if (ok) {
-          if (two)
-            attend_pages<D, VB, true, KB>(SLd{sa}, SLd{sa + KP}, BLOCK, SLd{sb}, SLd{sb + KP},
-                                          BLOCK, qw, A, sl, g, c);
+      // One loop per assignment, chosen once (the static one waits on its own
+      // stages' barriers directly: their copies were issued before its wait).
+      auto loop = [&](auto stat_c) {
+        constexpr bool STAT = decltype(stat_c)::value;
+        for (int it = 0;; ++it) {
+          int k;
+          if constexpr (STAT)
+            k = ok ? 2 * (warp + NW * it) : np;
           else
-            attend_pages<D, VB, true, KB>(SLd{sa}, SLd{sa + KP}, BLOCK, SLd{sa}, SLd{sa}, 0, qw,
-                                          A, sl, g, c);
+            k = take();
+          if (k >= np) break;
+          const bool two = k + 1 < np;
+          const uint32_t q = __umulhi((uint32_t)k, ns_magic);  // k even, ns even: k+1 in si+1
+          const int si = k - (int)q * ns;
+          if constexpr (STAT) {
+            const bool l0 = mbar_wait(bar0 + 8 * si, q & 1u);
+            const bool l1 = !two || mbar_wait(bar0 + 8 * (si + 1), q & 1u);
+            if (!__all_sync(0xffffffffu, l0 && l1 && !expire) && ok) {
+              ok = false;
+              if (lane == 0) set_error(st, EKV_ETIMEOUT);
+            }
+          } else {
+            wait_page(k, si, q);
+            if (two) wait_page(k + 1, si + 1, q);
+          }
+          const uint8_t* sa = smem + si * stage_bytes;
+          const uint8_t* sb = sa + stage_bytes;
+          if (ok) {
+            if (two)
+              attend_pages<D, VB, true, KB>(SLd{sa}, SLd{sa + KP}, BLOCK, SLd{sb},
+                                            SLd{sb + KP}, BLOCK, qw, A, sl, g, c);
+            else
+              attend_pages<D, VB, true, KB>(SLd{sa}, SLd{sa + KP}, BLOCK, SLd{sa}, SLd{sa}, 0,
+                                            qw, A, sl, g, c);
+          }
+          __syncwarp();
+          refill(k, si, two);
         }
-        __syncwarp();
-        refill(k, si, two);
-      }
+      };
+      if (stat)
+        loop(BoolC<true>{});
+      else
+        loop(BoolC<false>{});
     });
   } else {
     while (true) {
@@ -1172,8 +1215,9 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   // Copies still in flight (pages no warp took after a wait gave up) land before
   // the stage memory is reused: each stage waits, bounded, for its last copy.
   __syncthreads();
-  if (tid < ns && s_issued[tid] >= 0)
-    mbar_wait(bar0 + 8 * tid, __umulhi((uint32_t)s_issued[tid], ns_magic) & 1u);
+  if (tid < ns && s_issued[tid] >= 0 &&
+      !mbar_wait(bar0 + 8 * tid, __umulhi((uint32_t)s_issued[tid], ns_magic) & 1u))
+    set_error(st, EKV_ETIMEOUT);
   __syncthreads();  // every stage drained before the stage memory is reused
 
   // ---- remove the V code bias: o_c = (o_c - vbias(c) * sum P') / vmul(c) ------------
