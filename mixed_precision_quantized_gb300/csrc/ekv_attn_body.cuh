@@ -165,8 +165,20 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
           "r"(dst), "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
-// Poll the stage barrier for the given phase; false if the bound ran out.
+// Poll the stage barrier for the given phase; false if the bound ran out.  A
+// non-blocking test first: a landed page (the common case) costs less that way
+// than a first try_wait.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  {
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; "
+        "selp.u32 %0, 1, 0, p; }"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
   for (int i = 0; i < WAIT_LIMIT; ++i) {
     uint32_t done;
     asm volatile(
@@ -1011,6 +1023,10 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   // page-table copy, counter and barriers ready
   const bool uniform = !__syncthreads_or(mixed) && np > 0 && e_first != -1;
 
+  // A uniform split under static assignment gives each stage pair one barrier
+  // (pages k, k + 1 of a warp's pair, k even, in stages si, si + 1 signal
+  // barrier si / 2), so its warps wait once per pair.
+  const bool pairb = stat && uniform;
   // The pool of a uniform split's pages (its only format).
   const int fmt_u = uniform ? entry_fmt(e_first) : 0;
   const uint32_t bytes_u = (uint32_t)st.pool_page_bytes[fmt_u];
@@ -1018,6 +1034,9 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   // One thread: page k into stage si (= k % ns).  A page whose table entry is
   // missing (-1) is flagged and not copied, but still completes its barrier
   // phase (an arrival with no bytes), so the stage's phase count stays k / ns.
+  // With pair barriers the thread of the even page arrives expecting the bytes
+  // of both (the odd page's copy may land first: the transaction count dips
+  // below zero, but the phase cannot complete before that arrival).
   auto issue = [&](int k, int si) {
     const int32_t e = s_bt[k];
     uint32_t bytes = 0;
@@ -1031,9 +1050,13 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
       src = st.pool_base[fmt] + (size_t)entry_idx(e) * bytes;
     }
     if (src) {
+      const uint32_t bar = bar0 + 8 * (pairb ? si >> 1 : si);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_expect_tx(bar0 + 8 * si, bytes);
-      bulk_g2s(sbase + si * stage_bytes, src, bytes, bar0 + 8 * si);
+      if (!pairb)
+        mbar_expect_tx(bar, bytes);
+      else if (!(si & 1))
+        mbar_expect_tx(bar, k + 1 < np ? 2 * bytes : bytes);
+      bulk_g2s(sbase + si * stage_bytes, src, bytes, bar);
     } else {
       set_error(st, EKV_ESTATE);
       mbar_arrive(bar0 + 8 * si);
@@ -1141,10 +1164,9 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
           const bool two = k + 1 < np;
           const uint32_t q = __umulhi((uint32_t)k, ns_magic);  // k even, ns even: k+1 in si+1
           const int si = k - (int)q * ns;
-          if constexpr (STAT) {
-            const bool l0 = mbar_wait(bar0 + 8 * si, q & 1u);
-            const bool l1 = !two || mbar_wait(bar0 + 8 * (si + 1), q & 1u);
-            if (!__all_sync(0xffffffffu, l0 && l1 && !expire) && ok) {
+          if constexpr (STAT) {  // pair barrier (a uniform split with static assignment)
+            const bool l0 = mbar_wait(bar0 + 8 * (si >> 1), q & 1u);
+            if (!__all_sync(0xffffffffu, l0 && !expire) && ok) {
               ok = false;
               if (lane == 0) set_error(st, EKV_ETIMEOUT);
             }
@@ -1215,8 +1237,11 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   // Copies still in flight (pages no warp took after a wait gave up) land before
   // the stage memory is reused: each stage waits, bounded, for its last copy.
   __syncthreads();
-  if (tid < ns && s_issued[tid] >= 0 &&
-      !mbar_wait(bar0 + 8 * tid, __umulhi((uint32_t)s_issued[tid], ns_magic) & 1u))
+  // (With pair barriers only the even stage of a pair is checked: it holds the
+  // pair's latest page, and the odd stage's may be a round older.)
+  if (tid < ns && !(pairb && (tid & 1)) && s_issued[tid] >= 0 &&
+      !mbar_wait(bar0 + 8 * (pairb ? tid >> 1 : tid),
+                 __umulhi((uint32_t)s_issued[tid], ns_magic) & 1u))
     set_error(st, EKV_ETIMEOUT);
   __syncthreads();  // every stage drained before the stage memory is reused
 
