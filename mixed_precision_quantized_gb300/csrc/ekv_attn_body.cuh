@@ -896,7 +896,13 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   using Cfg = AttnCfg<VB, PACK>;
   constexpr int NW = Cfg::NW, NT = Cfg::NT;
   constexpr int KCH = D / 4, KW = KCH / 2, NMT = D / 16;
+  static_assert(NT >= RING_MAX, "the first ring fill gives each thread one page at most");
   extern __shared__ __align__(128) uint8_t smem[];
+  // A programmatic dependent of this launch (the next layer's) may start on an
+  // SM as soon as this launch's CTA there exits: it reads only its own layer's
+  // cache state before its own griddepcontrol.wait, and every CTA of this launch
+  // is resident by the time all have triggered, so none waits for an SM.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ __align__(8) uint64_t bars[RING_MAX];
   __shared__ int s_issued[RING_MAX];  // last page copied into each stage (-1: none)
   __shared__ float sm_m[NW][MAX_G], sm_l[NW][MAX_G], sm_f[NW][MAX_G], sm_ml[MAX_G][2];
@@ -1063,7 +1069,13 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
     }
     *reinterpret_cast<volatile int*>(&s_issued[si]) = k;
   };
-  if (tid < ns && tid < np) issue(tid, tid);
+  // The first ns pages, spread over all warps (warp w copies pages w, w + NW, ...;
+  // 32 NW >= RING_MAX): a warp's copy instructions go out one issuing lane after
+  // another, so a few lanes in each warp finish sooner than 32 lanes in two.
+  {
+    const int p = warp + NW * lane;
+    if (p < ns && p < np) issue(p, p);
+  }
 
   // Dependent-inputs overlap: everything above read only this layer's cache
   // state (length, page table, pages) and the slot list; the launch before may
@@ -1311,10 +1323,8 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
 
   // Launched as a programmatic dependent, everything above overlapped the end of
   // the launch before it in the stream, which may still be using the shared
-  // split scratch and O: wait for it here, then let the next launch start its
-  // own page reads on the SMs as they free up.  Both are no-ops otherwise.
+  // split scratch and O: wait for it here (a no-op otherwise).
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const size_t pbase = ((size_t)z * st.Hkv + h) * splits;
   const size_t pid = pbase + split;
