@@ -901,8 +901,11 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   // A programmatic dependent of this launch (the next layer's) may start on an
   // SM as soon as this launch's CTA there exits: it reads only its own layer's
   // cache state before its own griddepcontrol.wait, and every CTA of this launch
-  // is resident by the time all have triggered, so none waits for an SM.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // is resident by the time all have triggered, so none waits for an SM.  (Two
+  // CTAs per SM trigger after their loop instead: started early, the next
+  // launch's CTAs would fill the SMs in block order and undo the pairing of a
+  // long and a short sequence on each SM that a longest-first slot list gives.)
+  if constexpr (PACK == 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ __align__(8) uint64_t bars[RING_MAX];
   __shared__ int s_issued[RING_MAX];  // last page copied into each stage (-1: none)
   __shared__ float sm_m[NW][MAX_G], sm_l[NW][MAX_G], sm_f[NW][MAX_G], sm_ml[MAX_G][2];
@@ -1325,6 +1328,7 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   // the launch before it in the stream, which may still be using the shared
   // split scratch and O: wait for it here (a no-op otherwise).
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if constexpr (PACK != 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const size_t pbase = ((size_t)z * st.Hkv + h) * splits;
   const size_t pid = pbase + split;
