@@ -46,8 +46,8 @@ L2_BYTES = 129 * 2 ** 20        # GB300 L2
 # the 2-layer case of the 70B workload (the same per-launch work as one layer of
 # the full workload), valid only for the kernel source it was taken on: any
 # change to that source reports null until re-captured.
-TRAFFIC_BYTES = 156.88e6
-TRAFFIC_SOURCE_SHA = "c669c72814fd79d6"
+TRAFFIC_BYTES = 157.13e6
+TRAFFIC_SOURCE_SHA = "0d48819ec964c337"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 

@@ -31,7 +31,7 @@ constexpr int SEL_THREADS = 256;
 constexpr int SEL_WARPS = SEL_THREADS / 32;
 constexpr int SEL_TILE = 32;   // groups per CTA when each row holds one element of a group
 constexpr int SEL_BINS = 256;  // first pass (key bits 14..7); the second uses 128 (bits 6..0)
-constexpr int SEL_UNROLL = 16;  // rows in flight per warp (column groups)
+constexpr int SEL_UNROLL = 32;  // rows in flight per warp (column groups)
 constexpr int SEL_RU = 4;       // rows in flight per warp (segment groups)
 
 __device__ __forceinline__ uint32_t mag_key(__half x) { return __half_as_ushort(x) & 0x7fffu; }
