@@ -47,7 +47,7 @@ L2_BYTES = 129 * 2 ** 20        # GB300 L2
 # the full workload), valid only for the kernel source it was taken on: any
 # change to that source reports null until re-captured.
 TRAFFIC_BYTES = 157.13e6
-TRAFFIC_SOURCE_SHA = "0d48819ec964c337"
+TRAFFIC_SOURCE_SHA = "f1986ffba0a2f29a"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 

@@ -14,12 +14,13 @@
 // conditional speed trade-off").
 //
 // Work split: grid (split, kv_head, seq), one CTA per SM.  A split owns a
-// contiguous range of 16-token blocks; its warps take the range's pages two at a
-// time from a counter in shared memory, so the work evens out between warps that
-// the SM's scheduler serves unequally.  Each warp runs its own pipeline of
-// shared-memory stages: one TMA bulk copy (cp.async.bulk, completion counted on
-// the stage's mbarrier) per page, `ns` pages ahead of the page being computed, so
-// the warp's HBM requests stay in flight while it computes.  Per page the warp
+// contiguous range of 16-token blocks, streamed through one ring of `ns`
+// shared-memory stages per CTA: one TMA bulk copy (cp.async.bulk, completion
+// counted on an mbarrier) per page, page j in stage j mod ns, refilled with page
+// j + ns by the warp that computed page j, so the CTA's HBM requests stay in
+// flight while its warps compute.  Warps take pages two at a time: statically
+// (warp w the pairs w, w + NW, ...) when the ring holds two pairs per warp or
+// more, else from a counter in shared memory.  Per page the warp
 //   1. unpacks K codes to exact fp16 integers in registers (PRMT/LOP3/HFMA2)
 //      and folds the per-channel K scales into Q as an fp16 hi + lo pair,
 //   2. S^T[16 tokens x 8 heads] = K . Q^T with mma.sync m16n8k16 (fp32 acc):
@@ -31,8 +32,9 @@
 // straight from global memory, first, by one warp.  Warps merge in shared
 // memory; splits write (max, sum, numerator) partials and the last CTA of a
 // (sequence, KV head) — found with an atomic ticket, no waiting — merges them by
-// log-sum-exp.  Which warp takes which page depends on timing, so the fp32
-// summation order (not the set of terms) varies from launch to launch.
+// log-sum-exp.  With static assignment the fp32 summation order is fixed; with
+// the shared counter, which warp takes which page depends on timing, so the
+// order (not the set of terms) varies from launch to launch.
 //
 // Asymmetric pages (KIVI-style: xhat = u * s + z, unsigned codes u, fp16 zero
 // point z per group, "EchoKV: watching a language model decide its own
@@ -67,12 +69,10 @@ constexpr int RING_MAX = 96;             // stages of a CTA's page ring at most 
 constexpr int ATTN_LATE_BLOCKS = 80;
 // PACK CTAs per SM (1, or 2 when a launch has more (sequence, KV head) units
 // than SMs: then every CTA is resident at once and each SM holds a long and a
-// short one instead of running a second wave).  A CTA's warps share the
-// split's pages through a counter in shared memory, so a warp that runs ahead
-// takes more pages.  Stage memory: 200 KB per SM, split evenly between the
-// warps (quantized V: 16 warps, five K4/V4 pages each, registers capped at
-// 128; FP16 V pages are 3.5x larger and need more registers: 12 warps).  After
-// the stages come the split's page-table entries.
+// short one instead of running a second wave).  Stage memory: 200 KB per SM
+// for the CTA's page ring (quantized V: 16 warps, registers capped at 128;
+// FP16 V pages are 3.5x larger and need more registers: 12 warps).  After the
+// stages come the split's page-table entries.
 template <int VB, int PACK = 1>
 struct AttnCfg {
   static constexpr int NW = (VB == 16 ? 12 : 16) / PACK;
@@ -1117,9 +1117,8 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
     }
   }
 
-  // Warps take the split's pages two at a time from the shared counter.  After
-  // a wait gives up the warp takes nothing more; the copies still in flight are
-  // waited for (bounded) before the CTA reuses the stage memory.
+  // After a wait gives up the warp takes nothing more; the copies still in
+  // flight are waited for (bounded) before the CTA reuses the stage memory.
   bool ok = true;
   // (With the test hook dbg_wait_expiry set, a wait that saw its copy land still
   // reports expiry, so the timeout path runs with no copy left in flight.)
