@@ -67,7 +67,7 @@ typedef enum ekv_status {
   EKV_ENOMEM = 2,         /* allocation failed, or a page pool ran empty on the device  */
   EKV_ECUDA = 3,          /* a CUDA call or kernel launch failed                        */
   EKV_ETIMEOUT = 4,       /* a bounded device-side wait gave up                         */
-  EKV_EUNSUPPORTED = 5,   /* valid request outside what this build implements           */
+  EKV_EUNSUPPORTED = 5,   /* valid request outside what this library implements         */
   EKV_ESTATE = 6          /* device detected an inconsistent state (capacity, entries)  */
 } ekv_status;
 
