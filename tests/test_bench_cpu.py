@@ -44,3 +44,23 @@ def test_reference_arm_prints_one_contract_line():
 ])
 def test_amortized_region(fired, steps, period, want):
     assert bench.amortized_region(1.0, fired, 0.1, steps, period) == pytest.approx(want)
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """Launched as two ranks (gloo on the host), rank 0 alone times the oracle and
+    prints the line; the other rank exits 0 without work."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+                        "--nproc-per-node", "2", "--master-addr", "127.0.0.1",
+                        "--master-port", str(port), "bench.py", "--impl", "reference",
+                        "--gpus", "2", "--workload", "tiny", "--steps", "1", "--warmup", "1"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=600,
+                       env={**os.environ, "CUDA_VISIBLE_DEVICES": ""})
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0
