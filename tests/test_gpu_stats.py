@@ -11,7 +11,7 @@ import pytest
 import torch
 
 from mixed_precision_quantized_gb300 import build, ekv, workloads
-from oracle import decoder, pages
+from oracle import decoder, pages, sizes
 
 from gpu_harness import Run
 
@@ -56,7 +56,10 @@ def expected(ref: decoder.ReferenceRun, layers, asym=False) -> dict:
            "open_rows": openr.tolist(), "tokens": tokens}
     if tokens:
         kb, vb = kbits / tokens, vbits / tokens
-        out.update(k_bits=kb, v_bits=vb, cost_vs_c0=(kb + vb) / 32, page_bytes=float(nbytes),
+        # KV-Kaizen's c(a) of one token of one layer and KV head (K and V at
+        # their mean stored bits, no RoPE rank truncation) over its C0
+        cost = (sizes.kaizen_cost(d, 0, kb) + sizes.kaizen_cost(d, 0, vb)) / sizes.kaizen_c0(1, 1, d)
+        out.update(k_bits=kb, v_bits=vb, cost_vs_c0=cost, page_bytes=float(nbytes),
                    fp16_bytes=tokens * d * 4.0, saved_vs_fp16=1 - nbytes / (tokens * d * 4.0))
     return out
 
