@@ -1,6 +1,6 @@
 """A model of the decode-attention kernel's page-ring synchronization, checked on
-CPU under random schedules (the pool has no race detector for device code, so
-the protocol itself is checked here).
+CPU under random schedules: the protocol itself, independent of any device
+tool.
 
 What is modelled, as `csrc/ekv_attn_body.cuh` does it for one CTA:
 - ns stages (even); page j of the split always goes to stage j mod ns and is
