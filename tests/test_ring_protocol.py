@@ -18,7 +18,9 @@ What is modelled, as `csrc/ekv_attn_body.cuh` does it for one CTA:
   after the next pair's wait.
 - Dynamic assignment: one barrier per stage, a shared counter hands out
   pairs, a warp first waits for the stage's issue record to show its page,
-  then for the barrier, and refills right after computing.
+  then for the barrier, and refills right after computing.  A split with
+  mixed page formats runs the same per-stage waits with the static pairs
+  when the ring allows them ("static, mixed").
 - The first fill (pages 0 .. ns-1, issuing threads in any order) and the
   drain (each stage, or each pair's even stage, waits for its last copy).
 
@@ -60,12 +62,13 @@ class Barrier:
 class Ring:
     BYTES = 1
 
-    def __init__(self, np_, nw, ns, static, rng):
-        assert ns % 2 == 0
-        if static:
+    def __init__(self, np_, nw, ns, mode, rng):
+        assert ns % 2 == 0 and mode in ("static", "static_mixed", "dynamic")
+        if mode != "dynamic":
             assert ns % (2 * nw) == 0 and ns >= 4 * nw
-        self.np, self.nw, self.ns, self.static, self.rng = np_, nw, ns, static, rng
-        self.pairb = static
+        self.np, self.nw, self.ns, self.mode, self.rng = np_, nw, ns, mode, rng
+        self.static = mode == "static"
+        self.pairb = self.static
         nb = ns // 2 if self.pairb else ns
         self.bars = [Barrier() for _ in range(nb)]
         self.stage = [None] * ns          # page whose copy landed in the stage
@@ -126,9 +129,14 @@ class Ring:
                     self.compute(k + 1, si + 1)
                 it += 1
         else:
+            it = 0
             while True:
-                k = self.counter
-                self.counter += 2
+                if self.mode == "static_mixed":
+                    k = 2 * (w + self.nw * it)
+                    it += 1
+                else:
+                    k = self.counter
+                    self.counter += 2
                 if k >= np_:
                     break
                 two = k + 1 < np_
@@ -190,12 +198,12 @@ CASES = [  # (pages, warps, stages)
 
 
 @pytest.mark.parametrize("np_, nw, ns", CASES)
-@pytest.mark.parametrize("static", [True, False])
-def test_ring_protocol_random_schedules(np_, nw, ns, static):
-    if static and not (ns % (2 * nw) == 0 and ns >= 4 * nw):
+@pytest.mark.parametrize("mode", ["static", "static_mixed", "dynamic"])
+def test_ring_protocol_random_schedules(np_, nw, ns, mode):
+    if mode != "dynamic" and not (ns % (2 * nw) == 0 and ns >= 4 * nw):
         pytest.skip("static assignment needs a ring of two pairs per warp or more")
     for seed in range(40):
-        Ring(np_, nw, ns, static, random.Random(seed)).run()
+        Ring(np_, nw, ns, mode, random.Random(seed)).run()
 
 
 def test_drain_of_odd_stage_would_wait_forever():
@@ -203,7 +211,7 @@ def test_drain_of_odd_stage_would_wait_forever():
     barriers, the odd stage of a pair may hold an older page than the even one
     (an odd page count), and waiting on that older page's phase parity never
     succeeds once the newer phase has completed."""
-    r = Ring(3 * 16 + 1, 4, 16, True, random.Random(0))   # 49 pages: page 48 alone
+    r = Ring(3 * 16 + 1, 4, 16, "static", random.Random(0))   # 49 pages: page 48 alone
     r.run()
     odd = 48 % 16 + 1                 # the odd stage beside page 48
     assert r.issued[odd] == 33        # a round older than page 48
