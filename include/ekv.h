@@ -206,10 +206,11 @@ EKV_API int ekv_decode_attn(ekv_cache* cache, int32_t layer, int32_t n_seqs, con
  *           only seq_slots and this layer's lengths, page table and pages; it
  *           waits before its first read of q, k or v and before any write.
  *           Both bits: as EKV_AFTER_PRODUCER.  Any other bit: EKV_EINVAL.
- *           (Independently of these flags, a decode-attention launch of one CTA
- *           per SM lets its own programmatic dependents start as soon as all its
- *           CTAs run: work launched after it with programmatic stream
- *           serialization must wait for it (griddepcontrol.wait, i.e.
+ *           (A decode-attention launch lets its own programmatic dependents
+ *           start once every CTA has passed its wait for the work before it:
+ *           with EKV_AFTER_PRODUCER near its start, otherwise before it writes
+ *           o.  Work launched after it with programmatic stream serialization
+ *           must wait for it (griddepcontrol.wait, i.e.
  *           cudaGridDependencySynchronize) before reading o or any state of this
  *           handle.  Work launched without that attribute sees ordinary stream
  *           order.)

@@ -898,14 +898,6 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   constexpr int KCH = D / 4, KW = KCH / 2, NMT = D / 16;
   static_assert(NT >= RING_MAX, "the first ring fill gives each thread one page at most");
   extern __shared__ __align__(128) uint8_t smem[];
-  // A programmatic dependent of this launch (the next layer's) may start on an
-  // SM as soon as this launch's CTA there exits: it reads only its own layer's
-  // cache state before its own griddepcontrol.wait, and every CTA of this launch
-  // is resident by the time all have triggered, so none waits for an SM.  (Two
-  // CTAs per SM trigger after their loop instead: started early, the next
-  // launch's CTAs would fill the SMs in block order and undo the pairing of a
-  // long and a short sequence on each SM that a longest-first slot list gives.)
-  if constexpr (PACK == 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ __align__(8) uint64_t bars[RING_MAX];
   __shared__ int s_issued[RING_MAX];  // last page copied into each stage (-1: none)
   __shared__ float sm_m[NW][MAX_G], sm_l[NW][MAX_G], sm_f[NW][MAX_G], sm_ml[MAX_G][2];
@@ -1083,7 +1075,18 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
   // Dependent-inputs overlap: everything above read only this layer's cache
   // state (length, page table, pages) and the slot list; the launch before may
   // still be writing Q, K and V, so wait for it before the first read of them.
-  if (dep_inputs) asm volatile("griddepcontrol.wait;" ::: "memory");
+  // Once it is complete, a programmatic dependent of this launch (the next
+  // layer's) may start on an SM as soon as this launch's CTA there exits: it
+  // reads only its own layer's state before its own wait, and that layer's last
+  // writer is at least the launch before this one, now complete.  (A launch
+  // triggers only after its own wait, so at most two are ever in flight.  Two
+  // CTAs per SM trigger after their loop instead: started early, the next
+  // launch's CTAs would fill the SMs in block order and undo the pairing of a
+  // long and a short sequence on each SM that a longest-first slot list gives.)
+  if (dep_inputs) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if constexpr (PACK == 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  }
   load_q<D>(qrow, g < G, 0, qw);
 
   // The last block first (with the fused append, after appending to it), while
@@ -1340,9 +1343,10 @@ decode_attn_kernel(DevState st, int layer, const int32_t* __restrict__ slots,
 
   // Launched as a programmatic dependent, everything above overlapped the end of
   // the launch before it in the stream, which may still be using the shared
-  // split scratch and O: wait for it here (a no-op otherwise).
+  // split scratch and O: wait for it here (a no-op otherwise), then let the next
+  // launch start (unless the early wait above already did).
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if constexpr (PACK != 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (!(PACK == 1 && dep_inputs)) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const size_t pbase = ((size_t)z * st.Hkv + h) * splits;
   const size_t pid = pbase + split;
