@@ -256,6 +256,20 @@ def cpu_baseline(w, sample_layers: int, device, steps: int = 1, warmup: int = 1)
             "host": os.uname().machine, "nproc": os.cpu_count()}
 
 
+def traffic_field(workload_name: str, full_size: bool, fused: bool, asym: bool,
+                  static: bool) -> tuple:
+    """(DRAM bytes per launch, note): the captured figure when this run is the
+    captured configuration on the captured kernel source, else None and why."""
+    if not (workload_name == "llama70b_128k" and full_size and fused and not asym
+            and not static):
+        return None, "captured for the default 70B/128K fused step only"
+    if attn_source_sha() != TRAFFIC_SOURCE_SHA:
+        return None, (f"the last capture ({TRAFFIC_BYTES / 1e6:.1f} MB per launch) was taken "
+                      f"on kernel source {TRAFFIC_SOURCE_SHA}, not on this one "
+                      f"({attn_source_sha()})")
+    return TRAFFIC_BYTES, "dram__bytes_read.sum + dram__bytes_write.sum of one ncu capture"
+
+
 def amortized_region(t_region: float, fired: int, canary_s: float, steps: int,
                      period: int) -> float:
     """A timed region's time with the canary at its 1-in-`period` share: the
@@ -792,6 +806,7 @@ def main():
     peak, peak_kind = peaks()
     achieved = bytes_per_launch / attn_avg_s / 1e9 if attn_avg_s else None
     step_bytes = sum(layer_bytes)
+    traffic = traffic_field(w.name, not a.layers, fused, a.asym, bool(a.static))
     line = {
         "metric": METRIC,
         "value": rate(B * K, tA),
@@ -850,10 +865,8 @@ def main():
         "prefill_s": prefill_s,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak if achieved else None,
-                     "traffic": (TRAFFIC_BYTES if attn_source_sha() == TRAFFIC_SOURCE_SHA
-                                 and w.name == "llama70b_128k" and not a.layers and fused
-                                 and not a.asym and not a.static
-                                 else None),
+                     "traffic": traffic[0],
+                     "traffic_note": traffic[1],
                      "traffic_unit": "bytes per launch",
                      "kernel": ("decode_attn_kernel (fused append + attention)" if fused
                                 else "decode_attn_kernel"), "peak_kind": peak_kind,

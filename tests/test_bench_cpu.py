@@ -64,3 +64,18 @@ def test_reference_arm_under_torchrun_prints_once():
     assert len(lines) == 1, r.stdout
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["value"] > 0
+
+
+def test_traffic_field_only_for_the_captured_kernel_and_step(monkeypatch):
+    monkeypatch.setattr(bench, "TRAFFIC_SOURCE_SHA", bench.attn_source_sha())
+    assert bench.traffic_field("llama70b_128k", True, True, False, False)[0] == bench.TRAFFIC_BYTES
+    for args in (("qwen14b_32k", True, True, False, False),
+                 ("llama70b_128k", False, True, False, False),   # --layers
+                 ("llama70b_128k", True, False, False, False),   # separate calls
+                 ("llama70b_128k", True, True, True, False),     # asymmetric pages
+                 ("llama70b_128k", True, True, False, True)):    # static artifact
+        value, note = bench.traffic_field(*args)
+        assert value is None and note
+    monkeypatch.setattr(bench, "TRAFFIC_SOURCE_SHA", "0" * 16)
+    value, note = bench.traffic_field("llama70b_128k", True, True, False, False)
+    assert value is None and "0" * 16 in note and bench.attn_source_sha() in note
